@@ -1,0 +1,187 @@
+"""CPU fp64 oracle of the causal GQA attention step (qkv split, Q/K RMSNorm,
+RoPE, KV append, causal grouped-query attention).
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / reference leg of ``bench.py`` may import this package.  The
+product path never imports it and shares no code with it; the arithmetic
+lives in ``oracle.c`` (plain C, fp64, OpenMP over rows) and is described, with
+the passages it follows, in that file's header.
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+(brute force from the teaching snippet, closed forms, torch's ``rms_norm``,
+the complex form of RoPE, invariants).  The RoPE pairing convention itself
+(rotate-half) is a reading the pages leave open: parity unpinned for that
+choice, pinned for everything given it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_D = ctypes.c_double
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so with gcc (IEEE fp64, no contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".{os.getpid()}.tmp"
+        subprocess.check_call([
+            "gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math", "-std=c11",
+            "-shared", "-fPIC", "-o", tmp, _SRC, "-lm",
+        ])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        lib.oracle_bf16_round.restype = ctypes.c_uint16
+        lib.oracle_bf16_round.argtypes = [_D]
+        lib.oracle_rmsnorm.restype = None
+        lib.oracle_rmsnorm.argtypes = [_P, _P, ctypes.c_int, _D, _P]
+        lib.oracle_rope.restype = None
+        lib.oracle_rope.argtypes = [_P, ctypes.c_int, _D, _D]
+        lib.oracle_prologue.restype = ctypes.c_int
+        lib.oracle_prologue.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, _D, _D,
+            _P, _I64, _P, _P, ctypes.c_int, _P, _P, _P, _P, _I64, _P, _P, _I64, _P, _P, _P]
+        lib.oracle_attention.restype = None
+        lib.oracle_attention.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P, _P,
+            _I64, _P, _P, _P, _P]
+        lib.oracle_num_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(_P)
+
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> contiguous uint16 array of its bits (a copy)."""
+    assert t.dtype == torch.bfloat16
+    return np.array(t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16), copy=True)
+
+
+def bits_to_bf16(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+
+def bf16_round(x: float) -> int:
+    """Bits of the bf16 nearest to ``x`` (ties to even)."""
+    return int(_load().oracle_bf16_round(float(x)))
+
+
+def rmsnorm(x, w, eps: float) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    y = np.empty_like(x)
+    _load().oracle_rmsnorm(_ptr(x), _ptr(w), x.shape[-1], float(eps), _ptr(y))
+    return y
+
+
+def rope(x, pos: float, theta: float) -> np.ndarray:
+    y = np.array(x, dtype=np.float64, copy=True)
+    _load().oracle_rope(_ptr(y), y.shape[-1], float(pos), float(theta))
+    return y
+
+
+def prologue(cfg: dict, inputs: dict, q_rows=None):
+    """Steps 1-4.  Returns (k_cache, v_cache, q, bad) where the caches are new
+    bf16 tensors (the inputs are not modified), q is fp64 ``[N, Hq, D]`` (or
+    ``[R, D]`` for the (token, head) pairs in ``q_rows``), and ``bad`` counts
+    requests whose cache region is too small (they write nothing)."""
+    lib = _load()
+    Hq, Hkv, D = cfg["num_q_heads"], cfg["num_kv_heads"], cfg["head_dim"]
+    assert D <= 256 and D % 2 == 0 and Hq % Hkv == 0
+    qkv = _bits(inputs["qkv"])
+    N = qkv.shape[0]
+    kc = _bits(inputs["k_cache"])
+    vc = _bits(inputs["v_cache"])
+    qw, kw = _bits(inputs["q_norm_w"]), _bits(inputs["k_norm_w"])
+    cu = np.ascontiguousarray(inputs["cu_seqlens"].numpy().astype(np.int32))
+    cl = np.ascontiguousarray(inputs["cache_lens"].numpy().astype(np.int32))
+    sb = np.ascontiguousarray(inputs["slot_base"].numpy().astype(np.int64))
+    cap = np.ascontiguousarray(inputs["slot_capacity"].numpy().astype(np.int32))
+    B = cl.shape[0]
+    if q_rows is None:
+        nq = -1
+        q = np.zeros((N, Hq, D), dtype=np.float64)
+        qt = qh = np.zeros(1, dtype=np.int32)
+    else:
+        rows = np.ascontiguousarray(np.asarray(q_rows, dtype=np.int32).reshape(-1, 2))
+        nq = rows.shape[0]
+        qt = np.ascontiguousarray(rows[:, 0])
+        qh = np.ascontiguousarray(rows[:, 1])
+        q = np.zeros((nq, D), dtype=np.float64)
+    bad = lib.oracle_prologue(Hq, Hkv, D, float(cfg["rms_eps"]), float(cfg["rope_theta"]),
+                              _ptr(qkv), N, _ptr(qw), _ptr(kw), B, _ptr(cu), _ptr(cl), _ptr(sb),
+                              _ptr(cap), kc.shape[0], _ptr(kc), _ptr(vc), nq, _ptr(qt), _ptr(qh),
+                              _ptr(q))
+    return bits_to_bf16(kc), bits_to_bf16(vc), q, bad
+
+
+def attention(cfg: dict, k_cache: torch.Tensor, v_cache: torch.Tensor, inputs: dict,
+              rows, q: np.ndarray) -> np.ndarray:
+    """Step 5 for the (token, head) pairs ``rows`` ([R, 2]) with their fp64
+    queries ``q`` ([R, D]).  Returns fp64 ``[R, D]``."""
+    lib = _load()
+    Hq, Hkv, D = cfg["num_q_heads"], cfg["num_kv_heads"], cfg["head_dim"]
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
+    R = rows.shape[0]
+    tok = np.ascontiguousarray(rows[:, 0])
+    head = np.ascontiguousarray(rows[:, 1])
+    q = np.ascontiguousarray(q, dtype=np.float64).reshape(R, D)
+    kc, vc = _bits(k_cache), _bits(v_cache)
+    cu = np.ascontiguousarray(inputs["cu_seqlens"].numpy().astype(np.int32))
+    cl = np.ascontiguousarray(inputs["cache_lens"].numpy().astype(np.int32))
+    sb = np.ascontiguousarray(inputs["slot_base"].numpy().astype(np.int64))
+    out = np.zeros((R, D), dtype=np.float64)
+    lib.oracle_attention(Hq, Hkv, D, _ptr(kc), _ptr(vc), cl.shape[0], _ptr(cu), _ptr(cl), _ptr(sb),
+                         R, _ptr(tok), _ptr(head), _ptr(q), _ptr(out))
+    return out
+
+
+def all_rows(num_tokens: int, num_q_heads: int) -> np.ndarray:
+    t = np.repeat(np.arange(num_tokens, dtype=np.int32), num_q_heads)
+    h = np.tile(np.arange(num_q_heads, dtype=np.int32), num_tokens)
+    return np.stack([t, h], axis=1)
+
+
+def step(cfg: dict, inputs: dict, rows=None):
+    """The whole step: prologue then attention for ``rows`` (default: every
+    (token, head) pair, in [N, Hq] order).  Returns a dict with the updated
+    caches, the rows and the fp64 outputs ``[R, D]``."""
+    N = inputs["qkv"].shape[0]
+    if rows is None:
+        rows = all_rows(N, cfg["num_q_heads"])
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
+    kc, vc, q, bad = prologue(cfg, inputs, q_rows=rows)
+    out = attention(cfg, kc, vc, inputs, rows, q)
+    return {"k_cache": kc, "v_cache": vc, "rows": rows, "out": out, "q": q, "bad": bad}
+
+
+def cfg_of(w) -> dict:
+    """The per-call configuration of a workload (plain dict)."""
+    return {"num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "rms_eps": w.rms_eps, "rope_theta": w.rope_theta}

@@ -1,0 +1,225 @@
+/*
+ * CPU oracle of the per-layer causal grouped-query attention step.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the smoke check and the timed CPU
+ * baseline of the benchmark load this library.  It shares no code, header,
+ * table or constant with the CUDA path and never calls it.
+ *
+ * It computes the plain definition of the step in fp64, one (token, head)
+ * row at a time, with no blocking, fusion or online softmax:
+ *
+ *   1. split the packed qkv row into Q, K and V heads
+ *      (zero-to-sglang Ch.3 code walkthrough, section 3.3; transformer-basics
+ *      "Attention calculation: part 1": [1,12,4096] -> [1,12,32,128]);
+ *   2. RMSNorm over each Q and K head's last dimension with a learned weight
+ *      (code walkthrough section 3.3; part 1's q_norm / k_norm after .view);
+ *   3. RoPE on Q and K at each token's position (concept chapter section 2.2
+ *      and its section 2.6 table; the RoFormer paper they cite), V untouched;
+ *   4. append K (rounded once to bf16) and V (bit copy) to the cache
+ *      (transformer-basics "Prefill vs Decode": DynamicCache.update, 0 -> 12 -> 13);
+ *   5. causal GQA: query head h reads KV head h / (Hq/Hkv) (repeat_interleave),
+ *      scores q.k / sqrt(D), future keys excluded, softmax, weighted sum of V
+ *      (code walkthrough section 3.3 teaching snippet; transformer-basics
+ *      "Attention calculation: part 1", scaling = head_dim ** -0.5).
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *   - RMSNorm: y = w * x / sqrt(mean(x^2) + eps);
+ *   - RoPE: rotate-half pairing (i, i + D/2), frequency theta^(-2i/D),
+ *     rotation [[cos, -sin], [sin, cos]] applied to (x_i, x_{i+D/2});
+ *     the pairing convention is "parity unpinned": the pages fix no pairing;
+ *   - norm before RoPE; position of new token j of request b is c_b + j;
+ *   - Q stays in fp64; K is rounded to bf16 (round to nearest even) once,
+ *     when it is written to the cache; softmax and P.V in fp64.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static double bf16_bits_to_double(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* Round a double to the nearest bf16 (ties to even) directly, without an
+ * intermediate float rounding: scale the significand so that the last kept
+ * bit is the unit, round with nearbyint (the default rounding mode is
+ * round-to-nearest-even), scale back.  The result is exactly representable in
+ * float, so the final conversion and bit extraction are exact. */
+uint16_t oracle_bf16_round(double x) {
+  if (isnan(x)) return 0x7FC0;
+  uint16_t sign = signbit(x) ? 0x8000 : 0;
+  double a = fabs(x);
+  if (a == 0.0) return sign;
+  if (isinf(a)) return sign | 0x7F80;
+  int e;
+  double m = frexp(a, &e); /* a = m * 2^e, m in [0.5, 1) */
+  /* normal bf16 keeps 8 significant bits; below 2^-126 the quantum is 2^-133 */
+  int shift = (e >= -125) ? 8 : e + 133;
+  double r = nearbyint(ldexp(m, shift));
+  double y = ldexp(r, e - shift);
+  if (y >= ldexp(1.0, 128)) return sign | 0x7F80;
+  float f = (float)y;
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return sign | (uint16_t)(u >> 16);
+}
+
+/* Weighted RMSNorm of one head vector (step 2). */
+void oracle_rmsnorm(const double* x, const double* w, int D, double eps, double* y) {
+  double ss = 0.0;
+  for (int i = 0; i < D; ++i) ss += x[i] * x[i];
+  double inv = 1.0 / sqrt(ss / (double)D + eps);
+  for (int i = 0; i < D; ++i) y[i] = w[i] * (x[i] * inv);
+}
+
+/* RoPE of one head vector at position pos, in place (step 3). */
+void oracle_rope(double* x, int D, double pos, double theta) {
+  int half = D / 2;
+  for (int i = 0; i < half; ++i) {
+    double freq = pow(theta, -2.0 * (double)i / (double)D);
+    double a = pos * freq;
+    double c = cos(a), s = sin(a);
+    double x1 = x[i], x2 = x[i + half];
+    x[i] = x1 * c - x2 * s;
+    x[i + half] = x2 * c + x1 * s;
+  }
+}
+
+static int find_request(const int32_t* cu, int B, int64_t t) {
+  int lo = 0, hi = B; /* cu[lo] <= t < cu[hi] */
+  while (hi - lo > 1) {
+    int mid = (lo + hi) / 2;
+    if (cu[mid] <= t) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+static void load_head(const uint16_t* row, int64_t col0, int D, double* out) {
+  for (int i = 0; i < D; ++i) out[i] = bf16_bits_to_double(row[col0 + i]);
+}
+
+/*
+ * Steps 1-4 for all N tokens.  The cache (k_cache, v_cache: bf16 bits
+ * [num_slots, Hkv, D]) is updated in place: token j of request b goes to slot
+ * slot_base[b] + cache_lens[b] + j.  Q rows (normed, rotated, fp64) are written
+ * to q_out: all N*Hq rows as [N, Hq, D] when nq < 0, otherwise the nq rows
+ * (q_tok[r], q_head[r]) as [nq, D].  Returns the number of requests whose
+ * region cannot hold cache_lens + new tokens (those write nothing).
+ */
+int oracle_prologue(int Hq, int Hkv, int D, double eps, double theta,
+                    const uint16_t* qkv, int64_t N, const uint16_t* q_norm_w,
+                    const uint16_t* k_norm_w, int B, const int32_t* cu_seqlens,
+                    const int32_t* cache_lens, const int64_t* slot_base,
+                    const int32_t* slot_capacity, int64_t num_slots, uint16_t* k_cache,
+                    uint16_t* v_cache, int64_t nq, const int32_t* q_tok,
+                    const int32_t* q_head, double* q_out) {
+  const int64_t W = (int64_t)(Hq + 2 * Hkv) * D;
+  double* qw = malloc(sizeof(double) * D);
+  double* kw = malloc(sizeof(double) * D);
+  load_head(q_norm_w, 0, D, qw);
+  load_head(k_norm_w, 0, D, kw);
+  int bad = 0;
+  for (int b = 0; b < B; ++b) {
+    int64_t n = cu_seqlens[b + 1] - cu_seqlens[b];
+    int64_t end = (int64_t)cache_lens[b] + n;
+    if (n < 0 || end > slot_capacity[b] || slot_base[b] < 0 || slot_base[b] + end > num_slots) {
+      ++bad;
+      continue;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < n; ++j) {
+      int64_t t = cu_seqlens[b] + j;
+      double pos = (double)cache_lens[b] + (double)j;
+      int64_t slot = slot_base[b] + cache_lens[b] + j;
+      const uint16_t* row = qkv + t * W;
+      double x[256], y[256];
+      for (int kh = 0; kh < Hkv; ++kh) {
+        load_head(row, (int64_t)(Hq + kh) * D, D, x);
+        oracle_rmsnorm(x, kw, D, eps, y);
+        oracle_rope(y, D, pos, theta);
+        uint16_t* kd = k_cache + (slot * Hkv + kh) * D;
+        uint16_t* vd = v_cache + (slot * Hkv + kh) * D;
+        const uint16_t* vs = row + (int64_t)(Hq + Hkv + kh) * D;
+        for (int i = 0; i < D; ++i) {
+          kd[i] = oracle_bf16_round(y[i]);
+          vd[i] = vs[i];
+        }
+      }
+    }
+  }
+  int64_t rows = nq < 0 ? N * Hq : nq;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    int64_t t = nq < 0 ? r / Hq : q_tok[r];
+    int h = nq < 0 ? (int)(r % Hq) : q_head[r];
+    int b = find_request(cu_seqlens, B, t);
+    double pos = (double)cache_lens[b] + (double)(t - cu_seqlens[b]);
+    double x[256];
+    load_head(qkv + t * W, (int64_t)h * D, D, x);
+    oracle_rmsnorm(x, qw, D, eps, q_out + r * D);
+    oracle_rope(q_out + r * D, D, pos, theta);
+  }
+  free(qw);
+  free(kw);
+  return bad;
+}
+
+/*
+ * Step 5 for nrows (token, head) rows: out[r] = softmax(q_r . K^T / sqrt(D)) V
+ * over the keys at positions 0 .. c_b + j of the row's request (the query's
+ * own key included; later keys excluded), read from the cache.
+ */
+void oracle_attention(int Hq, int Hkv, int D, const uint16_t* k_cache, const uint16_t* v_cache,
+                      int B, const int32_t* cu_seqlens, const int32_t* cache_lens,
+                      const int64_t* slot_base, int64_t nrows, const int32_t* tok,
+                      const int32_t* head, const double* q, double* out) {
+  const int G = Hq / Hkv;
+  const double scale = 1.0 / sqrt((double)D);
+#pragma omp parallel for schedule(dynamic, 4)
+  for (int64_t r = 0; r < nrows; ++r) {
+    int64_t t = tok[r];
+    int h = head[r];
+    int b = find_request(cu_seqlens, B, t);
+    int64_t pos = (int64_t)cache_lens[b] + (t - cu_seqlens[b]);
+    int kvh = h / G;
+    int64_t nkeys = pos + 1;
+    double* s = malloc(sizeof(double) * (size_t)nkeys);
+    const double* qr = q + r * D;
+    for (int64_t u = 0; u < nkeys; ++u) {
+      const uint16_t* kr = k_cache + ((slot_base[b] + u) * Hkv + kvh) * D;
+      double acc = 0.0;
+      for (int i = 0; i < D; ++i) acc += qr[i] * bf16_bits_to_double(kr[i]);
+      s[u] = acc * scale;
+    }
+    /* softmax(s) = exp(s - max) / sum exp(s - max): the shift leaves it unchanged */
+    double m = -INFINITY;
+    for (int64_t u = 0; u < nkeys; ++u) m = s[u] > m ? s[u] : m;
+    double z = 0.0;
+    for (int64_t u = 0; u < nkeys; ++u) {
+      s[u] = exp(s[u] - m);
+      z += s[u];
+    }
+    double* o = out + r * D;
+    for (int i = 0; i < D; ++i) o[i] = 0.0;
+    for (int64_t u = 0; u < nkeys; ++u) {
+      double p = s[u] / z;
+      const uint16_t* vr = v_cache + ((slot_base[b] + u) * Hkv + kvh) * D;
+      for (int i = 0; i < D; ++i) o[i] += p * bf16_bits_to_double(vr[i]);
+    }
+    free(s);
+  }
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
