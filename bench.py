@@ -1,0 +1,458 @@
+#!/usr/bin/env python3
+"""Benchmark of the causal GQA attention step on GB300.
+
+One step = the whole path for one packed batch: K/V split + RMSNorm + RoPE +
+cache append (kv_append kernel) and causal GQA attention with fused Q
+RMSNorm + RoPE (prefill kernel; split-KV + combine for decode).
+
+Headline (``value``): prefill attention TFLOP/s on the Qwen3-4B-shaped
+prefill (8 packed sequences, lengths U[256, 2048], Hq 32 / Hkv 8 / D 128).
+FLOPs = 4 * D * Hq * (unmasked query-key pairs, diagonal included).
+The decode half of the metric (KV-read GB/s on 64 requests with cached
+lengths U[512, 8192]) is measured in the same run and reported under
+``decode``.  Inputs are seeded synthetic bf16 tensors resident in HBM; L2 is
+flushed (a 256 MiB write) before every timed step, outside the timed events.
+
+``--impl reference`` times the CPU fp64 oracle on the host cores instead
+(a bounded sample of the same workload per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill attn TFLOP/s & decode KV-read GB/s on 1 GB300, % of roofline"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen3_4b_prefill_8seq_U256_2048")
+    ap.add_argument("--decode-workload", default="decode_b64_cache_U512_8192")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode measurement")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU oracle sample budget")
+    return ap.parse_args()
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------- work counts
+def prefill_flops(w, lo=0, hi=None) -> float:
+    return 4.0 * w.head_dim * w.num_q_heads * w.attended_pairs(lo, hi)
+
+
+def decode_bytes(w, lo=0, hi=None) -> float:
+    """Algorithmic HBM bytes of the decode requests [lo, hi): cache read
+    (K and V of the c_b cached entries), the new token's qkv row, the K/V
+    append and the output row."""
+    hi = w.batch if hi is None else hi
+    D, Hq, Hkv = w.head_dim, w.num_q_heads, w.num_kv_heads
+    total = 0
+    for c in w.cache_lens[lo:hi]:
+        total += 2 * c * Hkv * D * 2 + w.qkv_width * 2 + 2 * Hkv * D * 2 + Hq * D * 2
+    return float(total)
+
+
+def source_sha(*names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "causal_gqa_attention_qkv_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def recorded_traffic(kernel: str, sha: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summaries, if
+    they were taken on the current source (same sha); else None."""
+    pat = re.compile(r"traffic_per_launch\s+" + re.escape(kernel) + r"\s+(\d+)\s+sha=(\w+)")
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    for fn in sorted(os.listdir(pdir)):
+        if not fn.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(pdir, fn)) as f:
+            for m in pat.finditer(f.read()):
+                if m.group(2) == sha:
+                    return int(m.group(1))
+    return None
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]),
+                             "power": float(parts[3]) if parts[3] not in ("[N/A]", "") else None,
+                             "hw_slowdown": parts[5] == "Active", "hw_thermal_slowdown": parts[6] == "Active",
+                             "sw_thermal_slowdown": parts[7] == "Active", "sw_power_cap": parts[8] == "Active"})
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        reasons = sorted({k for r in rows for k in ("hw_slowdown", "hw_thermal_slowdown",
+                                                    "sw_thermal_slowdown", "sw_power_cap") if r[k]})
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- our arm
+def env_rank():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+class Timed:
+    """Issues one step of a packed workload as append/attend launch groups,
+    with CUDA events on the launching stream between them."""
+
+    def __init__(self, ds, torch):
+        from causal_gqa_attention_qkv_gb300 import attn
+        self.ds, self.torch, self.attn = ds, torch, attn
+
+    def launches_per_step(self) -> int:
+        return self.ds.launches()
+
+    def run(self, ev):
+        """ev: list of 5 events: start, after prefill append, after prefill
+        attention, after decode append, after decode attention."""
+        ds, attn = self.ds, self.attn
+        n = ds.n_prefill_tokens
+        ev[0].record()
+        if ds.kv_prefill is not None:
+            attn.kv_append(ds.cfg, ds.qkv[:n], ds.k_norm_w, ds.cu_seqlens, ds.kv_prefill, ds.workspace)
+            ev[1].record()
+            attn.prefill_attend(ds.cfg, ds.qkv[:n], ds.q_norm_w, ds.cu_seqlens, ds.max_seqlen,
+                                ds.kv_prefill, ds.out[:n], ds.workspace)
+            ev[2].record()
+        else:
+            ev[1].record()
+            ev[2].record()
+        if ds.kv_decode is not None:
+            B = ds.qkv.shape[0] - n
+            attn.kv_append(ds.cfg, ds.qkv[n:], ds.k_norm_w, ds.decode_cu, ds.kv_decode, ds.workspace)
+            ev[3].record()
+            attn.decode_attend(ds.cfg, ds.qkv[n:], ds.q_norm_w, ds.max_cache_len, ds.kv_decode,
+                               ds.out[n:], ds.workspace)
+            ev[4].record()
+        else:
+            ev[3].record()
+            ev[4].record()
+
+
+def measure(w, steps, warmup, device, torch, dist_on):
+    """Device-timed steps of workload w.  Returns per-part mean ms and more."""
+    from causal_gqa_attention_qkv_gb300 import inputs as gen
+    from causal_gqa_attention_qkv_gb300 import step
+
+    host = gen.make_inputs(w)
+    ds = step.upload(w, host, device=device)
+    B_dec = w.batch - w.decode_from
+    ds.decode_cu = torch.arange(B_dec + 1, dtype=torch.int32, device=device)
+    t = Timed(ds, torch)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    for _ in range(warmup):
+        flush.fill_(1)
+        t.run([torch.cuda.Event(enable_timing=True) for _ in range(5)])
+    torch.cuda.synchronize()
+    if dist_on:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for k in range(steps):
+        flush.fill_(k & 0xFF)
+        t.run(evs[k])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if dist_on:
+        torch.distributed.barrier()
+    st = ds.status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed steps")
+    parts = {"prefill_append": [], "prefill_attend": [], "decode_append": [], "decode_attend": [], "step": []}
+    for e in evs:
+        parts["prefill_append"].append(e[0].elapsed_time(e[1]))
+        parts["prefill_attend"].append(e[1].elapsed_time(e[2]))
+        parts["decode_append"].append(e[2].elapsed_time(e[3]))
+        parts["decode_attend"].append(e[3].elapsed_time(e[4]))
+        parts["step"].append(e[0].elapsed_time(e[4]))
+    mean = {k: sum(v) / len(v) for k, v in parts.items()}
+    return {"ms": mean, "wall_s": wall, "launches": t.launches_per_step() * steps, "ds": ds,
+            "host": host}
+
+
+def measure_e2e(w, ds, host, steps, warmup, device, torch):
+    """The same step through the public API with the step's inputs in pinned
+    host memory: H2D copy of qkv (and the per-request metadata), the step,
+    D2H copy of the output, all inside the timed events."""
+    qkv_h = host["qkv"].pin_memory()
+    cu_h = host["cu_seqlens"][:ds.cu_seqlens.numel()].clone().pin_memory()
+    cl_h = host["cache_lens"].pin_memory()
+    out_h = torch.empty(ds.out.shape, dtype=ds.out.dtype).pin_memory()
+    h2d = qkv_h.numel() * 2 + cu_h.numel() * 4 + cl_h.numel() * 4
+    d2h = out_h.numel() * 2
+    times = []
+    for k in range(warmup + steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        ds.qkv.copy_(qkv_h, non_blocking=True)
+        ds.cu_seqlens.copy_(cu_h, non_blocking=True)
+        ds.cache_lens.copy_(cl_h, non_blocking=True)
+        ds.run()
+        out_h.copy_(ds.out, non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        if k >= warmup:
+            times.append(e0.elapsed_time(e1))
+    return sum(times) / len(times), h2d, d2h
+
+
+def cpu_oracle_rate(w, budget_s: float, seed: int = 0):
+    """The oracle as it stands on a bounded seeded sample of (token, head)
+    rows of workload w: returns (rate in the metric's unit per second
+    numerator, seconds, sample description, threads)."""
+    import numpy as np
+    import oracle
+    from causal_gqa_attention_qkv_gb300 import inputs as gen
+
+    host = gen.make_inputs(w)
+    cfg = oracle.cfg_of(w)
+    g = np.random.default_rng(seed)
+    all_tok = w.num_tokens
+    # grow the sample until it takes about budget_s
+    count = 16
+    while True:
+        toks = g.integers(0, all_tok, size=count).astype(np.int32)
+        heads = g.integers(0, w.num_q_heads, size=count).astype(np.int32)
+        rows = np.stack([toks, heads], 1)
+        t0 = time.perf_counter()
+        oracle.step(cfg, host, rows=rows)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s * 0.5 or count >= all_tok * w.num_q_heads:
+            break
+        count = int(min(count * max(2.0, budget_s / max(dt, 1e-3) * 0.8), all_tok * w.num_q_heads))
+    cu = host["cu_seqlens"].numpy()
+    cl = host["cache_lens"].numpy()
+    b = np.searchsorted(cu, toks, side="right") - 1
+    keys = cl[b] + (toks - cu[b]) + 1
+    flops = 4.0 * w.head_dim * float(keys.sum())
+    return flops, dt, f"{count} random (token, head) rows of {w.name}, with the full K/V prologue", \
+        oracle.num_threads(), host
+
+
+def cpu_oracle_decode_rate(w, budget_s: float):
+    import numpy as np
+    import oracle
+    from causal_gqa_attention_qkv_gb300 import inputs as gen
+
+    host = gen.make_inputs(w)
+    cfg = oracle.cfg_of(w)
+    nb = 1
+    while True:
+        rows = np.stack([np.repeat(np.arange(nb, dtype=np.int32), w.num_q_heads),
+                         np.tile(np.arange(w.num_q_heads, dtype=np.int32), nb)], 1)
+        t0 = time.perf_counter()
+        oracle.step(cfg, host, rows=rows)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s * 0.5 or nb >= w.batch:
+            break
+        nb = int(min(w.batch, max(nb * 2, nb * budget_s / max(dt, 1e-3) * 0.8)))
+    return decode_bytes(w, 0, nb), dt, f"all heads of the first {nb} requests of {w.name}", oracle.num_threads()
+
+
+def run_ours(args):
+    import torch
+
+    rank, local_rank, world = env_rank()
+    dist_on = world > 1
+    if dist_on:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    device = f"cuda:{local_rank}"
+    from causal_gqa_attention_qkv_gb300 import attn, build
+    from causal_gqa_attention_qkv_gb300 import inputs as gen
+    if rank == 0 or not dist_on:
+        build.build()
+    if dist_on:
+        torch.distributed.barrier()
+    attn.load()
+    peaks, peak_kind = load_peaks()
+    w = gen.ALL[args.workload]
+    assert w.decode_from == w.batch, "the headline workload is a prefill workload"
+    with ClockSampler(local_rank) as clk:
+        m = measure(w, args.steps, args.warmup, device, torch, dist_on)
+    clocks = clk.summary()
+    step_ms = m["ms"]["step"]
+    attend_ms = m["ms"]["prefill_attend"]
+    if dist_on:
+        t = torch.tensor([step_ms, attend_ms], device=device, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms, attend_ms = t.tolist()
+    flops = prefill_flops(w)
+    value = flops * world / (step_ms * 1e-3) / 1e12
+    achieved = flops / (attend_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    sha = source_sha("prefill.cu", "common.cuh")
+    e2e_ms, h2d, d2h = measure_e2e(w, m["ds"], m["host"], max(3, args.steps // 2), 2, device, torch)
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) qkv, norm weights 1+0.1N(0,1), no trained weights)",
+        "config": {"workload": w.name, "global_batch": w.batch * world, "seq_len": max(w.new_lens),
+                   "tokens": w.num_tokens, "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+                   "head_dim": w.head_dim, "attended_pairs": w.attended_pairs(),
+                   "parallelism": f"replicas{world}", "l2": "flushed before every timed step"},
+        "parts_ms": {"kv_append": round(m["ms"]["prefill_append"], 4),
+                     "prefill_attention": round(attend_ms, 4)},
+        "roofline": {"bound": "tensor", "kernel": "prefill attention", "achieved": round(achieved, 3),
+                     "peak": peak, "peak_kind": f"bf16_tflops ({peak_kind})", "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": recorded_traffic("prefill_attention", sha),
+                     "flops_per_launch": flops},
+        "gpu_launches": m["launches"],
+        "e2e": {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clocks,
+    }
+    if not args.no_decode:
+        wd = gen.ALL[args.decode_workload]
+        md = measure(wd, args.steps, args.warmup, device, torch, dist_on)
+        dms = md["ms"]["step"]
+        dattend = md["ms"]["decode_attend"]
+        if dist_on:
+            t = torch.tensor([dms, dattend], device=device, dtype=torch.float64)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            dms, dattend = t.tolist()
+        nbytes = decode_bytes(wd)
+        attend_bytes = nbytes - wd.batch * 2 * wd.num_kv_heads * wd.head_dim * 2  # no append write
+        hbm = float(peaks["hbm_gbs"])
+        line["decode"] = {
+            "value": round(nbytes * world / (dms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(dms, 4), "workload": wd.name, "bytes_per_step": nbytes,
+            "parts_ms": {"kv_append": round(md["ms"]["decode_append"], 4),
+                         "decode_attention": round(dattend, 4)},
+            "roofline": {"bound": "hbm", "kernel": "decode split-KV + combine",
+                         "achieved": round(attend_bytes / (dattend * 1e-3) / 1e9, 1), "peak": hbm,
+                         "peak_kind": f"hbm_gbs ({peak_kind})", "unit": "GB/s",
+                         "frac": round(attend_bytes / (dattend * 1e-3) / 1e9 / hbm, 4),
+                         "frac_of_8tbs_nominal": round(attend_bytes / (dattend * 1e-3) / 8e12, 4),
+                         "traffic": recorded_traffic("decode_split", source_sha("decode.cu", "common.cuh"))},
+            "gpu_launches": md["launches"],
+        }
+        line["gpu_launches"] += md["launches"]
+    if rank == 0 and world == 1 and not args.no_cpu:
+        flops_s, dt, desc, cores, _ = cpu_oracle_rate(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(flops_s / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+                                "kind": "oracle", "sample": desc, "seconds": round(dt, 2)}
+    if dist_on:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args):
+    rank, _, world = env_rank()
+    if rank != 0:
+        return
+    from causal_gqa_attention_qkv_gb300 import inputs as gen
+    w = gen.ALL[args.workload]
+    per_step = max(1.0, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
+    rates = []
+    desc = cores = None
+    for k in range(args.warmup + args.steps):
+        flops, dt, desc, cores, _ = cpu_oracle_rate(w, per_step, seed=k)
+        if k >= args.warmup:
+            rates.append((flops, dt))
+    tot_f = sum(f for f, _ in rates)
+    tot_t = sum(t for _, t in rates)
+    value = tot_f / tot_t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_t / len(rates) * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "global_batch": w.batch, "seq_len": max(w.new_lens),
+                   "tokens": w.num_tokens, "parallelism": "host cores (OpenMP)"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": desc + " per step"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,202 @@
+"""ctypes binding of libattn.so (include/attn.h).
+
+Argument marshalling only: every step of the attention path runs in the
+library's CUDA kernels.  PyTorch provides device memory and the current
+stream.  If the library has not been built (or cannot be loaded) every call
+raises; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libattn.so")
+
+ATTN_STATUS_CAPACITY = 1
+ATTN_STATUS_SEQLENS = 2
+ATTN_STATUS_TIMEOUT = 4
+ATTN_STATUS_BOUNDS = 8
+
+
+class AttnConfig(ctypes.Structure):
+    _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("rms_eps", ctypes.c_float),
+                ("rope_theta", ctypes.c_float)]
+
+
+class AttnKV(ctypes.Structure):
+    _fields_ = [("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+                ("num_slots", ctypes.c_int64), ("slot_base", ctypes.c_void_p),
+                ("cache_lens", ctypes.c_void_p), ("slot_capacity", ctypes.c_void_p)]
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"attn error {code}: {msg}")
+        self.code = code
+
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_SZ = ctypes.c_size_t
+_CFG = ctypes.POINTER(AttnConfig)
+_KV = ctypes.POINTER(AttnKV)
+
+EXPORTS = {
+    "attn_workspace_size": (_SZ, [_CFG, _I32, _I32, _I32]),
+    "attn_workspace_init": (ctypes.c_int, [_P, _SZ, _P]),
+    "attn_kv_append": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _I32, _I32, _KV, _P, _SZ, _P]),
+    "attn_prefill": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _I32, _I32, _I32, _KV, _P, _P, _SZ, _P]),
+    "attn_decode": (ctypes.c_int, [_CFG, _P, _P, _P, _I32, _I32, _KV, _P, _P, _SZ, _P]),
+    "attn_prefill_attend": (ctypes.c_int, [_CFG, _P, _P, _P, _I32, _I32, _I32, _KV, _P, _P, _SZ, _P]),
+    "attn_decode_attend": (ctypes.c_int, [_CFG, _P, _P, _I32, _I32, _KV, _P, _P, _SZ, _P]),
+    "attn_get_status": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
+    "attn_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+}
+
+
+def load(path: str = LIB_PATH):
+    """Load libattn.so and declare its exports (raises if it is missing)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is not built: run causal_gqa_attention_qkv_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in EXPORTS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _check(rc: int) -> None:
+    if rc != 0:
+        raise AttnError(rc, load().attn_strerror(rc).decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def config(num_q_heads: int, num_kv_heads: int, head_dim: int, rms_eps: float = 1e-6,
+           rope_theta: float = 1e6) -> AttnConfig:
+    return AttnConfig(num_q_heads, num_kv_heads, head_dim, rms_eps, rope_theta)
+
+
+@dataclasses.dataclass
+class KVCache:
+    """Device tensors of one layer's KV cache (see attn_kv_t)."""
+
+    k_cache: torch.Tensor       # bf16 [num_slots, Hkv, D]
+    v_cache: torch.Tensor       # bf16 [num_slots, Hkv, D]
+    slot_base: torch.Tensor     # int64 [B]
+    cache_lens: torch.Tensor    # int32 [B]
+    slot_capacity: torch.Tensor  # int32 [B]
+
+    def struct(self) -> AttnKV:
+        for name in ("k_cache", "v_cache"):
+            t = getattr(self, name)
+            assert t.dtype == torch.bfloat16 and t.is_contiguous() and t.is_cuda, name
+        assert self.slot_base.dtype == torch.int64 and self.slot_base.is_contiguous()
+        assert self.cache_lens.dtype == torch.int32 and self.cache_lens.is_contiguous()
+        assert self.slot_capacity.dtype == torch.int32 and self.slot_capacity.is_contiguous()
+        return AttnKV(self.k_cache.data_ptr(), self.v_cache.data_ptr(), self.k_cache.shape[0],
+                      self.slot_base.data_ptr(), self.cache_lens.data_ptr(),
+                      self.slot_capacity.data_ptr())
+
+
+def decode_max_splits(B: int, num_kv_heads: int, max_kv_len: int) -> int:
+    """Number of KV splits attn_decode uses for its longest request (mirrors
+    the library's split policy: about 2048 CTAs when every request is at its
+    longest, splits of at least 256 keys, at most 16 splits, 64-key multiples)."""
+    target = 2048
+    ln = max((max_kv_len * B * num_kv_heads + target - 1) // target, 256, (max_kv_len + 15) // 16)
+    ln = (ln + 63) // 64 * 64
+    return max(1, (max_kv_len + ln - 1) // ln)
+
+
+def workspace_size(cfg: AttnConfig, max_tokens: int, max_batch: int, max_kv_len: int) -> int:
+    n = load().attn_workspace_size(ctypes.byref(cfg), max_tokens, max_batch, max_kv_len)
+    if n == 0:
+        raise AttnError(-1, "invalid workspace query")
+    return int(n)
+
+
+def new_workspace(cfg: AttnConfig, max_tokens: int, max_batch: int, max_kv_len: int,
+                  device="cuda") -> torch.Tensor:
+    """Allocate (with torch) and initialise a workspace."""
+    n = workspace_size(cfg, max_tokens, max_batch, max_kv_len)
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    _check(load().attn_workspace_init(_ptr(ws), n, _stream()))
+    return ws
+
+
+def _bf16(t, name):
+    assert t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous(), name
+    return _ptr(t)
+
+
+def kv_append(cfg: AttnConfig, qkv, k_norm_w, cu_seqlens, kv: KVCache, workspace, stream=None):
+    B = cu_seqlens.numel() - 1
+    s = kv.struct()
+    _check(load().attn_kv_append(ctypes.byref(cfg), _bf16(qkv, "qkv"), None, _bf16(k_norm_w, "k_norm_w"),
+                                 _ptr(cu_seqlens), B, qkv.shape[0], ctypes.byref(s), _ptr(workspace),
+                                 workspace.numel(), _stream(stream)))
+
+
+def prefill(cfg: AttnConfig, qkv, q_norm_w, k_norm_w, cu_seqlens, max_seqlen: int, kv: KVCache,
+            out, workspace, stream=None):
+    assert cu_seqlens.dtype == torch.int32 and cu_seqlens.is_cuda
+    B = cu_seqlens.numel() - 1
+    s = kv.struct()
+    _check(load().attn_prefill(ctypes.byref(cfg), _bf16(qkv, "qkv"), _bf16(q_norm_w, "q_norm_w"),
+                               _bf16(k_norm_w, "k_norm_w"), _ptr(cu_seqlens), B, qkv.shape[0],
+                               int(max_seqlen), ctypes.byref(s), _bf16(out, "out"), _ptr(workspace),
+                               workspace.numel(), _stream(stream)))
+
+
+def decode(cfg: AttnConfig, qkv, q_norm_w, k_norm_w, max_cache_len: int, kv: KVCache, out,
+           workspace, stream=None):
+    B = qkv.shape[0]
+    s = kv.struct()
+    _check(load().attn_decode(ctypes.byref(cfg), _bf16(qkv, "qkv"), _bf16(q_norm_w, "q_norm_w"),
+                              _bf16(k_norm_w, "k_norm_w"), B, int(max_cache_len), ctypes.byref(s),
+                              _bf16(out, "out"), _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def prefill_attend(cfg: AttnConfig, qkv, q_norm_w, cu_seqlens, max_seqlen: int, kv: KVCache, out,
+                   workspace, stream=None):
+    """Attention half of ``prefill`` (the cache already holds the new K/V)."""
+    B = cu_seqlens.numel() - 1
+    s = kv.struct()
+    _check(load().attn_prefill_attend(ctypes.byref(cfg), _bf16(qkv, "qkv"), _bf16(q_norm_w, "q_norm_w"),
+                                      _ptr(cu_seqlens), B, qkv.shape[0], int(max_seqlen), ctypes.byref(s),
+                                      _bf16(out, "out"), _ptr(workspace), workspace.numel(),
+                                      _stream(stream)))
+
+
+def decode_attend(cfg: AttnConfig, qkv, q_norm_w, max_cache_len: int, kv: KVCache, out, workspace,
+                  stream=None):
+    """Attention half of ``decode`` (the cache already holds the new K/V)."""
+    s = kv.struct()
+    _check(load().attn_decode_attend(ctypes.byref(cfg), _bf16(qkv, "qkv"), _bf16(q_norm_w, "q_norm_w"),
+                                     qkv.shape[0], int(max_cache_len), ctypes.byref(s), _bf16(out, "out"),
+                                     _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def get_status(workspace, stream=None) -> int:
+    st = ctypes.c_int32(0)
+    _check(load().attn_get_status(_ptr(workspace), _stream(stream), ctypes.byref(st)))
+    return int(st.value)

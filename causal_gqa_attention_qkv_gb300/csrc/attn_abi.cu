@@ -1,0 +1,305 @@
+// C ABI of the attention step (declared in include/attn.h): argument checks,
+// workspace carving, tensor-map encoding and kernel launches.  No allocation,
+// no state between calls, no stream synchronisation except attn_get_status.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "kernels.cuh"
+
+namespace gb300 {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+int encode_cache_map(void* base, int64_t num_slots, int Hkv, int D, int box_rows, CUtensorMap* m) {
+  auto enc = encoder();
+  if (!enc) return -1;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)num_slots};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -1;
+}
+
+bool is_pow2_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+
+int check_config(const attn_config_t* cfg) {
+  if (!cfg) return ATTN_EINVAL;
+  if (cfg->head_dim != 64 && cfg->head_dim != 128) return ATTN_EINVAL;
+  if (cfg->num_q_heads <= 0 || cfg->num_kv_heads <= 0 || cfg->num_q_heads > 128) return ATTN_EINVAL;
+  if (!(cfg->rms_eps >= 0.f) || !(cfg->rope_theta > 1.f)) return ATTN_EINVAL;
+  if (cfg->num_q_heads % cfg->num_kv_heads != 0) return ATTN_EGQA;
+  if (!is_pow2_group(cfg->num_q_heads / cfg->num_kv_heads)) return ATTN_EGQA;
+  return ATTN_OK;
+}
+
+int check_kv(const attn_kv_t* kv) {
+  if (!kv || !kv->k_cache || !kv->v_cache || !kv->slot_base || !kv->cache_lens ||
+      !kv->slot_capacity)
+    return ATTN_EINVAL;
+  if (kv->num_slots <= 0 || kv->num_slots >= (int64_t(1) << 31)) return ATTN_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(kv->k_cache) | reinterpret_cast<uintptr_t>(kv->v_cache)) & 15)
+    return ATTN_EINVAL;
+  return ATTN_OK;
+}
+
+int check_device() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ELAUNCH;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return ATTN_ELAUNCH;
+  return (major == 10 && minor == 3) ? ATTN_OK : ATTN_EDEVICE;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+size_t partial_bytes(const attn_config_t& c, int64_t B, int max_splits) {
+  size_t rows = (size_t)B * c.num_q_heads * max_splits;
+  return align_up(rows * c.head_dim * 4, 256) + align_up(rows * 2 * 4, 256);
+}
+
+int32_t* status_of(void* ws) { return static_cast<int32_t*>(ws); }
+
+}  // namespace
+
+void make_rope_freqs(float theta, int head_dim, RopeFreqs* out) {
+  const int half = head_dim / 2;
+  for (int i = 0; i < 64; ++i) {
+    double f = i < half ? std::pow((double)theta, -2.0 * i / head_dim) : 0.0;
+    float hi = (float)f;
+    out->hi[i] = hi;
+    out->lo[i] = (float)(f - (double)hi);
+  }
+  const double two_pi = 6.283185307179586476925286766559;
+  out->two_pi_hi = (float)two_pi;
+  out->two_pi_lo = (float)(two_pi - (double)out->two_pi_hi);
+  out->inv_two_pi = (float)(1.0 / two_pi);
+}
+
+int make_cache_maps(const attn_kv_t& kv, int Hkv, int D, int box_rows, CacheMaps* maps) {
+  if (encode_cache_map(kv.k_cache, kv.num_slots, Hkv, D, box_rows, &maps->k) != 0) return -1;
+  if (encode_cache_map(kv.v_cache, kv.num_slots, Hkv, D, box_rows, &maps->v) != 0) return -1;
+  return 0;
+}
+
+namespace {
+
+// Checks shared by the entry points that read qkv and write out.
+int check_common(const attn_config_t* cfg, const attn_kv_t* kv, const void* qkv,
+                 const void* w, const void* out) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  if ((rc = check_kv(kv))) return rc;
+  if (!qkv || !w || !out) return ATTN_EINVAL;
+  if (!aligned16(qkv) || !aligned16(w) || !aligned16(out)) return ATTN_EINVAL;
+  return ATTN_OK;
+}
+
+bool ws_ok(const void* ws, size_t bytes, size_t need) {
+  return ws && (reinterpret_cast<uintptr_t>(ws) & 255) == 0 && bytes >= need;
+}
+
+int append(const attn_config_t* cfg, const void* qkv, const void* k_norm_w,
+           const int32_t* cu_seqlens, int32_t B, int32_t N, const attn_kv_t* kv, void* workspace,
+           cudaStream_t s) {
+  PrologueArgs a;
+  a.cfg = *cfg;
+  a.qkv = qkv;
+  a.k_norm_w = k_norm_w;
+  a.cu_seqlens = cu_seqlens;
+  a.B = B;
+  a.N = N;
+  a.kv = *kv;
+  a.status = status_of(workspace);
+  make_rope_freqs(cfg->rope_theta, cfg->head_dim, &a.freqs);
+  return launch_prologue(a, s) == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
+}
+
+int prefill_attend(const attn_config_t* cfg, const void* qkv, const void* q_norm_w,
+                   const int32_t* cu_seqlens, int32_t B, int32_t N, int32_t max_seqlen,
+                   const attn_kv_t* kv, void* out, void* workspace, cudaStream_t s) {
+  PrefillArgs pa;
+  pa.cfg = *cfg;
+  pa.B = B;
+  pa.N = N;
+  pa.max_seqlen = max_seqlen;
+  pa.cu_seqlens = cu_seqlens;
+  pa.kv = *kv;
+  pa.qkv = qkv;
+  pa.q_norm_w = q_norm_w;
+  make_rope_freqs(cfg->rope_theta, cfg->head_dim, &pa.freqs);
+  pa.out = out;
+  pa.status = status_of(workspace);
+  return launch_prefill(pa, s);
+}
+
+size_t decode_ws_need(const attn_config_t* cfg, int32_t B, int32_t max_cache_len, int* split_len,
+                      int* max_splits) {
+  *split_len = decode_split_len(std::max(B, 1), cfg->num_kv_heads, max_cache_len + 1, max_splits);
+  return kWsHeader + partial_bytes(*cfg, B, *max_splits);
+}
+
+int decode_attend(const attn_config_t* cfg, const void* qkv, const void* q_norm_w, int32_t B,
+                  int32_t max_cache_len, const attn_kv_t* kv, void* out, void* workspace,
+                  cudaStream_t s) {
+  int split_len = 0, max_splits = 1;
+  decode_ws_need(cfg, B, max_cache_len, &split_len, &max_splits);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t rows = (size_t)B * cfg->num_q_heads * max_splits;
+  DecodeArgs d;
+  d.cfg = *cfg;
+  d.B = B;
+  d.kv = *kv;
+  d.qkv = qkv;
+  d.q_norm_w = q_norm_w;
+  make_rope_freqs(cfg->rope_theta, cfg->head_dim, &d.freqs);
+  d.out = out;
+  d.part_o = reinterpret_cast<float*>(ws + kWsHeader);
+  d.part_ml = reinterpret_cast<float*>(ws + kWsHeader + align_up(rows * cfg->head_dim * 4, 256));
+  d.split_len = split_len;
+  d.max_splits = max_splits;
+  d.status = status_of(workspace);
+  return launch_decode(d, s);
+}
+
+}  // namespace
+}  // namespace gb300
+
+using namespace gb300;
+
+extern "C" {
+
+size_t attn_workspace_size(const attn_config_t* cfg, int32_t max_tokens, int32_t max_batch,
+                           int32_t max_kv_len) {
+  if (check_config(cfg) != ATTN_OK || max_tokens < 0 || max_batch < 0 || max_kv_len < 0) return 0;
+  int split_len = 0, max_splits = 1;
+  const size_t decode = decode_ws_need(cfg, max_batch, std::max(max_kv_len, 1) - 1, &split_len, &max_splits);
+  return std::max<size_t>(kWsHeader, decode);
+}
+
+int attn_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
+  if (!ws_ok(workspace, ws_bytes, kWsHeader)) return ATTN_EWORKSPACE;
+  return cudaMemsetAsync(workspace, 0, kWsHeader, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? ATTN_OK
+             : ATTN_ELAUNCH;
+}
+
+int attn_kv_append(const attn_config_t* cfg, const void* qkv, const void* q_norm_w,
+                   const void* k_norm_w, const int32_t* cu_seqlens, int32_t B, int32_t N,
+                   const attn_kv_t* kv, void* workspace, size_t ws_bytes, void* stream) {
+  (void)q_norm_w;
+  int rc = check_common(cfg, kv, qkv, k_norm_w, k_norm_w);
+  if (rc) return rc;
+  if (!cu_seqlens || B < 0 || N < 0) return ATTN_EINVAL;
+  if (!ws_ok(workspace, ws_bytes, kWsHeader)) return ATTN_EWORKSPACE;
+  if ((rc = check_device())) return rc;
+  if (N == 0 || B == 0) return ATTN_OK;
+  return append(cfg, qkv, k_norm_w, cu_seqlens, B, N, kv, workspace, static_cast<cudaStream_t>(stream));
+}
+
+int attn_prefill_attend(const attn_config_t* cfg, const void* qkv, const void* q_norm_w,
+                        const int32_t* cu_seqlens, int32_t B, int32_t N, int32_t max_seqlen,
+                        const attn_kv_t* kv, void* out, void* workspace, size_t ws_bytes,
+                        void* stream) {
+  int rc = check_common(cfg, kv, qkv, q_norm_w, out);
+  if (rc) return rc;
+  if (!cu_seqlens || B < 0 || N < 0 || max_seqlen < 0) return ATTN_EINVAL;
+  if (!ws_ok(workspace, ws_bytes, kWsHeader)) return ATTN_EWORKSPACE;
+  if ((rc = check_device())) return rc;
+  if (N == 0 || B == 0) return ATTN_OK;
+  return prefill_attend(cfg, qkv, q_norm_w, cu_seqlens, B, N, max_seqlen, kv, out, workspace,
+                        static_cast<cudaStream_t>(stream));
+}
+
+int attn_prefill(const attn_config_t* cfg, const void* qkv, const void* q_norm_w,
+                 const void* k_norm_w, const int32_t* cu_seqlens, int32_t B, int32_t N,
+                 int32_t max_seqlen, const attn_kv_t* kv, void* out, void* workspace,
+                 size_t ws_bytes, void* stream) {
+  int rc = check_common(cfg, kv, qkv, q_norm_w, out);
+  if (rc) return rc;
+  if (!k_norm_w || !aligned16(k_norm_w)) return ATTN_EINVAL;
+  if (!cu_seqlens || B < 0 || N < 0 || max_seqlen < 0) return ATTN_EINVAL;
+  if (!ws_ok(workspace, ws_bytes, kWsHeader)) return ATTN_EWORKSPACE;
+  if ((rc = check_device())) return rc;
+  if (N == 0 || B == 0) return ATTN_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((rc = append(cfg, qkv, k_norm_w, cu_seqlens, B, N, kv, workspace, s))) return rc;
+  return prefill_attend(cfg, qkv, q_norm_w, cu_seqlens, B, N, max_seqlen, kv, out, workspace, s);
+}
+
+int attn_decode_attend(const attn_config_t* cfg, const void* qkv, const void* q_norm_w, int32_t B,
+                       int32_t max_cache_len, const attn_kv_t* kv, void* out, void* workspace,
+                       size_t ws_bytes, void* stream) {
+  int rc = check_common(cfg, kv, qkv, q_norm_w, out);
+  if (rc) return rc;
+  if (B < 0 || max_cache_len < 0) return ATTN_EINVAL;
+  int split_len = 0, max_splits = 1;
+  if (!ws_ok(workspace, ws_bytes, decode_ws_need(cfg, B, max_cache_len, &split_len, &max_splits)))
+    return ATTN_EWORKSPACE;
+  if ((rc = check_device())) return rc;
+  if (B == 0) return ATTN_OK;
+  return decode_attend(cfg, qkv, q_norm_w, B, max_cache_len, kv, out, workspace,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int attn_decode(const attn_config_t* cfg, const void* qkv, const void* q_norm_w,
+                const void* k_norm_w, int32_t B, int32_t max_cache_len, const attn_kv_t* kv,
+                void* out, void* workspace, size_t ws_bytes, void* stream) {
+  int rc = check_common(cfg, kv, qkv, q_norm_w, out);
+  if (rc) return rc;
+  if (!k_norm_w || !aligned16(k_norm_w)) return ATTN_EINVAL;
+  if (B < 0 || max_cache_len < 0) return ATTN_EINVAL;
+  int split_len = 0, max_splits = 1;
+  if (!ws_ok(workspace, ws_bytes, decode_ws_need(cfg, B, max_cache_len, &split_len, &max_splits)))
+    return ATTN_EWORKSPACE;
+  if ((rc = check_device())) return rc;
+  if (B == 0) return ATTN_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((rc = append(cfg, qkv, k_norm_w, nullptr, B, B, kv, workspace, s))) return rc;
+  return decode_attend(cfg, qkv, q_norm_w, B, max_cache_len, kv, out, workspace, s);
+}
+
+int attn_get_status(void* workspace, void* stream, int32_t* status) {
+  if (!workspace || !status) return ATTN_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ELAUNCH;
+  if (cudaMemcpy(status, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_ELAUNCH;
+  if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), s) != cudaSuccess) return ATTN_ELAUNCH;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ELAUNCH;
+  return ATTN_OK;
+}
+
+const char* attn_strerror(int code) {
+  switch (code) {
+    case ATTN_OK: return "ok";
+    case ATTN_EINVAL: return "invalid argument (NULL pointer, negative size, unsupported shape or misaligned buffer)";
+    case ATTN_EGQA: return "Hq must be a multiple of Hkv with Hq/Hkv in {1, 2, 4, 8}";
+    case ATTN_EWORKSPACE: return "workspace missing, not 256-byte aligned or too small";
+    case ATTN_ELAUNCH: return "CUDA launch or driver call failed";
+    case ATTN_EDEVICE: return "the current CUDA device is not sm_103 (GB300)";
+    default: return "unknown error";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,255 @@
+// Device helpers shared by the attention kernels: bf16 packing, mbarriers,
+// TMA tile loads, ldmatrix / mma.sync fragments, bounded pipeline waits.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "../../include/attn.h"
+
+namespace gb300 {
+
+// Layout of the caller's workspace: a 256-byte header (status word first),
+// then the per-call scratch areas, each 256-byte aligned.
+constexpr size_t kWsHeader = 256;
+
+constexpr float kNegInf = -__builtin_huge_valf();
+
+__host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- bf16
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---------------------------------------------------------------- status
+__device__ __forceinline__ void set_status(int32_t* status, int32_t bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// ---------------------------------------------------------------- shared memory addresses
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete.  Gives up after about
+// two seconds (a pipeline that never completes is an internal error): returns
+// false and the caller records ATTN_STATUS_TIMEOUT and leaves its loop.
+constexpr uint32_t kWaitSpinLimit = 1u << 22;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  for (uint32_t i = 0; i < kWaitSpinLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (i > 64) __nanosleep(i < 4096 ? 64 : 512);
+  }
+  return false;
+}
+
+// ---------------------------------------------------------------- TMA
+// 3-D tiled load global -> shared, completion counted on `bar` (bytes).
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t c0, int32_t c1, int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t c0, int32_t c1, int32_t c2, int32_t c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a tile
+// written by TMA with CU_TENSOR_MAP_SWIZZLE_128B (rows of 128 bytes; the
+// chunk index is XORed with the row index modulo 8; tile base 1024-aligned).
+__device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk) {
+  return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+// ---------------------------------------------------------------- mma.sync fragments
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D = A * B + D, m16n8k16, bf16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+      " {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---------------------------------------------------------------- RoPE
+// Rotation frequencies theta^(-2i/D) for i < D/2 as float-float pairs
+// (hi = nearest float, lo = remainder), and 2*pi as a float-float pair for
+// the range reduction.  Computed on the host in double for every call.
+struct RopeFreqs {
+  float hi[64];
+  float lo[64];
+  float two_pi_hi, two_pi_lo, inv_two_pi;
+};
+
+// cos and sin of pos * f for f = hi + lo: float-float product (pos is an
+// exact integer below 2^24, so one fma recovers the rounding error of pos*hi
+// exactly), then Cody-Waite additive range reduction modulo 2*pi with 2*pi
+// split into two floats, then sincosf on |r| <= pi.  The angle keeps about
+// 1e-7 rad absolute error at any position.
+__device__ __forceinline__ void rope_angle(float pos, float f_hi, float f_lo, const RopeFreqs& fr,
+                                           float* c, float* s) {
+  const float a_hi = pos * f_hi;
+  const float a_err = fmaf(pos, f_hi, -a_hi);
+  const float a_lo = fmaf(pos, f_lo, a_err);
+  const float k = rintf(a_hi * fr.inv_two_pi);
+  float r = fmaf(-k, fr.two_pi_hi, a_hi);
+  r = fmaf(-k, fr.two_pi_lo, r);
+  r += a_lo;
+  sincosf(r, s, c);
+}
+
+// One query row (D bf16 values at `row`) normalised and rotated, delivered in
+// the m16n8k16 A-fragment distribution: this thread (quad member q = lane & 3)
+// holds columns 16ks + 2q + {0,1} in frag[ks][0] and 16ks + 8 + 2q + {0,1} in
+// frag[ks][1].  The four threads of a quad hold the whole row, so the RMSNorm
+// sum is a quad reduction, and RoPE's partner column c + D/2 sits in the same
+// thread at ks + D/32.  All 32 lanes must call this (it shuffles); rows with
+// valid == false yield zeros.
+template <int D>
+__device__ __forceinline__ void q_row_frags(const uint16_t* row, bool valid, const uint16_t* w,
+                                            float eps, float pos, const RopeFreqs& fr,
+                                            uint32_t (&frag)[D / 16][2]) {
+  const int q = threadIdx.x & 3;
+  float x[D / 16][4];
+  float ss = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    const uint32_t a = valid ? __ldg(reinterpret_cast<const uint32_t*>(row + 16 * ks + 2 * q)) : 0u;
+    const uint32_t b = valid ? __ldg(reinterpret_cast<const uint32_t*>(row + 16 * ks + 8 + 2 * q)) : 0u;
+    x[ks][0] = bf16_lo(a);
+    x[ks][1] = bf16_hi(a);
+    x[ks][2] = bf16_lo(b);
+    x[ks][3] = bf16_hi(b);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) ss = fmaf(x[ks][j], x[ks][j], ss);
+  }
+  ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+  const float inv = rsqrtf(ss * (1.0f / D) + eps);
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    const uint32_t wa = __ldg(reinterpret_cast<const uint32_t*>(w + 16 * ks + 2 * q));
+    const uint32_t wb = __ldg(reinterpret_cast<const uint32_t*>(w + 16 * ks + 8 + 2 * q));
+    x[ks][0] = bf16_lo(wa) * (x[ks][0] * inv);
+    x[ks][1] = bf16_hi(wa) * (x[ks][1] * inv);
+    x[ks][2] = bf16_lo(wb) * (x[ks][2] * inv);
+    x[ks][3] = bf16_hi(wb) * (x[ks][3] * inv);
+  }
+#pragma unroll
+  for (int ks = 0; ks < D / 32; ++ks) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = 16 * ks + (j >> 1) * 8 + 2 * q + (j & 1);  // rotation pair index < D/2
+      float c, s;
+      rope_angle(pos, fr.hi[i], fr.lo[i], fr, &c, &s);
+      const float x1 = x[ks][j], x2 = x[ks + D / 32][j];
+      x[ks][j] = x1 * c - x2 * s;
+      x[ks + D / 32][j] = x2 * c + x1 * s;
+    }
+  }
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    frag[ks][0] = pack_bf16(x[ks][0], x[ks][1]);
+    frag[ks][1] = pack_bf16(x[ks][2], x[ks][3]);
+  }
+}
+
+// ---------------------------------------------------------------- requests
+// Per-request facts every kernel derives the same way from the arguments.
+struct ReqInfo {
+  int64_t slot0;   // slot of position 0 of the request
+  int32_t cached;  // c_b
+  int32_t n_new;   // n_b
+  bool valid;      // region can hold c_b + n_b entries and cu_seqlens is sane
+};
+
+__device__ __forceinline__ ReqInfo load_request(const int64_t* slot_base, const int32_t* cache_lens,
+                                                const int32_t* slot_capacity, int64_t num_slots,
+                                                int32_t n_new) {
+  ReqInfo r;
+  r.slot0 = slot_base[0];
+  r.cached = cache_lens[0];
+  r.n_new = n_new;
+  int64_t end = (int64_t)r.cached + (int64_t)n_new;
+  r.valid = n_new >= 0 && r.cached >= 0 && r.slot0 >= 0 && end <= (int64_t)slot_capacity[0] &&
+            r.slot0 + end <= num_slots && end <= (1 << 24);
+  return r;
+}
+
+}  // namespace gb300

@@ -1,0 +1,341 @@
+// Decode: one new query token per request against its KV cache.
+//
+// Concept chapter section 4.2/4.3: decode reads the cached history for every
+// new token and is memory-bandwidth bound; transformer-basics "Prefill vs
+// Decode": attention of the new token to the cache is one more row of the
+// lower-triangular attention matrix.  The grid is (split, KV head, request):
+// each CTA streams one contiguous slice of one KV head's cache through shared
+// memory exactly once (TMA, 3-stage mbarrier pipeline) and applies it to all
+// Hq/Hkv query heads of the group at the same time, so every cached byte is
+// read from HBM once per step.  Partial results (running max, sum, unscaled
+// output) of the splits are merged by log-sum-exp in a second kernel.
+#include "kernels.cuh"
+
+namespace gb300 {
+
+namespace {
+
+constexpr int kKeysPerTile = 64;
+constexpr int kStages = 3;
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+
+
+struct DecodePar {
+  const uint16_t* qkv;       // [B, W]
+  const uint16_t* q_norm_w;  // [D]
+  RopeFreqs freqs;
+  float eps;
+  int32_t W;
+  uint16_t* out;
+  float* part_o;
+  float* part_ml;
+  const int64_t* slot_base;
+  const int32_t* cache_lens;
+  const int32_t* slot_capacity;
+  int64_t num_slots;
+  int32_t* status;
+  int32_t Hq, G, split_len, max_splits;
+  float scale_log2;  // log2(e) / sqrt(D)
+};
+
+template <int D>
+struct DecodeLayout {
+  static constexpr int kRegions = D / 64;                        // 128-byte column blocks
+  static constexpr int kRegionBytes = kKeysPerTile * 128;        // 64 rows x 128 B
+  static constexpr int kTileBytes = kRegions * kRegionBytes;     // 64 keys x D
+  static constexpr int kStageBytes = 2 * kTileBytes;             // K + V
+  static constexpr int kBarOffset = kStages * kStageBytes;
+  static constexpr int kSmemBytes = kBarOffset + 2 * kStages * 8 + 1024;  // + alignment slack
+};
+
+__device__ __forceinline__ void named_sync_consumers() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+    decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap, const DecodePar p) {
+  using Lay = DecodeLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::kBarOffset);
+  uint64_t* empty = full + kStages;
+  __shared__ int s_abort;       // written by the producer only
+  __shared__ int s_cons_abort;  // written by consumers only, read after their barrier
+
+  const int split = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
+  const ReqInfo r = load_request(p.slot_base + b, p.cache_lens + b, p.slot_capacity + b,
+                                 p.num_slots, 1);
+  if (!r.valid) return;  // flagged by the prologue
+  const int kv_len = r.cached + 1;
+  const int n_splits = (kv_len + p.split_len - 1) / p.split_len;
+  if (n_splits > p.max_splits) {  // max_cache_len below this request's length
+    if (split == 0 && kh == 0 && threadIdx.x == 0) set_status(p.status, ATTN_STATUS_BOUNDS);
+    return;
+  }
+  if (split >= n_splits) return;
+  const int k0 = split * p.split_len;
+  const int k1 = min(k0 + p.split_len, kv_len);
+  const int ntiles = (k1 - k0 + kKeysPerTile - 1) / kKeysPerTile;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    s_abort = 0;
+    s_cons_abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {  // producer warp: one thread issues all TMA loads
+    if (lane == 0) {
+      prefetch_tmap(&kmap);
+      prefetch_tmap(&vmap);
+      int issued = 0;
+      for (int i = 0; i < ntiles; ++i) {
+        const int st = i % kStages;
+        if (i >= kStages && !mbar_wait(&empty[st], ((i / kStages) - 1) & 1)) {
+          s_abort = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[st], Lay::kStageBytes);
+        uint8_t* kt = smem + st * Lay::kStageBytes;
+        uint8_t* vt = kt + Lay::kTileBytes;
+        const int slot = (int)(r.slot0 + k0 + i * kKeysPerTile);
+#pragma unroll
+        for (int rg = 0; rg < Lay::kRegions; ++rg) {
+          tma_load_3d(kt + rg * Lay::kRegionBytes, &kmap, &full[st], rg * 64, kh, slot);
+          tma_load_3d(vt + rg * Lay::kRegionBytes, &vmap, &full[st], rg * 64, kh, slot);
+        }
+        issued = i + 1;
+      }
+      __syncwarp(1);
+      // After a failed wait, let the copies still in flight land before exit.
+      if (s_abort) {
+        for (int i = max(0, issued - kStages); i < issued; ++i)
+          (void)mbar_wait(&full[i % kStages], (i / kStages) & 1);
+        set_status(p.status, ATTN_STATUS_TIMEOUT);
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumer warps: warp w owns keys [16w, 16w + 16) of each tile
+  const int G = p.G;
+  const int h0 = kh * G;
+  const int qrow = lane >> 2;  // A/C fragment row of this thread (rows >= G are padding)
+  uint32_t qa[D / 16][2];  // rows 0-7 of the A fragment; rows 8-15 are zero
+  q_row_frags<D>(p.qkv + (int64_t)b * p.W + (int64_t)(h0 + min(qrow, G - 1)) * D, qrow < G,
+                 p.q_norm_w, p.eps, (float)r.cached, p.freqs, qa);
+  float o[D / 8][4];
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m = kNegInf, l = 0.f;
+  bool ok = true;
+
+  for (int i = 0; i < ntiles; ++i) {
+    const int st = i % kStages;
+    if (!mbar_wait(&full[st], (i / kStages) & 1)) {
+      ok = false;
+      break;
+    }
+    const uint32_t kb = smem_u32(smem + st * Lay::kStageBytes);
+    const uint32_t vb = kb + Lay::kTileBytes;
+    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const int mi = lane >> 3;
+      const int key = warp * 16 + (mi >> 1) * 8 + (lane & 7);
+      const int chunk = 2 * ks + (mi & 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(kb + (chunk >> 3) * Lay::kRegionBytes + sw128(key, chunk & 7), b0, b1, b2, b3);
+      const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
+      mma_bf16_16816(s[0], a, b0, b1);
+      mma_bf16_16816(s[1], a, b2, b3);
+    }
+    const int kfirst = k0 + i * kKeysPerTile + warp * 16;  // first key of this warp's slice
+    const int kA = kfirst + 2 * (lane & 3);
+    float sc[4];
+    sc[0] = kA < k1 ? s[0][0] * p.scale_log2 : kNegInf;
+    sc[1] = kA + 1 < k1 ? s[0][1] * p.scale_log2 : kNegInf;
+    sc[2] = kA + 8 < k1 ? s[1][0] * p.scale_log2 : kNegInf;
+    sc[3] = kA + 9 < k1 ? s[1][1] * p.scale_log2 : kNegInf;
+    float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float m_new = fmaxf(m, mx);
+    const float m_use = m_new == kNegInf ? 0.f : m_new;
+    const float alpha = fast_exp2(m - m_use);
+    float pr[4], rs = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      pr[e] = fast_exp2(sc[e] - m_use);
+      rs += pr[e];
+    }
+    l = l * alpha + rs;
+    m = m_new;
+#pragma unroll
+    for (int dt = 0; dt < D / 8; ++dt) {
+      o[dt][0] *= alpha;
+      o[dt][1] *= alpha;
+    }
+    const uint32_t pa[4] = {pack_bf16(pr[0], pr[1]), 0u, pack_bf16(pr[2], pr[3]), 0u};
+    // keys past the end hold arbitrary bits: zero their V entries so 0 * NaN cannot occur
+    const bool partial = kfirst + 16 > k1;
+    const uint32_t mA = (kA < k1 ? 0x0000FFFFu : 0u) | (kA + 1 < k1 ? 0xFFFF0000u : 0u);
+    const uint32_t mB = (kA + 8 < k1 ? 0x0000FFFFu : 0u) | (kA + 9 < k1 ? 0xFFFF0000u : 0u);
+#pragma unroll
+    for (int dp = 0; dp < D / 16; ++dp) {
+      const int mi = lane >> 3;
+      const int key = warp * 16 + (mi & 1) * 8 + (lane & 7);
+      const int chunk = 2 * dp + (mi >> 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(vb + (chunk >> 3) * Lay::kRegionBytes + sw128(key, chunk & 7), b0, b1, b2, b3);
+      if (partial) {
+        b0 &= mA; b2 &= mA;
+        b1 &= mB; b3 &= mB;
+      }
+      mma_bf16_16816(o[2 * dp], pa, b0, b1);
+      mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+  }
+  if (!ok) {
+    s_cons_abort = 1;
+    set_status(p.status, ATTN_STATUS_TIMEOUT);
+  }
+  l += __shfl_xor_sync(0xffffffffu, l, 1);
+  l += __shfl_xor_sync(0xffffffffu, l, 2);
+
+  // ---------------- merge the four warps' partial softmax states
+  named_sync_consumers();  // every consumer is done with the stage buffers
+  if (s_cons_abort) return;  // same value for every consumer thread
+  float* mo = reinterpret_cast<float*>(smem);                 // [warps][G][D]
+  float* mm = mo + kConsumerWarps * G * D;                      // [warps][G]
+  float* ml = mm + kConsumerWarps * G;                          // [warps][G]
+  if (qrow < G) {
+    float* dst = mo + (warp * G + qrow) * D + 2 * (lane & 3);
+#pragma unroll
+    for (int dt = 0; dt < D / 8; ++dt) {
+      dst[dt * 8] = o[dt][0];
+      dst[dt * 8 + 1] = o[dt][1];
+    }
+    if ((lane & 3) == 0) {
+      mm[warp * G + qrow] = m;
+      ml[warp * G + qrow] = l;
+    }
+  }
+  named_sync_consumers();
+  const bool direct = n_splits == 1;
+  for (int idx = threadIdx.x; idx < G * D; idx += kConsumerWarps * 32) {
+    const int row = idx / D, d = idx % D;
+    float M = kNegInf;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mm[w * G + row]);
+    float L = 0.f, acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float sw = fast_exp2(mm[w * G + row] - M);
+      L += sw * ml[w * G + row];
+      acc += sw * mo[(w * G + row) * D + d];
+    }
+    const int64_t hrow = (int64_t)b * p.Hq + h0 + row;
+    if (direct) {
+      const __nv_bfloat16 v = __float2bfloat16_rn(acc / L);
+      p.out[hrow * D + d] = *reinterpret_cast<const uint16_t*>(&v);
+    } else {
+      const int64_t prow = hrow * p.max_splits + split;
+      p.part_o[prow * D + d] = acc;
+      if (d == 0) {
+        p.part_ml[prow * 2] = M;
+        p.part_ml[prow * 2 + 1] = L;
+      }
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(D) decode_combine_kernel(const DecodePar p) {
+  const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+  const ReqInfo r = load_request(p.slot_base + b, p.cache_lens + b, p.slot_capacity + b,
+                                 p.num_slots, 1);
+  if (!r.valid) return;
+  const int n = (r.cached + 1 + p.split_len - 1) / p.split_len;
+  if (n <= 1 || n > p.max_splits) return;  // written directly / flagged by the split kernel
+  const int64_t row = (int64_t)b * p.Hq + h;
+  const float* ml = p.part_ml + row * p.max_splits * 2;
+  float M = kNegInf;
+  for (int s = 0; s < n; ++s) M = fmaxf(M, ml[2 * s]);
+  float L = 0.f, acc = 0.f;
+  for (int s = 0; s < n; ++s) {
+    const float w = fast_exp2(ml[2 * s] - M);
+    L += w * ml[2 * s + 1];
+    acc += w * p.part_o[(row * p.max_splits + s) * D + d];
+  }
+  const __nv_bfloat16 v = __float2bfloat16_rn(acc / L);
+  p.out[row * D + d] = *reinterpret_cast<const uint16_t*>(&v);
+}
+
+template <int D>
+int launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
+  using Lay = DecodeLayout<D>;
+  CacheMaps maps;
+  if (make_cache_maps(a.kv, a.cfg.num_kv_heads, D, kKeysPerTile, &maps) != 0) return ATTN_ELAUNCH;
+  DecodePar p;
+  p.qkv = static_cast<const uint16_t*>(a.qkv);
+  p.q_norm_w = static_cast<const uint16_t*>(a.q_norm_w);
+  p.freqs = a.freqs;
+  p.eps = a.cfg.rms_eps;
+  p.W = (a.cfg.num_q_heads + 2 * a.cfg.num_kv_heads) * D;
+  p.out = static_cast<uint16_t*>(a.out);
+  p.part_o = a.part_o;
+  p.part_ml = a.part_ml;
+  p.slot_base = a.kv.slot_base;
+  p.cache_lens = a.kv.cache_lens;
+  p.slot_capacity = a.kv.slot_capacity;
+  p.num_slots = a.kv.num_slots;
+  p.status = a.status;
+  p.Hq = a.cfg.num_q_heads;
+  p.G = a.cfg.num_q_heads / a.cfg.num_kv_heads;
+  p.split_len = a.split_len;
+  p.max_splits = a.max_splits;
+  p.scale_log2 = 1.4426950408889634f / sqrtf((float)D);
+  if (cudaFuncSetAttribute(decode_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Lay::kSmemBytes) != cudaSuccess)
+    return ATTN_ELAUNCH;
+  dim3 grid(a.max_splits, a.cfg.num_kv_heads, a.B);
+  decode_split_kernel<D><<<grid, kThreads, Lay::kSmemBytes, stream>>>(maps.k, maps.v, p);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
+  if (a.max_splits > 1) {
+    decode_combine_kernel<D><<<dim3(a.cfg.num_q_heads, a.B), D, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
+  }
+  return ATTN_OK;
+}
+
+}  // namespace
+
+// Keys per split: enough CTAs to fill 152 SMs several times over when every
+// request is at its longest, at least 256 keys, and at most 16 splits.
+int decode_split_len(int B, int Hkv, int max_kv_len, int* max_splits) {
+  const int64_t target_ctas = 2048;
+  int64_t len = ((int64_t)max_kv_len * B * Hkv + target_ctas - 1) / target_ctas;
+  len = std::max<int64_t>(len, 256);
+  len = std::max<int64_t>(len, ((int64_t)max_kv_len + 15) / 16);
+  len = (len + 63) / 64 * 64;
+  *max_splits = (int)std::max<int64_t>(1, ((int64_t)max_kv_len + len - 1) / len);
+  return (int)len;
+}
+
+int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.B <= 0) return ATTN_OK;
+  return a.cfg.head_dim == 128 ? launch_decode_t<128>(a, stream) : launch_decode_t<64>(a, stream);
+}
+
+}  // namespace gb300

@@ -1,0 +1,62 @@
+// Launch interfaces between the C ABI (attn_abi.cu) and the kernels.
+#pragma once
+
+#include "common.cuh"
+
+namespace gb300 {
+
+void make_rope_freqs(float theta, int head_dim, RopeFreqs* out);
+
+// K RMSNorm + RoPE and the K/V append of N new tokens (no Q work).
+struct PrologueArgs {
+  attn_config_t cfg;
+  const void* qkv;
+  const void* k_norm_w;
+  const int32_t* cu_seqlens;  // NULL in decode mode (token b = request b)
+  int32_t B, N;
+  attn_kv_t kv;
+  int32_t* status;
+  RopeFreqs freqs;
+};
+cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t stream);
+
+// Tensor maps over the K and V cache pools, [num_slots, Hkv, D] bf16, 128-byte
+// swizzled boxes of 64 (d) x 1 (head) x box_rows (slots).
+struct CacheMaps {
+  CUtensorMap k;
+  CUtensorMap v;
+};
+int make_cache_maps(const attn_kv_t& kv, int Hkv, int D, int box_rows, CacheMaps* maps);
+
+// The attention kernels read Q straight from qkv and normalise and rotate
+// it themselves.
+struct DecodeArgs {
+  attn_config_t cfg;
+  int32_t B;
+  attn_kv_t kv;
+  const void* qkv;       // [B, W] bf16
+  const void* q_norm_w;  // [D] bf16
+  RopeFreqs freqs;
+  void* out;      // [B, Hq*D] bf16
+  float* part_o;  // [B, Hq, max_splits, D] fp32
+  float* part_ml; // [B, Hq, max_splits, 2] fp32 (running max in log2 units, sum)
+  int32_t split_len, max_splits;
+  int32_t* status;
+};
+int decode_split_len(int B, int Hkv, int max_kv_len, int* max_splits);
+int launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+struct PrefillArgs {
+  attn_config_t cfg;
+  int32_t B, N, max_seqlen;
+  const int32_t* cu_seqlens;
+  attn_kv_t kv;
+  const void* qkv;       // [N, W] bf16
+  const void* q_norm_w;  // [D] bf16
+  RopeFreqs freqs;
+  void* out;      // [N, Hq*D] bf16
+  int32_t* status;
+};
+int launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+
+}  // namespace gb300

@@ -1,0 +1,174 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) causal grouped-query attention step.
+ *
+ * The step is the attention part of one decoder layer of a Qwen3-style model,
+ * as the zero-to-sglang Ch.3 code walkthrough (section 3.3, "QKV, RoPE, and
+ * causal attention": AttentionLayer.forward) and the transformer-basics page
+ * ("Attention calculation: part 1", "Prefill vs Decode") describe it:
+ *
+ *   qkv [N, (Hq + 2*Hkv) * D]  --split-->  Q [N, Hq, D], K [N, Hkv, D], V [N, Hkv, D]
+ *   Q, K  <- w * x / sqrt(mean(x^2) + eps)          (per head, over D)
+ *   Q, K  <- RoPE at each token's position           (V is not rotated)
+ *   cache <- append K, V                             (KV cache update)
+ *   out[t, h*D:(h+1)*D] = softmax(q . K^T / sqrt(D)) V over the keys at
+ *       positions 0 .. p(t) of the same request, KV head h / (Hq / Hkv)
+ *
+ * Conventions used by every entry point:
+ *
+ * Data types.  qkv, the norm weights, the caches and the output are bf16
+ *   (IEEE bfloat16 bits, round-to-nearest-even on every store).  All
+ *   arithmetic is fp32 (norm, rotation, scores, softmax, accumulation); Q and
+ *   the softmax probabilities enter the tensor-core products rounded to bf16.
+ * Positions.  Request b has cache_lens[b] = c_b entries already cached and
+ *   n_b new tokens; new token j sits at position c_b + j and is written to
+ *   slot slot_base[b] + c_b + j.  The query at position p attends to the keys
+ *   at positions 0 .. p (its own key included).
+ * RMSNorm.  y = w * x / sqrt(mean(x^2) + eps) over each head's D values, one
+ *   weight vector [D] for all Q heads and one for all K heads.
+ * RoPE.  Rotate-half pairing: for i in [0, D/2), the pair (x_i, x_{i+D/2}) is
+ *   rotated by the angle p * theta^(-2i/D):
+ *   (x_i, x_{i+D/2}) <- (x_i cos a - x_{i+D/2} sin a, x_{i+D/2} cos a + x_i sin a).
+ *   The zero-to-sglang chapters name RoPE and cite RoFormer without printing
+ *   a formula; this is the RoFormer rotation with the rotate-half pairing of
+ *   the Qwen3 model family.  The norm comes first (q_norm(q_proj(x).view)).
+ * Memory.  Every pointer argument is a device pointer unless stated
+ *   otherwise.  The library allocates nothing, keeps no state between calls
+ *   and never synchronises the stream except in attn_get_status.  All
+ *   buffers, the stream and the workspace belong to the caller.  Calls are
+ *   asynchronous on `stream` (a cudaStream_t; NULL is the legacy default
+ *   stream).
+ * Sizes.  D in {64, 128}; Hq / Hkv in {1, 2, 4, 8}; Hq <= 128; the cache pool
+ *   holds fewer than 2^31 slots; cache_lens[b] + n_b <= 2^24.
+ * Errors.  A host-side check failure returns a negative ATTN_E* code and
+ *   launches nothing.  Problems only visible on the device (a request whose
+ *   region cannot hold c_b + n_b entries, cu_seqlens that are not
+ *   non-decreasing or do not end at N, a host bound max_seqlen or
+ *   max_cache_len below the device data) set bits of the status word in the
+ *   workspace (ATTN_STATUS_*); that request writes nothing to the cache and
+ *   its output rows are left unwritten.  Nothing traps.
+ */
+#ifndef GB300_ATTN_H
+#define GB300_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Per-layer shape and constants (host struct, passed by pointer). */
+typedef struct attn_config {
+  int32_t num_q_heads;  /* Hq */
+  int32_t num_kv_heads; /* Hkv; Hq % Hkv == 0 (grouped-query attention) */
+  int32_t head_dim;     /* D: 64 or 128 */
+  float rms_eps;        /* eps of the Q/K RMSNorm (Qwen3: 1e-6) */
+  float rope_theta;     /* RoPE base (Qwen3: 1e6) */
+} attn_config_t;
+
+/* The KV cache of one layer (host struct holding device pointers).
+ * k_cache, v_cache: bf16 [num_slots, Hkv, D], contiguous, row = one slot.
+ * Request b owns slots [slot_base[b], slot_base[b] + slot_capacity[b]).
+ * cache_lens[b] is read, never written: the caller advances it after the
+ * call (the transformer-basics "Prefill vs Decode" cache goes 0 -> 12 -> 13). */
+typedef struct attn_kv {
+  void* k_cache;
+  void* v_cache;
+  int64_t num_slots;
+  const int64_t* slot_base;     /* [B] */
+  const int32_t* cache_lens;    /* [B] */
+  const int32_t* slot_capacity; /* [B] */
+} attn_kv_t;
+
+enum {
+  ATTN_OK = 0,
+  ATTN_EINVAL = -1,       /* NULL pointer, negative size, unsupported D or Hq */
+  ATTN_EGQA = -2,         /* Hq % Hkv != 0 or Hq / Hkv not in {1, 2, 4, 8} */
+  ATTN_EWORKSPACE = -3,   /* workspace NULL, misaligned or smaller than required */
+  ATTN_ELAUNCH = -4,      /* a CUDA launch or driver call failed */
+  ATTN_EDEVICE = -5       /* the current device is not sm_103 */
+};
+
+/* Bits of the device status word (see attn_get_status). */
+enum {
+  ATTN_STATUS_CAPACITY = 1, /* a request's region cannot hold c_b + n_b entries */
+  ATTN_STATUS_SEQLENS = 2,  /* cu_seqlens decreasing or cu_seqlens[B] != N */
+  ATTN_STATUS_TIMEOUT = 4,  /* a pipeline wait gave up (internal error) */
+  ATTN_STATUS_BOUNDS = 8    /* max_seqlen / max_cache_len below a request's length:
+                               that request's output rows are left unwritten */
+};
+
+/* Workspace bytes needed by any call with at most `max_tokens` new tokens,
+ * `max_batch` requests and `max_kv_len` keys per request (c_b + n_b).  The
+ * workspace is a caller-owned device buffer, 256-byte aligned: a 256-byte
+ * header holding the status word, then (decode only) the split-KV partial
+ * results.  Returns 0 for invalid arguments. */
+ATTN_API size_t attn_workspace_size(const attn_config_t* cfg, int32_t max_tokens, int32_t max_batch,
+                           int32_t max_kv_len);
+
+/* Zero the workspace's status word (asynchronous).  Call once after
+ * allocating a workspace; attn_get_status clears it again. */
+ATTN_API int attn_workspace_init(void* workspace, size_t ws_bytes, void* stream);
+
+/* KV append only: split, K RMSNorm + RoPE, write K and V of the N new tokens
+ * to the cache (no attention).  qkv: bf16 [N, (Hq+2Hkv)*D]; k_norm_w: bf16 [D];
+ * cu_seqlens: int32 [B+1] on the device.  q_norm_w is unused and may be NULL.
+ * transformer-basics "Prefill vs Decode": past_key_values.update. */
+ATTN_API int attn_kv_append(const attn_config_t* cfg, const void* qkv, const void* q_norm_w,
+                   const void* k_norm_w, const int32_t* cu_seqlens, int32_t B, int32_t N,
+                   const attn_kv_t* kv, void* workspace, size_t ws_bytes, void* stream);
+
+/* Attention half of attn_prefill: the cache must already hold this call's
+ * K/V (attn_kv_append with the same arguments, earlier on the stream).  Q is
+ * read from qkv and normalised and rotated inside the attention kernel.
+ * attn_prefill == attn_kv_append followed by attn_prefill_attend. */
+ATTN_API int attn_prefill_attend(const attn_config_t* cfg, const void* qkv, const void* q_norm_w,
+                                 const int32_t* cu_seqlens, int32_t B, int32_t N,
+                                 int32_t max_seqlen, const attn_kv_t* kv, void* out,
+                                 void* workspace, size_t ws_bytes, void* stream);
+
+/* Prefill over ragged packed sequences: the whole step for the N new tokens
+ * of B requests (request b's tokens are rows cu_seqlens[b] .. cu_seqlens[b+1]-1
+ * of qkv), appending their K/V after the c_b cached entries and attending
+ * over c_b + n_b keys.  max_seqlen >= every n_b (host value; bounds the grid).
+ * out: bf16 [N, Hq*D].  Concept chapter section 4.1 "Prefill"; code
+ * walkthrough section 3.1 (packed [N, C] layout) and section 3.3. */
+ATTN_API int attn_prefill(const attn_config_t* cfg, const void* qkv, const void* q_norm_w,
+                 const void* k_norm_w, const int32_t* cu_seqlens, int32_t B, int32_t N,
+                 int32_t max_seqlen, const attn_kv_t* kv, void* out, void* workspace,
+                 size_t ws_bytes, void* stream);
+
+/* Decode: one new token per request (row b of qkv is request b's token at
+ * position c_b), appended and attended over c_b + 1 keys with split-KV and a
+ * log-sum-exp merge.  max_cache_len >= every c_b (host value).
+ * out: bf16 [B, Hq*D].  Concept chapter section 4.2 "Decode";
+ * transformer-basics "Prefill vs Decode" (one more row of the lower triangle). */
+ATTN_API int attn_decode(const attn_config_t* cfg, const void* qkv, const void* q_norm_w,
+                const void* k_norm_w, int32_t B, int32_t max_cache_len, const attn_kv_t* kv,
+                void* out, void* workspace, size_t ws_bytes, void* stream);
+
+/* Attention half of attn_decode (the cache must already hold the new
+ * token's K/V at slot slot_base[b] + c_b).  attn_decode == attn_kv_append
+ * (cu_seqlens = 0, 1, ..., B) followed by attn_decode_attend. */
+ATTN_API int attn_decode_attend(const attn_config_t* cfg, const void* qkv, const void* q_norm_w,
+                                int32_t B, int32_t max_cache_len, const attn_kv_t* kv, void* out,
+                                void* workspace, size_t ws_bytes, void* stream);
+
+/* Synchronise `stream`, copy the status word to *status (host pointer) and
+ * clear it.  Returns ATTN_OK or ATTN_ELAUNCH. */
+ATTN_API int attn_get_status(void* workspace, void* stream, int32_t* status);
+
+/* Static string for an ATTN_E* code. */
+ATTN_API const char* attn_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_ATTN_H */

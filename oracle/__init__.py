@@ -83,6 +83,12 @@ def _bits(t: torch.Tensor) -> np.ndarray:
     return np.array(t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16), copy=True)
 
 
+def _bits_view(t: torch.Tensor) -> np.ndarray:
+    """bf16 CPU tensor -> uint16 array sharing its memory (read-only use)."""
+    assert t.dtype == torch.bfloat16
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
 def bits_to_bf16(a: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
 
@@ -114,7 +120,7 @@ def prologue(cfg: dict, inputs: dict, q_rows=None):
     lib = _load()
     Hq, Hkv, D = cfg["num_q_heads"], cfg["num_kv_heads"], cfg["head_dim"]
     assert D <= 256 and D % 2 == 0 and Hq % Hkv == 0
-    qkv = _bits(inputs["qkv"])
+    qkv = _bits_view(inputs["qkv"])
     N = qkv.shape[0]
     kc = _bits(inputs["k_cache"])
     vc = _bits(inputs["v_cache"])
@@ -152,7 +158,7 @@ def attention(cfg: dict, k_cache: torch.Tensor, v_cache: torch.Tensor, inputs: d
     tok = np.ascontiguousarray(rows[:, 0])
     head = np.ascontiguousarray(rows[:, 1])
     q = np.ascontiguousarray(q, dtype=np.float64).reshape(R, D)
-    kc, vc = _bits(k_cache), _bits(v_cache)
+    kc, vc = _bits_view(k_cache), _bits_view(v_cache)
     cu = np.ascontiguousarray(inputs["cu_seqlens"].numpy().astype(np.int32))
     cl = np.ascontiguousarray(inputs["cache_lens"].numpy().astype(np.int32))
     sb = np.ascontiguousarray(inputs["slot_base"].numpy().astype(np.int64))

@@ -1,0 +1,86 @@
+"""Helpers shared by the GPU parity tests: run a workload through the C ABI
+and compare outputs and caches with the CPU oracle."""
+import numpy as np
+import torch
+
+import oracle
+
+# Floating-point tolerance on bf16 outputs against the fp64 oracle: max-abs
+# error and relative Frobenius error (fp32 accumulation, bf16 operands).
+MAX_ABS = 2e-2
+REL_FRO = 1e-2
+
+
+def ordered_bits(t: torch.Tensor) -> np.ndarray:
+    """bf16 bits mapped to integers that are monotone in the value (so that
+    adjacent representable values differ by one)."""
+    u = t.contiguous().view(torch.int16).numpy().astype(np.int32) & 0xFFFF
+    return np.where(u < 0x8000, u, 0x8000 - u)
+
+
+def written_slots(host: dict, lo: int = 0, hi: int | None = None) -> np.ndarray:
+    cl = host["cache_lens"].numpy()
+    cu = host["cu_seqlens"].numpy()
+    sb = host["slot_base"].numpy()
+    hi = len(cl) if hi is None else hi
+    out = []
+    for b in range(lo, hi):
+        n = cu[b + 1] - cu[b]
+        out.extend(range(sb[b] + cl[b], sb[b] + cl[b] + n))
+    return np.asarray(out, dtype=np.int64)
+
+
+def check_caches(host: dict, ref: dict, k_gpu: torch.Tensor, v_gpu: torch.Tensor) -> None:
+    """V bit-exact everywhere; K within one bf16 step on the written slots and
+    bit-exact (unchanged) everywhere else; every other slot untouched."""
+    k_gpu, v_gpu = k_gpu.cpu(), v_gpu.cpu()
+    assert torch.equal(v_gpu.view(torch.int16), ref["v_cache"].view(torch.int16)), "V cache differs"
+    slots = written_slots(host)
+    mask = np.zeros(k_gpu.shape[0], dtype=bool)
+    mask[slots] = True
+    kg = k_gpu.view(torch.int16).numpy()
+    kr = ref["k_cache"].view(torch.int16).numpy()
+    assert np.array_equal(kg[~mask], kr[~mask]), "K cache changed outside the appended slots"
+    if slots.size:
+        d = np.abs(ordered_bits(k_gpu[torch.from_numpy(slots)]) - ordered_bits(ref["k_cache"][torch.from_numpy(slots)]))
+        assert d.max() <= 1, f"K differs by {d.max()} bf16 steps"
+
+
+def check_out(out_rows: torch.Tensor, ref_out: np.ndarray, what: str = "") -> dict:
+    got = out_rows.double().cpu().numpy()
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    diff = got - ref_out
+    max_abs = float(np.abs(diff).max()) if diff.size else 0.0
+    rel = float(np.linalg.norm(diff) / max(np.linalg.norm(ref_out), 1e-30)) if diff.size else 0.0
+    assert max_abs <= MAX_ABS, f"{what}: max-abs {max_abs:.3e} > {MAX_ABS}"
+    assert rel <= REL_FRO, f"{what}: rel-Frobenius {rel:.3e} > {REL_FRO}"
+    return {"max_abs": max_abs, "rel_fro": rel}
+
+
+def gather_rows(out: torch.Tensor, w, rows: np.ndarray) -> torch.Tensor:
+    o = out.view(w.num_tokens, w.num_q_heads, w.head_dim)
+    t = torch.from_numpy(np.ascontiguousarray(rows[:, 0])).long().to(out.device)
+    h = torch.from_numpy(np.ascontiguousarray(rows[:, 1])).long().to(out.device)
+    return o[t, h]
+
+
+def run_and_compare(w, host: dict, rows=None, check_cache: bool = True) -> dict:
+    """Run workload w on the GPU through the C ABI and compare with the oracle
+    on ``rows`` ((token, head) pairs; default every row)."""
+    from causal_gqa_attention_qkv_gb300 import step
+
+    ds = step.upload(w, host)
+    ds.run()
+    torch.cuda.synchronize()
+    status = ds.status()
+    assert status == 0, f"device status {status}"
+    cfg = oracle.cfg_of(w)
+    if rows is None:
+        rows = oracle.all_rows(w.num_tokens, w.num_q_heads)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
+    ref = oracle.step(cfg, host, rows=rows)
+    stats = check_out(gather_rows(ds.out, w, rows), ref["out"], w.name)
+    if check_cache:
+        check_caches(host, ref, ds.k_cache, ds.v_cache)
+    stats["rows"] = int(rows.shape[0])
+    return {"stats": stats, "ds": ds, "ref": ref}

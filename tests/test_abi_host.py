@@ -1,0 +1,109 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point include/attn.h declares, and rejects bad arguments before
+touching a pointer or the device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from causal_gqa_attention_qkv_gb300 import attn, build
+    build.build()
+    return attn.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "attn.h")).read()
+    return sorted(set(re.findall(r"ATTN_API\s+[\w\s\*]*?\b(attn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_calls():
+    names = declared_functions()
+    for n in ("attn_prefill", "attn_decode", "attn_kv_append", "attn_workspace_size",
+              "attn_get_status", "attn_strerror", "attn_workspace_init"):
+        assert n in names
+
+
+def test_library_exports_every_declared_function(lib):
+    from causal_gqa_attention_qkv_gb300 import attn
+    nm = subprocess.run(["nm", "-D", "--defined-only", attn.LIB_PATH], capture_output=True, text=True,
+                        check=True).stdout
+    exported = set(re.findall(r"\sT\s+(attn_\w+)", nm))
+    for n in declared_functions():
+        assert n in exported, n
+        assert getattr(lib, n) is not None
+
+
+def test_strerror(lib):
+    for code in (0, -1, -2, -3, -4, -5, -99):
+        assert isinstance(lib.attn_strerror(code), bytes)
+    assert b"multiple" in lib.attn_strerror(-2)
+
+
+def test_workspace_size(lib):
+    from causal_gqa_attention_qkv_gb300 import attn
+    cfg = attn.config(32, 8, 128)
+    # prefill needs only the 256-byte status header; decode adds split partials
+    assert attn.workspace_size(cfg, 4096, 0, 4096) == 256
+    c = attn.workspace_size(cfg, 16, 64, 16384)
+    d = attn.workspace_size(cfg, 16, 8, 4096)
+    assert 256 < d < c
+    assert c >= 256 + 64 * 32 * 128 * 4
+    assert lib.attn_workspace_size(ctypes.byref(attn.config(32, 5, 128)), 16, 1, 16) == 0
+    assert lib.attn_workspace_size(ctypes.byref(attn.config(32, 8, 96)), 16, 1, 16) == 0
+
+
+def _kv(attn):
+    fake = 1 << 20  # never dereferenced: every call below fails its checks first
+    return attn.AttnKV(fake, fake, 100, fake, fake, fake)
+
+
+@pytest.mark.parametrize("hq,hkv,d,code", [(32, 5, 128, -2), (24, 8, 128, -2), (32, 8, 96, -1),
+                                            (0, 1, 64, -1), (256, 32, 64, -1)])
+def test_bad_config_rejected(lib, hq, hkv, d, code):
+    from causal_gqa_attention_qkv_gb300 import attn
+    cfg = attn.config(hq, hkv, d)
+    fake = ctypes.c_void_p(1 << 20)
+    kv = _kv(attn)
+    rc = lib.attn_prefill(ctypes.byref(cfg), fake, fake, fake, fake, 1, 4, 4, ctypes.byref(kv), fake,
+                          fake, 1 << 20, None)
+    assert rc == code
+    rc = lib.attn_decode(ctypes.byref(cfg), fake, fake, fake, 1, 4, ctypes.byref(kv), fake, fake,
+                         1 << 20, None)
+    assert rc == code
+
+
+def test_null_and_alignment_rejected(lib):
+    from causal_gqa_attention_qkv_gb300 import attn
+    cfg = attn.config(8, 2, 64)
+    fake = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 2)
+    kv = _kv(attn)
+    call = lambda qkv, ws, wsb, n=4, kvp=ctypes.byref(kv): lib.attn_prefill(
+        ctypes.byref(cfg), qkv, fake, fake, fake, 1, n, 4, kvp, fake, ws, wsb, None)
+    assert call(None, fake, 1 << 20) == -1          # NULL qkv
+    assert call(odd, fake, 1 << 20) == -1           # misaligned qkv
+    assert call(fake, fake, 1 << 20, n=-1) == -1    # negative N
+    assert call(fake, None, 1 << 20) == -3          # no workspace
+    assert call(fake, fake, 100) == -3              # workspace too small
+    assert call(fake, ctypes.c_void_p((1 << 20) + 16), 1 << 20) == -3  # not 256-aligned
+    assert call(fake, fake, 1 << 20, kvp=None) == -1  # no cache
+    bad_kv = attn.AttnKV(1 << 20, 1 << 20, 0, 1 << 20, 1 << 20, 1 << 20)
+    assert call(fake, fake, 1 << 20, kvp=ctypes.byref(bad_kv)) == -1  # empty pool
+    assert lib.attn_get_status(None, None, None) == -1
+
+
+@pytest.mark.parametrize("B,max_kv", [(1, 13), (5, 3001), (64, 8193), (256, 16385), (8, 300)])
+def test_decode_split_mirror_matches_library(lib, B, max_kv):
+    from causal_gqa_attention_qkv_gb300 import attn
+    cfg = attn.config(32, 8, 128)
+    ms = attn.decode_max_splits(B, 8, max_kv)
+    al = lambda x: (x + 255) // 256 * 256
+    expect = 256 + al(B * 32 * ms * 128 * 4) + al(B * 32 * ms * 2 * 4)
+    assert attn.workspace_size(cfg, 1, B, max_kv) == expect

@@ -1,0 +1,193 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the
+same seeded inputs.  Outputs: max-abs <= 2e-2 and relative Frobenius <= 1e-2
+(bf16 outputs, fp32 accumulation); caches: V bit-exact, K within one bf16
+step, every slot outside the appended ones unchanged."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from causal_gqa_attention_qkv_gb300 import inputs as gen
+from parity_util import check_caches, check_out, gather_rows, run_and_compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from causal_gqa_attention_qkv_gb300 import build
+    build.build()
+
+
+def test_tiny_prefill_then_decode_cache_0_12_13():
+    w = gen.tiny()
+    host = gen.make_inputs(w)
+    res = run_and_compare(w, host)
+    ds = res["ds"]
+    # decode step against the 12-entry cache the prefill left behind
+    dw = gen.custom("tiny_decode", w.num_q_heads, w.num_kv_heads, w.head_dim, [1], [12], seed=0,
+                    decode_from=0)
+    dhost = dict(host, qkv=gen.make_followup_decode_qkv(w), cu_seqlens=torch.tensor([0, 1], dtype=torch.int32),
+                 cache_lens=torch.tensor([12], dtype=torch.int32), k_cache=ds.k_cache.cpu(),
+                 v_cache=ds.v_cache.cpu())
+    r2 = run_and_compare(dw, dhost)
+    base = int(host["slot_base"][0])
+    # exactly slot base+12 changed in the decode step
+    before = ds.k_cache.cpu().view(torch.int16)
+    after = r2["ds"].k_cache.cpu().view(torch.int16)
+    changed = (before != after).flatten(1).any(1).nonzero().flatten().tolist()
+    assert changed == [base + 12]
+
+
+RAGGED = [
+    # (Hq, Hkv, D, new lens, cached lens)
+    (8, 2, 128, [1, 17, 64, 100, 200], [0, 5, 0, 130, 37]),
+    (8, 8, 64, [33, 2, 70], [0, 64, 1]),
+    (16, 2, 64, [9, 130, 1], [3, 0, 200]),
+    (8, 1, 128, [40, 65], [0, 300]),
+    (32, 8, 128, [257, 31], [0, 100]),
+]
+
+
+@pytest.mark.parametrize("hq,hkv,d,lens,cache", RAGGED)
+def test_ragged_prefill_all_rows(hq, hkv, d, lens, cache):
+    w = gen.custom(f"ragged_{hq}_{hkv}_{d}", hq, hkv, d, lens, cache, seed=sum(lens) + hq)
+    run_and_compare(w, gen.make_inputs(w))
+
+
+DECODE = [
+    (32, 8, 128, [0, 1, 63, 64, 65, 255, 256, 257, 1000, 3000]),
+    (4, 2, 64, [0, 5, 511, 2047]),
+    (16, 2, 128, [7, 129, 4000]),
+    (8, 8, 64, [12, 300]),
+]
+
+
+@pytest.mark.parametrize("hq,hkv,d,cache", DECODE)
+def test_decode_all_rows(hq, hkv, d, cache):
+    w = gen.custom(f"decode_{hq}_{hkv}_{d}", hq, hkv, d, [1] * len(cache), cache, seed=len(cache) + d,
+                   decode_from=0)
+    run_and_compare(w, gen.make_inputs(w))
+
+
+def test_mixed_prefill_and_decode_small():
+    w = gen.custom("mixed_small", 32, 8, 128, [100, 64, 1, 1, 1], [50, 0, 10, 700, 0], seed=77,
+                   decode_from=2)
+    run_and_compare(w, gen.make_inputs(w))
+
+
+def test_prefill_one_token_rows_equal_decode():
+    # attn_prefill with n_b = 1 gives the decode result (same definition)
+    cache = [5, 300, 1000]
+    wp = gen.custom("p1", 16, 4, 128, [1, 1, 1], cache, seed=91, decode_from=3)
+    wd = gen.custom("d1", 16, 4, 128, [1, 1, 1], cache, seed=91, decode_from=0)
+    host = gen.make_inputs(wp)
+    a = run_and_compare(wp, host)["ds"].out.cpu()
+    b = run_and_compare(wd, host)["ds"].out.cpu()
+    torch.testing.assert_close(a.float(), b.float(), rtol=0, atol=1.6e-2)
+
+
+def test_deterministic_and_idempotent():
+    w = gen.custom("det", 8, 2, 128, [150, 40], [20, 0], seed=5)
+    host = gen.make_inputs(w)
+    from causal_gqa_attention_qkv_gb300 import step
+    ds = step.upload(w, host)
+    ds.run()
+    first = ds.out.clone()
+    k1 = ds.k_cache.clone()
+    ds.run()  # cache_lens not advanced: writes the same slots again
+    torch.cuda.synchronize()
+    assert torch.equal(first.view(torch.int16), ds.out.view(torch.int16))
+    assert torch.equal(k1.view(torch.int16), ds.k_cache.view(torch.int16))
+
+
+def test_status_capacity_and_seqlens():
+    from causal_gqa_attention_qkv_gb300 import attn, step
+    w = gen.custom("cap", 8, 2, 64, [10, 6], [0, 4], seed=8)
+    host = gen.make_inputs(w)
+    host["slot_capacity"][1] = 9  # needs 4 + 6
+    ds = step.upload(w, host)
+    ds.run()
+    assert ds.status() & attn.ATTN_STATUS_CAPACITY
+    assert ds.status() == 0  # read-and-clear
+    # request 1 wrote nothing; request 0 is intact
+    ref = oracle.step(oracle.cfg_of(w), host)
+    assert ref["bad"] == 1
+    kc = ds.k_cache.cpu().view(torch.int16)
+    b1 = int(host["slot_base"][1])
+    assert torch.equal(kc[b1 + 4:b1 + 10], host["k_cache"][b1 + 4:b1 + 10].view(torch.int16))
+    rows = oracle.all_rows(10, w.num_q_heads)
+    check_out(gather_rows(ds.out, w, rows), ref["out"][:rows.shape[0]], "valid request")
+    # cu_seqlens that do not end at N
+    ds2 = step.upload(w, gen.make_inputs(w))
+    ds2.cu_seqlens[-1] = 15
+    ds2.run()
+    assert ds2.status() & attn.ATTN_STATUS_SEQLENS
+
+
+def test_abi_rejects_bad_arguments_on_device():
+    from causal_gqa_attention_qkv_gb300 import attn, step
+    w = gen.custom("args", 8, 2, 64, [4], [0], seed=9)
+    ds = step.upload(w, gen.make_inputs(w))
+    small_ws = ds.workspace[:256]
+    with pytest.raises(attn.AttnError) as e:
+        attn.prefill(ds.cfg, ds.qkv, ds.q_norm_w, ds.k_norm_w, ds.cu_seqlens, 4, ds.kv_prefill, ds.out,
+                     small_ws)
+    assert e.value.code == -3
+    bad = attn.config(8, 3, 64)
+    with pytest.raises(attn.AttnError) as e:
+        attn.prefill(bad, ds.qkv, ds.q_norm_w, ds.k_norm_w, ds.cu_seqlens, 4, ds.kv_prefill, ds.out,
+                     ds.workspace)
+    assert e.value.code == -2
+
+
+# ------------------------------------------------------------------ full sizes
+def _sampled(w, tail, count, seed):
+    return gen.sample_rows(w, count=count, tail=tail, seed=seed).numpy()
+
+
+def test_full_tiny_config():
+    w = gen.tiny()
+    run_and_compare(w, gen.make_inputs(w))
+
+
+def test_full_qwen3_4b_prefill():
+    w = gen.qwen3_4b_prefill()
+    run_and_compare(w, gen.make_inputs(w), rows=_sampled(w, tail=64, count=4096, seed=1))
+
+
+def test_full_decode_batch_all_rows():
+    w = gen.decode_batch()
+    run_and_compare(w, gen.make_inputs(w))
+
+
+def test_full_long_prefill_sampled():
+    w = gen.long_prefill()
+    run_and_compare(w, gen.make_inputs(w), rows=_sampled(w, tail=24, count=1024, seed=3))
+
+
+def test_full_mixed_step_sampled():
+    w = gen.mixed_step()
+    host = gen.make_inputs(w)
+    rows = _sampled(w, tail=16, count=1024, seed=4)
+    run_and_compare(w, host, rows=rows)
+
+
+def test_status_bounds_when_host_bounds_too_small():
+    from causal_gqa_attention_qkv_gb300 import attn, step
+    w = gen.custom("bounds", 8, 2, 64, [100], [0], seed=10)
+    ds = step.upload(w, gen.make_inputs(w))
+    ds.max_seqlen = 10
+    ds.run()
+    assert ds.status() & attn.ATTN_STATUS_BOUNDS
+    wd = gen.custom("bounds_d", 8, 2, 64, [1, 1], [5000, 10], seed=11, decode_from=0)
+    host = gen.make_inputs(wd)
+    dd = step.upload(wd, host)
+    dd.max_cache_len = 100
+    dd.run()
+    assert dd.status() & attn.ATTN_STATUS_BOUNDS
+    # the short request is still computed correctly
+    ref = oracle.step(oracle.cfg_of(wd), host, rows=oracle.all_rows(2, 8)[8:])
+    check_out(gather_rows(dd.out, wd, ref["rows"]), ref["out"], "short request")
