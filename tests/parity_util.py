@@ -30,9 +30,23 @@ def written_slots(host: dict, lo: int = 0, hi: int | None = None) -> np.ndarray:
     return np.asarray(out, dtype=np.int64)
 
 
+# K is computed in fp32 on the device and in fp64 by the oracle, then rounded
+# to bf16 by both: the results may differ by one bf16 step where the exact
+# value sits near a rounding tie, and by the fp32 error (far below 1e-5 for
+# these magnitudes) where the rotation cancels to a value near zero.
+K_ABS_SLACK = 1e-5
+K_MAX_MISMATCH_FRACTION = 1e-2
+
+
+def bf16_step(x: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values at |x| (normal range)."""
+    a = np.maximum(np.abs(x), 2.0 ** -126)
+    return np.exp2(np.floor(np.log2(a)) - 7)
+
+
 def check_caches(host: dict, ref: dict, k_gpu: torch.Tensor, v_gpu: torch.Tensor) -> None:
-    """V bit-exact everywhere; K within one bf16 step on the written slots and
-    bit-exact (unchanged) everywhere else; every other slot untouched."""
+    """V bit-exact everywhere; K within one bf16 step (+ fp32 slack) on the
+    written slots and bit-exact (unchanged) everywhere else."""
     k_gpu, v_gpu = k_gpu.cpu(), v_gpu.cpu()
     assert torch.equal(v_gpu.view(torch.int16), ref["v_cache"].view(torch.int16)), "V cache differs"
     slots = written_slots(host)
@@ -42,8 +56,14 @@ def check_caches(host: dict, ref: dict, k_gpu: torch.Tensor, v_gpu: torch.Tensor
     kr = ref["k_cache"].view(torch.int16).numpy()
     assert np.array_equal(kg[~mask], kr[~mask]), "K cache changed outside the appended slots"
     if slots.size:
-        d = np.abs(ordered_bits(k_gpu[torch.from_numpy(slots)]) - ordered_bits(ref["k_cache"][torch.from_numpy(slots)]))
-        assert d.max() <= 1, f"K differs by {d.max()} bf16 steps"
+        idx = torch.from_numpy(slots)
+        g = k_gpu[idx].float().numpy().astype(np.float64)
+        r = ref["k_cache"][idx].float().numpy().astype(np.float64)
+        err = np.abs(g - r)
+        bound = bf16_step(r) + K_ABS_SLACK
+        assert (err <= bound).all(), f"K off by {float((err / bound).max()):.2f} x (step + slack)"
+        frac = float((g != r).mean())
+        assert frac <= K_MAX_MISMATCH_FRACTION, f"{frac:.3%} of K elements differ"
 
 
 def check_out(out_rows: torch.Tensor, ref_out: np.ndarray, what: str = "") -> dict:

@@ -131,7 +131,7 @@ def test_abi_rejects_bad_arguments_on_device():
     from causal_gqa_attention_qkv_gb300 import attn, step
     w = gen.custom("args", 8, 2, 64, [4], [0], seed=9)
     ds = step.upload(w, gen.make_inputs(w))
-    small_ws = ds.workspace[:256]
+    small_ws = ds.workspace[:128]
     with pytest.raises(attn.AttnError) as e:
         attn.prefill(ds.cfg, ds.qkv, ds.q_norm_w, ds.k_norm_w, ds.cu_seqlens, 4, ds.kv_prefill, ds.out,
                      small_ws)
