@@ -96,6 +96,19 @@ void make_rope_freqs(float theta, int head_dim, RopeFreqs* out) {
   out->inv_two_pi = (float)(1.0 / two_pi);
 }
 
+int make_qkv_map(const void* qkv, int N, int Htot, int D, int G, int BT, CUtensorMap* m) {
+  auto enc = encoder();
+  if (!enc) return -1;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Htot, (cuuint64_t)N};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Htot * D * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)BT};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(qkv), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -1;
+}
+
 int make_cache_maps(const attn_kv_t& kv, int Hkv, int D, int box_rows, CacheMaps* maps) {
   if (encode_cache_map(kv.k_cache, kv.num_slots, Hkv, D, box_rows, &maps->k) != 0) return -1;
   if (encode_cache_map(kv.v_cache, kv.num_slots, Hkv, D, box_rows, &maps->v) != 0) return -1;

@@ -28,6 +28,11 @@ struct CacheMaps {
 };
 int make_cache_maps(const attn_kv_t& kv, int Hkv, int D, int box_rows, CacheMaps* maps);
 
+// Tensor map over qkv viewed as [N, Htot, D] bf16 (Htot = Hq + 2*Hkv), 128-byte
+// swizzled boxes of 64 (d) x G (heads) x BT (tokens): one box is the half
+// (64 of D columns) of a 128-row Q tile of packed (token, group head) rows.
+int make_qkv_map(const void* qkv, int N, int Htot, int D, int G, int BT, CUtensorMap* map);
+
 // The attention kernels read Q straight from qkv and normalise and rotate
 // it themselves.
 struct DecodeArgs {

@@ -311,7 +311,7 @@ int launch_prefill_t(const PrefillArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
-int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
+int launch_prefill_sync(const PrefillArgs& a, cudaStream_t stream) {
   if (a.B <= 0 || a.N <= 0 || a.max_seqlen <= 0) return ATTN_OK;
   return a.cfg.head_dim == 128 ? launch_prefill_t<128>(a, stream) : launch_prefill_t<64>(a, stream);
 }
