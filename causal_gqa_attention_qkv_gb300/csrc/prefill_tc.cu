@@ -62,7 +62,10 @@ struct TcLayout {
   static constexpr int kBar = kP + 2 * kRegionBytes;
   static constexpr int kNumBars = 16;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
-  static constexpr int kSmemBytes = kTmemSlot + 16 + 1024;  // + alignment slack
+  // + alignment slack; at least 116 KB so that one CTA runs per SM: each CTA
+  // allocates all 512 TMEM columns.
+  static constexpr int kSmemRaw = kTmemSlot + 16 + 1024;
+  static constexpr int kSmemBytes = kSmemRaw > 116 * 1024 ? kSmemRaw : 116 * 1024;
 };
 
 enum Bar {
@@ -72,6 +75,13 @@ enum Bar {
 
 __device__ __forceinline__ void softmax_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
+}
+
+// mbarrier wait whose outcome is the same for every lane of the warp, so that
+// warp-collective tcgen05.ld/st after it are never reached by part of a warp.
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity) {
+  const bool w = mbar_wait(bar, parity);
+  return __all_sync(0xffffffffu, w);
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -250,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float2* table = reinterpret_cast<float2*>(smem + Lay::kP);  // RoPE table, P buffer reused
 
     // ---- Q: RMSNorm with q_norm_w, then RoPE at this row's position, in place
-    ok = mbar_wait(&bars[kQFull], 0);
+    ok = wait_warp(&bars[kQFull], 0);
     {
       float x[D];
 #pragma unroll
@@ -318,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cta_min_lim = r.cached + t0;
     const uint32_t p_row = sbase + Lay::kP;
     for (int j = 0; j < nk && ok; ++j) {
-      if (!mbar_wait(&bars[kSFull0 + (j & 1)], (j >> 1) & 1)) { ok = false; break; }
+      if (!wait_warp(&bars[kSFull0 + (j & 1)], (j >> 1) & 1)) { ok = false; break; }
       tc::fence_after();
       float s[kKeys];
 #pragma unroll
@@ -344,9 +354,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float alpha = fast_exp2(m - m_new);
       if (j >= 1) {
         // PV of the previous tile must be complete before O or P is touched
-        if (!mbar_wait(&bars[kODone], (j - 1) & 1)) { ok = false; break; }
+        if (!wait_warp(&bars[kODone], (j - 1) & 1)) { ok = false; break; }
         tc::fence_after();
-        if (alpha < 1.f) {
+        // warp-uniform: lanes whose max did not grow multiply by exactly 1
+        if (__any_sync(0xffffffffu, alpha < 1.f)) {
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
@@ -369,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       m = m_new;
       if (kv0 + kKeys > kv_total) {
         // keys past the end of the sequence hold arbitrary bits: zero those V rows
-        if (!mbar_wait(&bars[kVFull0 + (j & 1)], (j >> 1) & 1)) { ok = false; break; }
+        if (!wait_warp(&bars[kVFull0 + (j & 1)], (j >> 1) & 1)) { ok = false; break; }
         if (kv0 + row >= kv_total) {
           const uint32_t v_addr = sbase + Lay::kV + (j & 1) * Lay::kTile;
 #pragma unroll
@@ -392,16 +403,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&bars[kPFull]);
     }
     // ---- epilogue: O / l -> bf16 rows of out
-    if (ok) ok = mbar_wait(&bars[kODone], (nk - 1) & 1);
+    if (ok) ok = wait_warp(&bars[kODone], (nk - 1) & 1);
     tc::fence_after();
-    if (ok && tok < n_b) {
+    if (ok) {  // warp-uniform; only the stores depend on the row
       const float inv_l = 1.f / l;
-      uint16_t* dst = p.out + (int64_t)(tokbase + tok) * p.Hq * D + (int64_t)h * D;
+      const bool store = tok < n_b;
+      uint16_t* dst = p.out + (int64_t)(tokbase + (store ? tok : 0)) * p.Hq * D + (int64_t)h * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tc::ld_32x32b_x32(lane_base + 256 + c * 32, o);
         tc::wait_ld();
+        if (!store) continue;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint4 v;
@@ -412,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) = v;
         }
       }
-    } else if (!ok) {
+    } else {
       set_status(p.status, ATTN_STATUS_TIMEOUT);
     }
   }
