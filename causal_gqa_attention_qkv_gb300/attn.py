@@ -56,6 +56,7 @@ EXPORTS = {
     "attn_decode": (ctypes.c_int, [_CFG, _P, _P, _P, _I32, _I32, _KV, _P, _P, _SZ, _P]),
     "attn_prefill_attend": (ctypes.c_int, [_CFG, _P, _P, _P, _I32, _I32, _I32, _KV, _P, _P, _SZ, _P]),
     "attn_decode_attend": (ctypes.c_int, [_CFG, _P, _P, _I32, _I32, _KV, _P, _P, _SZ, _P]),
+    "attn_decode_static_scratch": (ctypes.c_int, [_CFG, _P, _P, _P, _I32, _I32, _KV, _P, _P, _P]),
     "attn_get_status": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "attn_strerror": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -194,6 +195,17 @@ def decode_attend(cfg: AttnConfig, qkv, q_norm_w, max_cache_len: int, kv: KVCach
     _check(load().attn_decode_attend(ctypes.byref(cfg), _bf16(qkv, "qkv"), _bf16(q_norm_w, "q_norm_w"),
                                      qkv.shape[0], int(max_cache_len), ctypes.byref(s), _bf16(out, "out"),
                                      _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def decode_static_scratch(cfg: AttnConfig, qkv, q_norm_w, k_norm_w, max_cache_len: int, kv: KVCache,
+                          out, device_status=None, stream=None):
+    """``decode`` with the split-KV scratch in the library's static device
+    buffer (no workspace; for callers that cannot allocate)."""
+    s = kv.struct()
+    _check(load().attn_decode_static_scratch(
+        ctypes.byref(cfg), _bf16(qkv, "qkv"), _bf16(q_norm_w, "q_norm_w"), _bf16(k_norm_w, "k_norm_w"),
+        qkv.shape[0], int(max_cache_len), ctypes.byref(s), _bf16(out, "out"), _ptr(device_status),
+        _stream(stream)))
 
 
 def get_status(workspace, stream=None) -> int:

@@ -96,6 +96,10 @@ void make_rope_freqs(float theta, int head_dim, RopeFreqs* out) {
   out->inv_two_pi = (float)(1.0 / two_pi);
 }
 
+int abi_check_config(const attn_config_t* cfg) { return check_config(cfg); }
+int abi_check_kv(const attn_kv_t* kv) { return check_kv(kv); }
+int abi_check_device() { return check_device(); }
+
 int make_qkv_map(const void* qkv, int N, int Htot, int D, int G, int BT, CUtensorMap* m) {
   auto enc = encoder();
   if (!enc) return -1;
@@ -311,6 +315,7 @@ const char* attn_strerror(int code) {
     case ATTN_EWORKSPACE: return "workspace missing, not 256-byte aligned or too small";
     case ATTN_ELAUNCH: return "CUDA launch or driver call failed";
     case ATTN_EDEVICE: return "the current CUDA device is not sm_103 (GB300)";
+    case ATTN_ESCRATCH: return "request needs more split-KV scratch than the library's static 16 MiB buffer (use attn_decode with a workspace)";
     default: return "unknown error";
   }
 }

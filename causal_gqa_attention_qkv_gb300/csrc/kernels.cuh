@@ -7,6 +7,11 @@ namespace gb300 {
 
 void make_rope_freqs(float theta, int head_dim, RopeFreqs* out);
 
+// Host-side argument checks of the C ABI (ATTN_OK or an ATTN_E* code).
+int abi_check_config(const attn_config_t* cfg);
+int abi_check_kv(const attn_kv_t* kv);
+int abi_check_device();
+
 // K RMSNorm + RoPE and the K/V append of N new tokens (no Q work).
 struct PrologueArgs {
   attn_config_t cfg;

@@ -92,7 +92,8 @@ enum {
   ATTN_EGQA = -2,         /* Hq % Hkv != 0 or Hq / Hkv not in {1, 2, 4, 8} */
   ATTN_EWORKSPACE = -3,   /* workspace NULL, misaligned or smaller than required */
   ATTN_ELAUNCH = -4,      /* a CUDA launch or driver call failed */
-  ATTN_EDEVICE = -5       /* the current device is not sm_103 */
+  ATTN_EDEVICE = -5,      /* the current device is not sm_103 */
+  ATTN_ESCRATCH = -6      /* attn_decode_static_scratch: request exceeds the static scratch */
 };
 
 /* Bits of the device status word (see attn_get_status). */
@@ -159,6 +160,31 @@ ATTN_API int attn_decode(const attn_config_t* cfg, const void* qkv, const void* 
 ATTN_API int attn_decode_attend(const attn_config_t* cfg, const void* qkv, const void* q_norm_w,
                                 int32_t B, int32_t max_cache_len, const attn_kv_t* kv, void* out,
                                 void* workspace, size_t ws_bytes, void* stream);
+
+/* Decode without any caller-provided scratch, for callers that cannot
+ * allocate device memory where they run decode (a plugin inside a host
+ * framework that owns all device allocations; a serving loop that cannot
+ * afford cudaMalloc's implicit synchronisation).  Same arguments and result
+ * as attn_decode, except that the split-KV partial results live in a
+ * library-owned static device array of 16 MiB per GPU (held by every GPU that
+ * loads the library until the process exits) instead of a workspace.
+ *   - Requests whose partials need more than that (B * Hq * splits * (D + 2)
+ *     * 4 bytes, splits as chosen by attn_decode) return ATTN_ESCRATCH and
+ *     launch nothing.
+ *   - device_status: optional caller-owned device int32 (NULL: not recorded)
+ *     that receives the ATTN_STATUS_* bits; the caller zeroes it.
+ *   - The first call on a device looks up the array's device address on the
+ *     current device (cudaGetSymbolAddress); make that first call before any
+ *     stream capture.
+ *   - All calls share the array: calls that overlap on the GPU race.
+ *   - Allocates nothing (no cudaMalloc, no cudaFree, no allocating library
+ *     call).
+ * Not part of the attention method: the zero-to-sglang and transformer-basics
+ * pages this library follows have no counterpart to it. */
+ATTN_API int attn_decode_static_scratch(const attn_config_t* cfg, const void* qkv,
+                                        const void* q_norm_w, const void* k_norm_w, int32_t B,
+                                        int32_t max_cache_len, const attn_kv_t* kv, void* out,
+                                        int32_t* device_status, void* stream);
 
 /* Synchronise `stream`, copy the status word to *status (host pointer) and
  * clear it.  Returns ATTN_OK or ATTN_ELAUNCH. */
