@@ -357,7 +357,7 @@ def run_ours(args):
     value = flops * world / (step_ms * 1e-3) / 1e12
     achieved = flops / (attend_ms * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
-    sha = source_sha("prefill.cu", "common.cuh")
+    sha = source_sha("prefill_tc.cu", "tcgen05.cuh", "common.cuh")
     e2e_ms, h2d, d2h = measure_e2e(w, m["ds"], m["host"], max(3, args.steps // 2), 2, device, torch)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,

@@ -35,6 +35,7 @@ constexpr int kMmaWarp = 5;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kRegionBytes = 128 * 128;  // 128 rows x 128 bytes (64 bf16)
 constexpr int kPairsPerPass = 16;        // RoPE table pass width
+constexpr float kRescaleThreshold = 8.f; // log2 units: rescale O only past a 256x growth
 
 struct TcPar {
   const int32_t* cu_seqlens;
@@ -336,27 +337,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::ld_32x32b_x32(lane_base + (uint32_t)(j & 1) * 128 + c * 32, reinterpret_cast<uint32_t*>(s + c * 32));
       tc::wait_ld();
       const int kv0 = j * kKeys;
-      float mt = kNegInf;
+      // raw scores; keys past this row's causal limit become -inf (select, so
+      // arbitrary bits in keys past the sequence end cannot leak through)
       if (kv0 + kKeys - 1 > cta_min_lim) {
 #pragma unroll
-        for (int c = 0; c < kKeys; ++c) {
-          s[c] = (kv0 + c <= lim) ? s[c] * p.scale_log2 : kNegInf;
-          mt = fmaxf(mt, s[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kKeys; ++c) {
-          s[c] *= p.scale_log2;
-          mt = fmaxf(mt, s[c]);
-        }
+        for (int c = 0; c < kKeys; ++c) s[c] = (kv0 + c <= lim) ? s[c] : kNegInf;
       }
-      const float m_new = fmaxf(m, mt);  // finite: key 0 is visible to every row
-      const float alpha = fast_exp2(m - m_new);
+      // row max with 8 independent chains (one warp per SM sub-partition:
+      // latency is hidden by instruction-level parallelism only)
+      float mx[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mx[e] = s[e];
+#pragma unroll
+      for (int c = 8; c < kKeys; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
+      // Reference max for the exponentials: moved only when the row max grows
+      // by more than 2^8 (P stays <= 256, exact after the final division by l),
+      // so O is rescaled in TMEM rarely.  Tile 0 always sets it (key 0 is
+      // visible to every row, so mt is finite there).
+      const bool grow = (j == 0) || (mt > m + kRescaleThreshold);
+      const float m_new = grow ? fmaxf(m, mt) : m;
+      const float alpha = fast_exp2(m - m_new);  // 0 on tile 0, 1 when not growing
+      const float neg_m = -m_new;
+      float acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+      for (int c = 0; c < kKeys; ++c) {
+        s[c] = fast_exp2(fmaf(s[c], p.scale_log2, neg_m));  // exp2(-inf) = 0
+        acc[c & 7] += s[c];
+      }
+      const float rs = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+      l = l * alpha + rs;
+      m = m_new;
       if (j >= 1) {
-        // PV of the previous tile must be complete before O or P is touched
+        // P.V of the previous tile must be complete before O or P is touched
         if (!wait_warp(&bars[kODone], (j - 1) & 1)) { ok = false; break; }
         tc::fence_after();
-        // warp-uniform: lanes whose max did not grow multiply by exactly 1
+        // warp-uniform: lanes whose reference max did not move multiply by 1
         if (__any_sync(0xffffffffu, alpha < 1.f)) {
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
@@ -370,14 +389,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::wait_st();
         }
       }
-      float rs = 0.f;
-#pragma unroll
-      for (int c = 0; c < kKeys; ++c) {
-        s[c] = fast_exp2(s[c] - m_new);
-        rs += s[c];
-      }
-      l = l * alpha + rs;
-      m = m_new;
       if (kv0 + kKeys > kv_total) {
         // keys past the end of the sequence hold arbitrary bits: zero those V rows
         if (!wait_warp(&bars[kVFull0 + (j & 1)], (j >> 1) & 1)) { ok = false; break; }

@@ -19,11 +19,11 @@ constexpr int kTokPerBlock = 8;
 constexpr int kThreads = 256;
 
 struct ProloguePar {
-  const uint16_t* qkv;        // [N, W] bf16
-  const uint16_t* k_norm_w;   // [D] bf16
+  const uint16_t* __restrict__ qkv;        // [N, W] bf16
+  const uint16_t* __restrict__ k_norm_w;   // [D] bf16
   const int32_t* cu_seqlens;  // [B+1] or NULL: token b is request b (decode)
-  uint16_t* k_cache;
-  uint16_t* v_cache;
+  uint16_t* __restrict__ k_cache;
+  uint16_t* __restrict__ v_cache;
   const int64_t* slot_base;
   const int32_t* cache_lens;
   const int32_t* slot_capacity;
@@ -104,57 +104,72 @@ __global__ void __launch_bounds__(kThreads) kv_append_kernel(const ProloguePar p
 
   const int nhead = 2 * p.Hkv;  // K heads then V heads
   const int ntask = kTokPerBlock * nhead;
-  for (int task = group; task < ntask; task += kGroups) {  // whole groups move together
-    const int tk = task / nhead, hd = task % nhead;
-    if (!s_ok[tk]) continue;
-    const int t = t0 + tk;
-    const bool is_k = hd < p.Hkv;
-    const int kvh = is_k ? hd : hd - p.Hkv;
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
-        p.qkv + (int64_t)t * W + (int64_t)(p.Hq + hd) * D + li * 8));
-    const int64_t dst = (s_slot[tk] * p.Hkv + kvh) * D + li * 8;
-    if (!is_k) {  // V: bit copy into the cache
-      *reinterpret_cast<uint4*>(p.v_cache + dst) = raw;
-      continue;
-    }
-    float x[8];
-    const uint32_t* rw = reinterpret_cast<const uint32_t*>(&raw);
+  constexpr int kMaxTasks = 8;  // tasks per group held in flight (loads issued first)
+  for (int base = 0; base < ntask; base += kGroups * kMaxTasks) {
+    uint4 raw[kMaxTasks];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      x[2 * e] = bf16_lo(rw[e]);
-      x[2 * e + 1] = bf16_hi(rw[e]);
-    }
-    float ss = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
-#pragma unroll
-    for (int off = L / 2; off >= 1; off >>= 1) ss += __shfl_xor_sync(gmask, ss, off);
-    const float inv = rsqrtf(ss * (1.0f / D) + p.eps);
-    const uint32_t* ww = reinterpret_cast<const uint32_t*>(&kw4);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      x[2 * e] = bf16_lo(ww[e]) * (x[2 * e] * inv);
-      x[2 * e + 1] = bf16_hi(ww[e]) * (x[2 * e + 1] * inv);
-    }
-    uint32_t o[4];
-#pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-      const float y0 = x[e], y1 = x[e + 1];
-      const float q0 = __shfl_xor_sync(gmask, y0, L / 2);
-      const float q1 = __shfl_xor_sync(gmask, y1, L / 2);
-      const float c0 = s_cos[tk][pair0 + e], s0 = s_sin[tk][pair0 + e];
-      const float c1 = s_cos[tk][pair0 + e + 1], s1 = s_sin[tk][pair0 + e + 1];
-      float r0, r1;
-      if (first_half) {
-        r0 = y0 * c0 - q0 * s0;
-        r1 = y1 * c1 - q1 * s1;
-      } else {
-        r0 = y0 * c0 + q0 * s0;
-        r1 = y1 * c1 + q1 * s1;
+    for (int k = 0; k < kMaxTasks; ++k) {
+      const int task = base + group + k * kGroups;
+      raw[k] = make_uint4(0, 0, 0, 0);
+      if (task < ntask) {
+        const int tk = task / nhead, hd = task % nhead;
+        if (s_ok[tk])
+          raw[k] = __ldg(reinterpret_cast<const uint4*>(
+              p.qkv + (int64_t)(t0 + tk) * W + (int64_t)(p.Hq + hd) * D + li * 8));
       }
-      o[e / 2] = pack_bf16(r0, r1);
     }
-    *reinterpret_cast<uint4*>(p.k_cache + dst) = make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+    for (int k = 0; k < kMaxTasks; ++k) {
+      const int task = base + group + k * kGroups;  // whole groups move together
+      if (task >= ntask) break;
+      const int tk = task / nhead, hd = task % nhead;
+      if (!s_ok[tk]) continue;
+      const bool is_k = hd < p.Hkv;
+      const int kvh = is_k ? hd : hd - p.Hkv;
+      const int64_t dst = (s_slot[tk] * p.Hkv + kvh) * D + li * 8;
+      if (!is_k) {  // V: bit copy into the cache
+        *reinterpret_cast<uint4*>(p.v_cache + dst) = raw[k];
+        continue;
+      }
+      float x[8];
+      const uint32_t* rw = reinterpret_cast<const uint32_t*>(&raw[k]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        x[2 * e] = bf16_lo(rw[e]);
+        x[2 * e + 1] = bf16_hi(rw[e]);
+      }
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+#pragma unroll
+      for (int off = L / 2; off >= 1; off >>= 1) ss += __shfl_xor_sync(gmask, ss, off);
+      const float inv = rsqrtf(ss * (1.0f / D) + p.eps);
+      const uint32_t* ww = reinterpret_cast<const uint32_t*>(&kw4);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        x[2 * e] = bf16_lo(ww[e]) * (x[2 * e] * inv);
+        x[2 * e + 1] = bf16_hi(ww[e]) * (x[2 * e + 1] * inv);
+      }
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const float y0 = x[e], y1 = x[e + 1];
+        const float q0 = __shfl_xor_sync(gmask, y0, L / 2);
+        const float q1 = __shfl_xor_sync(gmask, y1, L / 2);
+        const float c0 = s_cos[tk][pair0 + e], s0 = s_sin[tk][pair0 + e];
+        const float c1 = s_cos[tk][pair0 + e + 1], s1 = s_sin[tk][pair0 + e + 1];
+        float r0, r1;
+        if (first_half) {
+          r0 = y0 * c0 - q0 * s0;
+          r1 = y1 * c1 - q1 * s1;
+        } else {
+          r0 = y0 * c0 + q0 * s0;
+          r1 = y1 * c1 + q1 * s1;
+        }
+        o[e / 2] = pack_bf16(r0, r1);
+      }
+      *reinterpret_cast<uint4*>(p.k_cache + dst) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
   }
 }
 
