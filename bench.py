@@ -1,9 +1,10 @@
 #!/usr/bin/env python3
 """Benchmark of the causal GQA attention step on GB300.
 
-One step = the whole path for one packed batch: K/V split + RMSNorm + RoPE +
-cache append (kv_append kernel) and causal GQA attention with fused Q
-RMSNorm + RoPE (prefill kernel; split-KV + combine for decode).
+One step = the whole path for one packed batch: qkv split + Q/K RMSNorm +
+RoPE + cache append (prologue kernel; for prefill it also writes the prepared
+Q) and causal GQA attention (tcgen05 prefill kernel; split-KV + combine for
+decode, which prepares its few Q rows itself).
 
 Headline (``value``): prefill attention TFLOP/s on the Qwen3-4B-shaped
 prefill (8 packed sequences, lengths U[256, 2048], Hq 32 / Hkv 8 / D 128).
@@ -159,6 +160,24 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+# ----------------------------------------------------------------- ranks
+def max_over_ranks(values, device="cpu"):
+    """Element-wise maximum of per-rank timings over all ranks (identity
+    without an initialised process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(work_per_rank: float, world: int, ms_max: float) -> float:
+    """Aggregate throughput: the units every rank processed / the slowest rank's time."""
+    return work_per_rank * world / (ms_max * 1e-3)
+
+
 # ----------------------------------------------------------------- our arm
 def env_rank():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
@@ -183,10 +202,11 @@ class Timed:
         n = ds.n_prefill_tokens
         ev[0].record()
         if ds.kv_prefill is not None:
-            attn.kv_append(ds.cfg, ds.qkv[:n], ds.k_norm_w, ds.cu_seqlens, ds.kv_prefill, ds.workspace)
+            attn.prefill_prepare(ds.cfg, ds.qkv[:n], ds.q_norm_w, ds.k_norm_w, ds.cu_seqlens,
+                                 ds.kv_prefill, ds.q_stage[:n], ds.workspace)
             ev[1].record()
-            attn.prefill_attend(ds.cfg, ds.qkv[:n], ds.q_norm_w, ds.cu_seqlens, ds.max_seqlen,
-                                ds.kv_prefill, ds.out[:n], ds.workspace)
+            attn.prefill_attend(ds.cfg, ds.q_stage[:n], ds.cu_seqlens, ds.max_seqlen, ds.kv_prefill,
+                                ds.out[:n], ds.workspace)
             ev[2].record()
         else:
             ev[1].record()
@@ -212,6 +232,8 @@ def measure(w, steps, warmup, device, torch, dist_on):
     ds = step.upload(w, host, device=device)
     B_dec = w.batch - w.decode_from
     ds.decode_cu = torch.arange(B_dec + 1, dtype=torch.int32, device=device)
+    ds.q_stage = torch.empty((max(ds.n_prefill_tokens, 1), w.num_q_heads, w.head_dim), dtype=torch.bfloat16,
+                             device=device)
     t = Timed(ds, torch)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
@@ -347,14 +369,9 @@ def run_ours(args):
     with ClockSampler(local_rank) as clk:
         m = measure(w, args.steps, args.warmup, device, torch, dist_on)
     clocks = clk.summary()
-    step_ms = m["ms"]["step"]
-    attend_ms = m["ms"]["prefill_attend"]
-    if dist_on:
-        t = torch.tensor([step_ms, attend_ms], device=device, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms, attend_ms = t.tolist()
+    step_ms, attend_ms = max_over_ranks([m["ms"]["step"], m["ms"]["prefill_attend"]], device)
     flops = prefill_flops(w)
-    value = flops * world / (step_ms * 1e-3) / 1e12
+    value = whole_job_rate(flops, world, step_ms) / 1e12
     achieved = flops / (attend_ms * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
     sha = source_sha("prefill_tc.cu", "tcgen05.cuh", "common.cuh")
@@ -368,7 +385,7 @@ def run_ours(args):
                    "tokens": w.num_tokens, "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
                    "head_dim": w.head_dim, "attended_pairs": w.attended_pairs(),
                    "parallelism": f"replicas{world}", "l2": "flushed before every timed step"},
-        "parts_ms": {"kv_append": round(m["ms"]["prefill_append"], 4),
+        "parts_ms": {"prologue": round(m["ms"]["prefill_append"], 4),
                      "prefill_attention": round(attend_ms, 4)},
         "roofline": {"bound": "tensor", "kernel": "prefill attention", "achieved": round(achieved, 3),
                      "peak": peak, "peak_kind": f"bf16_tflops ({peak_kind})", "unit": "TFLOP/s",
@@ -382,17 +399,12 @@ def run_ours(args):
     if not args.no_decode:
         wd = gen.ALL[args.decode_workload]
         md = measure(wd, args.steps, args.warmup, device, torch, dist_on)
-        dms = md["ms"]["step"]
-        dattend = md["ms"]["decode_attend"]
-        if dist_on:
-            t = torch.tensor([dms, dattend], device=device, dtype=torch.float64)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            dms, dattend = t.tolist()
+        dms, dattend = max_over_ranks([md["ms"]["step"], md["ms"]["decode_attend"]], device)
         nbytes = decode_bytes(wd)
         attend_bytes = nbytes - wd.batch * 2 * wd.num_kv_heads * wd.head_dim * 2  # no append write
         hbm = float(peaks["hbm_gbs"])
         line["decode"] = {
-            "value": round(nbytes * world / (dms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "value": round(whole_job_rate(nbytes, world, dms) / 1e9, 1), "unit": "GB/s",
             "ms_per_step": round(dms, 4), "workload": wd.name, "bytes_per_step": nbytes,
             "parts_ms": {"kv_append": round(md["ms"]["decode_append"], 4),
                          "decode_attention": round(dattend, 4)},

@@ -54,7 +54,8 @@ EXPORTS = {
     "attn_kv_append": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _I32, _I32, _KV, _P, _SZ, _P]),
     "attn_prefill": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _I32, _I32, _I32, _KV, _P, _P, _SZ, _P]),
     "attn_decode": (ctypes.c_int, [_CFG, _P, _P, _P, _I32, _I32, _KV, _P, _P, _SZ, _P]),
-    "attn_prefill_attend": (ctypes.c_int, [_CFG, _P, _P, _P, _I32, _I32, _I32, _KV, _P, _P, _SZ, _P]),
+    "attn_prefill_prepare": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _I32, _I32, _KV, _P, _P, _SZ, _P]),
+    "attn_prefill_attend": (ctypes.c_int, [_CFG, _P, _P, _I32, _I32, _I32, _KV, _P, _P, _SZ, _P]),
     "attn_decode_attend": (ctypes.c_int, [_CFG, _P, _P, _I32, _I32, _KV, _P, _P, _SZ, _P]),
     "attn_decode_static_scratch": (ctypes.c_int, [_CFG, _P, _P, _P, _I32, _I32, _KV, _P, _P, _P]),
     "attn_get_status": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
@@ -177,15 +178,27 @@ def decode(cfg: AttnConfig, qkv, q_norm_w, k_norm_w, max_cache_len: int, kv: KVC
                               _bf16(out, "out"), _ptr(workspace), workspace.numel(), _stream(stream)))
 
 
-def prefill_attend(cfg: AttnConfig, qkv, q_norm_w, cu_seqlens, max_seqlen: int, kv: KVCache, out,
-                   workspace, stream=None):
-    """Attention half of ``prefill`` (the cache already holds the new K/V)."""
+def prefill_prepare(cfg: AttnConfig, qkv, q_norm_w, k_norm_w, cu_seqlens, kv: KVCache, q_out,
+                    workspace, stream=None):
+    """First half of ``prefill``: K/V appended to the cache, prepared Q
+    (normed, rotated, bf16 [N, Hq, D]) written to ``q_out``."""
     B = cu_seqlens.numel() - 1
     s = kv.struct()
-    _check(load().attn_prefill_attend(ctypes.byref(cfg), _bf16(qkv, "qkv"), _bf16(q_norm_w, "q_norm_w"),
-                                      _ptr(cu_seqlens), B, qkv.shape[0], int(max_seqlen), ctypes.byref(s),
-                                      _bf16(out, "out"), _ptr(workspace), workspace.numel(),
-                                      _stream(stream)))
+    _check(load().attn_prefill_prepare(ctypes.byref(cfg), _bf16(qkv, "qkv"), _bf16(q_norm_w, "q_norm_w"),
+                                       _bf16(k_norm_w, "k_norm_w"), _ptr(cu_seqlens), B, qkv.shape[0],
+                                       ctypes.byref(s), _bf16(q_out, "q_out"), _ptr(workspace),
+                                       workspace.numel(), _stream(stream)))
+
+
+def prefill_attend(cfg: AttnConfig, q, cu_seqlens, max_seqlen: int, kv: KVCache, out, workspace,
+                   stream=None):
+    """Second half of ``prefill``: attention over the prepared Q ``q``
+    [N, Hq, D] (the cache already holds the new K/V)."""
+    B = cu_seqlens.numel() - 1
+    s = kv.struct()
+    _check(load().attn_prefill_attend(ctypes.byref(cfg), _bf16(q, "q"), _ptr(cu_seqlens), B, q.shape[0],
+                                      int(max_seqlen), ctypes.byref(s), _bf16(out, "out"), _ptr(workspace),
+                                      workspace.numel(), _stream(stream)))
 
 
 def decode_attend(cfg: AttnConfig, qkv, q_norm_w, max_cache_len: int, kv: KVCache, out, workspace,

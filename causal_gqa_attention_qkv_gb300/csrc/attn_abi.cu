@@ -136,13 +136,16 @@ bool ws_ok(const void* ws, size_t bytes, size_t need) {
   return ws && (reinterpret_cast<uintptr_t>(ws) & 255) == 0 && bytes >= need;
 }
 
-int append(const attn_config_t* cfg, const void* qkv, const void* k_norm_w,
-           const int32_t* cu_seqlens, int32_t B, int32_t N, const attn_kv_t* kv, void* workspace,
-           cudaStream_t s) {
+// Prologue kernel: K (and, with q_out, Q) norm + RoPE, K/V cache append.
+int append(const attn_config_t* cfg, const void* qkv, const void* q_norm_w, const void* k_norm_w,
+           const int32_t* cu_seqlens, int32_t B, int32_t N, const attn_kv_t* kv, void* q_out,
+           void* workspace, cudaStream_t s) {
   PrologueArgs a;
   a.cfg = *cfg;
   a.qkv = qkv;
+  a.q_norm_w = q_norm_w;
   a.k_norm_w = k_norm_w;
+  a.q_out = q_out;
   a.cu_seqlens = cu_seqlens;
   a.B = B;
   a.N = N;
@@ -152,9 +155,9 @@ int append(const attn_config_t* cfg, const void* qkv, const void* k_norm_w,
   return launch_prologue(a, s) == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
 }
 
-int prefill_attend(const attn_config_t* cfg, const void* qkv, const void* q_norm_w,
-                   const int32_t* cu_seqlens, int32_t B, int32_t N, int32_t max_seqlen,
-                   const attn_kv_t* kv, void* out, void* workspace, cudaStream_t s) {
+int prefill_attend(const attn_config_t* cfg, const void* q, const int32_t* cu_seqlens, int32_t B,
+                   int32_t N, int32_t max_seqlen, const attn_kv_t* kv, void* out, void* workspace,
+                   cudaStream_t s) {
   PrefillArgs pa;
   pa.cfg = *cfg;
   pa.B = B;
@@ -162,12 +165,14 @@ int prefill_attend(const attn_config_t* cfg, const void* qkv, const void* q_norm
   pa.max_seqlen = max_seqlen;
   pa.cu_seqlens = cu_seqlens;
   pa.kv = *kv;
-  pa.qkv = qkv;
-  pa.q_norm_w = q_norm_w;
-  make_rope_freqs(cfg->rope_theta, cfg->head_dim, &pa.freqs);
+  pa.q = q;
   pa.out = out;
   pa.status = status_of(workspace);
   return launch_prefill(pa, s);
+}
+
+size_t q_stage_bytes(const attn_config_t* cfg, int64_t N) {
+  return align_up((size_t)N * cfg->num_q_heads * cfg->head_dim * 2, 256);
 }
 
 size_t decode_ws_need(const attn_config_t* cfg, int32_t B, int32_t max_cache_len, int* split_len,
@@ -211,7 +216,8 @@ size_t attn_workspace_size(const attn_config_t* cfg, int32_t max_tokens, int32_t
   if (check_config(cfg) != ATTN_OK || max_tokens < 0 || max_batch < 0 || max_kv_len < 0) return 0;
   int split_len = 0, max_splits = 1;
   const size_t decode = decode_ws_need(cfg, max_batch, std::max(max_kv_len, 1) - 1, &split_len, &max_splits);
-  return std::max<size_t>(kWsHeader, decode);
+  const size_t prefill = kWsHeader + q_stage_bytes(cfg, max_tokens);
+  return std::max(prefill, decode);
 }
 
 int attn_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
@@ -231,20 +237,35 @@ int attn_kv_append(const attn_config_t* cfg, const void* qkv, const void* q_norm
   if (!ws_ok(workspace, ws_bytes, kWsHeader)) return ATTN_EWORKSPACE;
   if ((rc = check_device())) return rc;
   if (N == 0 || B == 0) return ATTN_OK;
-  return append(cfg, qkv, k_norm_w, cu_seqlens, B, N, kv, workspace, static_cast<cudaStream_t>(stream));
+  return append(cfg, qkv, nullptr, k_norm_w, cu_seqlens, B, N, kv, nullptr, workspace,
+                static_cast<cudaStream_t>(stream));
 }
 
-int attn_prefill_attend(const attn_config_t* cfg, const void* qkv, const void* q_norm_w,
-                        const int32_t* cu_seqlens, int32_t B, int32_t N, int32_t max_seqlen,
-                        const attn_kv_t* kv, void* out, void* workspace, size_t ws_bytes,
-                        void* stream) {
-  int rc = check_common(cfg, kv, qkv, q_norm_w, out);
+int attn_prefill_prepare(const attn_config_t* cfg, const void* qkv, const void* q_norm_w,
+                         const void* k_norm_w, const int32_t* cu_seqlens, int32_t B, int32_t N,
+                         const attn_kv_t* kv, void* q_out, void* workspace, size_t ws_bytes,
+                         void* stream) {
+  int rc = check_common(cfg, kv, qkv, q_norm_w, q_out);
+  if (rc) return rc;
+  if (!k_norm_w || !aligned16(k_norm_w)) return ATTN_EINVAL;
+  if (!cu_seqlens || B < 0 || N < 0) return ATTN_EINVAL;
+  if (!ws_ok(workspace, ws_bytes, kWsHeader)) return ATTN_EWORKSPACE;
+  if ((rc = check_device())) return rc;
+  if (N == 0 || B == 0) return ATTN_OK;
+  return append(cfg, qkv, q_norm_w, k_norm_w, cu_seqlens, B, N, kv, q_out, workspace,
+                static_cast<cudaStream_t>(stream));
+}
+
+int attn_prefill_attend(const attn_config_t* cfg, const void* q, const int32_t* cu_seqlens,
+                        int32_t B, int32_t N, int32_t max_seqlen, const attn_kv_t* kv, void* out,
+                        void* workspace, size_t ws_bytes, void* stream) {
+  int rc = check_common(cfg, kv, q, q, out);
   if (rc) return rc;
   if (!cu_seqlens || B < 0 || N < 0 || max_seqlen < 0) return ATTN_EINVAL;
   if (!ws_ok(workspace, ws_bytes, kWsHeader)) return ATTN_EWORKSPACE;
   if ((rc = check_device())) return rc;
   if (N == 0 || B == 0) return ATTN_OK;
-  return prefill_attend(cfg, qkv, q_norm_w, cu_seqlens, B, N, max_seqlen, kv, out, workspace,
+  return prefill_attend(cfg, q, cu_seqlens, B, N, max_seqlen, kv, out, workspace,
                         static_cast<cudaStream_t>(stream));
 }
 
@@ -256,12 +277,14 @@ int attn_prefill(const attn_config_t* cfg, const void* qkv, const void* q_norm_w
   if (rc) return rc;
   if (!k_norm_w || !aligned16(k_norm_w)) return ATTN_EINVAL;
   if (!cu_seqlens || B < 0 || N < 0 || max_seqlen < 0) return ATTN_EINVAL;
-  if (!ws_ok(workspace, ws_bytes, kWsHeader)) return ATTN_EWORKSPACE;
+  if (!ws_ok(workspace, ws_bytes, kWsHeader + q_stage_bytes(cfg, N))) return ATTN_EWORKSPACE;
   if ((rc = check_device())) return rc;
   if (N == 0 || B == 0) return ATTN_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if ((rc = append(cfg, qkv, k_norm_w, cu_seqlens, B, N, kv, workspace, s))) return rc;
-  return prefill_attend(cfg, qkv, q_norm_w, cu_seqlens, B, N, max_seqlen, kv, out, workspace, s);
+  void* q_stage = static_cast<uint8_t*>(workspace) + kWsHeader;
+  if ((rc = append(cfg, qkv, q_norm_w, k_norm_w, cu_seqlens, B, N, kv, q_stage, workspace, s)))
+    return rc;
+  return prefill_attend(cfg, q_stage, cu_seqlens, B, N, max_seqlen, kv, out, workspace, s);
 }
 
 int attn_decode_attend(const attn_config_t* cfg, const void* qkv, const void* q_norm_w, int32_t B,
@@ -292,7 +315,7 @@ int attn_decode(const attn_config_t* cfg, const void* qkv, const void* q_norm_w,
   if ((rc = check_device())) return rc;
   if (B == 0) return ATTN_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if ((rc = append(cfg, qkv, k_norm_w, nullptr, B, B, kv, workspace, s))) return rc;
+  if ((rc = append(cfg, qkv, nullptr, k_norm_w, nullptr, B, B, kv, nullptr, workspace, s))) return rc;
   return decode_attend(cfg, qkv, q_norm_w, B, max_cache_len, kv, out, workspace, s);
 }
 

@@ -78,7 +78,9 @@ extern "C" int attn_decode_static_scratch(const attn_config_t* cfg, const void* 
   PrologueArgs a;
   a.cfg = *cfg;
   a.qkv = qkv;
+  a.q_norm_w = nullptr;
   a.k_norm_w = k_norm_w;
+  a.q_out = nullptr;       // Q is prepared inside the decode kernel
   a.cu_seqlens = nullptr;  // token b is request b
   a.B = B;
   a.N = B;

@@ -12,11 +12,14 @@ int abi_check_config(const attn_config_t* cfg);
 int abi_check_kv(const attn_kv_t* kv);
 int abi_check_device();
 
-// K RMSNorm + RoPE and the K/V append of N new tokens (no Q work).
+// K RMSNorm + RoPE and the K/V append of N new tokens; with q_out, also Q
+// RMSNorm + RoPE into q_out [N, Hq, D] bf16.
 struct PrologueArgs {
   attn_config_t cfg;
   const void* qkv;
+  const void* q_norm_w;  // used when q_out != NULL
   const void* k_norm_w;
+  void* q_out;           // NULL: K/V only
   const int32_t* cu_seqlens;  // NULL in decode mode (token b = request b)
   int32_t B, N;
   attn_kv_t kv;
@@ -61,9 +64,7 @@ struct PrefillArgs {
   int32_t B, N, max_seqlen;
   const int32_t* cu_seqlens;
   attn_kv_t kv;
-  const void* qkv;       // [N, W] bf16
-  const void* q_norm_w;  // [D] bf16
-  RopeFreqs freqs;
+  const void* q;  // [N, Hq, D] bf16, normed and rotated
   void* out;      // [N, Hq*D] bf16
   int32_t* status;
 };

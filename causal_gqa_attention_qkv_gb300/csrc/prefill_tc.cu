@@ -1,4 +1,5 @@
-// Prefill attention on the 5th-generation tensor cores (tcgen05 + TMEM).
+// Prefill attention on the 5th-generation tensor cores (tcgen05 + TMEM),
+// persistent: one CTA per SM walks a list of work items.
 //
 // Code walkthrough section 3.3 teaching snippet and transformer-basics
 // "Attention calculation: part 1": scores q.k / sqrt(D) against KV head
@@ -6,19 +7,26 @@
 // input type, P times V; concept chapter section 2.6: computed the I/O-aware
 // way (flash attention), never materialising the score matrix.
 //
-// One CTA computes 128 query rows packed as (token, group head) pairs of one
-// KV head (128/G tokens x G heads), so every K/V tile it loads serves the
-// whole GQA group.  Roles (192 threads):
-//   warps 0-3  softmax: thread r owns row r = TMEM lane r.  Normalise and
-//              rotate Q in shared memory, then per KV tile: read S from
-//              TMEM, mask, online softmax in fp32 (exp2 domain), rescale O in
-//              TMEM when the row max grows, write P (bf16) to shared memory.
-//   warp 4     TMA producer: Q tile once, then K and V tiles (128 keys,
-//              128-byte swizzle) through a 2-stage ring.
-//   warp 5     MMA issuer (one thread) and TMEM owner: S = Q K^T into one
-//              of two TMEM buffers, O += P V into TMEM.
-// TMEM: columns [0,128) and [128,256) hold S (fp32), [256, 256+D) hold O.
-// KV tiles past the causal limit of the CTA's last row are never loaded.
+// Q arrives normed and rotated (prologue kernel).  Work item = (sequence b,
+// KV head kh, 128-row query tile).  The tile's rows
+// are 128/G tokens x G heads of the group, so every K/V tile loaded serves the
+// whole GQA group.  Items are numbered sequence by sequence, heaviest tile of
+// a sequence first; CTA c takes items c, c + gridDim.x, ...  Roles (256 threads):
+//   warps 0-3  softmax: thread r owns row r = TMEM lane r.  Per KV tile: read
+//              S from TMEM, mask, online softmax in fp32 (exp2 domain), write P
+//              (bf16) to TMEM, rescale O in TMEM when the reference max moves;
+//              per item: O / l -> bf16 rows of out.
+//   warp 4     TMA producers: lane 0 loads Q (one of three Q buffers per item,
+//              up to two items ahead)
+//              and K (2-stage ring of 128-key tiles running across items);
+//              lane 1 loads V (2-stage ring), so that waiting for a free V slot
+//              never delays the next K tile.
+//   warp 5     MMA issuer (one thread) and TMEM owner: S = Q K^T into one of
+//              two TMEM buffers and O += P V.  Once P of tile g is ready it
+//              issues the S of tiles up to g + 2 whose K (and Q) are already
+//              loaded, then P.V of tile g (also across item boundaries).
+// TMEM: columns [0,128) and [128,256) hold S (fp32), [256, 256+D) hold O,
+// [384,448) and [448,512) hold P (bf16 pairs) for P.V with A read from TMEM.
 #include "kernels.cuh"
 #include "tcgen05.cuh"
 
@@ -26,16 +34,18 @@ namespace gb300 {
 
 namespace {
 
-constexpr int kRows = 128;   // query rows per CTA (MMA M)
-constexpr int kKeys = 128;   // keys per KV tile (MMA N of Q K^T)
+constexpr int kRows = 128;  // query rows per item (MMA M)
+constexpr int kKeys = 128;  // keys per KV tile (MMA N of Q K^T)
 constexpr int kThreads = 192;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
+constexpr int kQBufs = 3;  // Q tiles in flight: the current item and the next two
 constexpr uint32_t kTmemCols = 512;
-constexpr int kRegionBytes = 128 * 128;  // 128 rows x 128 bytes (64 bf16)
-constexpr int kPairsPerPass = 16;        // RoPE table pass width
-constexpr float kRescaleThreshold = 8.f; // log2 units: rescale O only past a 256x growth
+constexpr uint32_t kTmemO = 256;  // O columns
+constexpr uint32_t kTmemP = 384;  // two P buffers of 64 columns
+constexpr int kRegionBytes = 128 * 128;   // 128 rows x 128 bytes (64 bf16)
+constexpr float kRescaleThreshold = 8.f;  // log2 units: move the reference max past 256x growth
 
 struct TcPar {
   const int32_t* cu_seqlens;
@@ -45,41 +55,103 @@ struct TcPar {
   int64_t num_slots;
   int32_t* status;
   uint16_t* out;
-  const uint16_t* q_norm_w;
-  RopeFreqs freqs;
-  float eps;
   float scale_log2;  // log2(e) / sqrt(D)
-  int32_t Hq, log2G, N;
+  int32_t Hq, Hkv, log2G, log2BT, N, B, max_seqlen;
+  int32_t num_vitems;  // ((N >> log2BT) + B) * Hkv: size of the item numbering
 };
 
 template <int D>
 struct TcLayout {
   static constexpr int kRegions = D / 64;
   static constexpr int kTile = kRegions * kRegionBytes;  // Q, K or V tile: 128 rows x D
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTile;           // 2 stages
-  static constexpr int kV = kK + 2 * kTile;       // 2 stages
-  static constexpr int kP = kV + 2 * kTile;       // 128 x 128 bf16, 2 regions of 64 keys
-  static constexpr int kBar = kP + 2 * kRegionBytes;
-  static constexpr int kNumBars = 16;
+  static constexpr int kQ = 0;                // kQBufs buffers
+  static constexpr int kK = kQ + kQBufs * kTile;  // 2 stages
+  static constexpr int kV = kK + 2 * kTile;   // 2 stages
+  static constexpr int kBar = kV + 2 * kTile;
+  static constexpr int kNumBars = 24;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
-  // + alignment slack; at least 116 KB so that one CTA runs per SM: each CTA
-  // allocates all 512 TMEM columns.
+  // + alignment slack; at least 116 KB so that one CTA runs per SM (each CTA
+  // allocates all 512 TMEM columns).
   static constexpr int kSmemRaw = kTmemSlot + 16 + 1024;
   static constexpr int kSmemBytes = kSmemRaw > 116 * 1024 ? kSmemRaw : 116 * 1024;
 };
 
 enum Bar {
-  kQFull = 0, kQReady, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVEmpty0,
-  kVEmpty1, kSFull0, kSFull1, kPFull, kODone, kMmaDone
+  kQFull0 = 0, kQEmpty0 = kQFull0 + kQBufs,
+  kKFull0 = kQEmpty0 + kQBufs, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVEmpty0, kVEmpty1,
+  kSFull0, kSFull1, kPFull, kODone, kMmaDone
 };
 
-__device__ __forceinline__ void softmax_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
+// ---------------------------------------------------------------- work items
+// Item numbering without a table: sequence b owns the "virtual tiles"
+// [vstart(b), vstart(b) + ntiles(b)) with vstart(b) = cu_seqlens[b] / BT + b
+// (these ranges never overlap; each sequence leaves at most one slot empty).
+// Virtual item i = (virtual tile i / Hkv, KV head i % Hkv).
+struct Item {
+  int b, kh, t0, n_b, tokbase, cached, nk, kv_total;
+  int64_t slot0;
+};
+
+__device__ __forceinline__ bool item_at(const TcPar& p, int vi, Item& it) {
+  const int v = vi / p.Hkv;
+  it.kh = vi - v * p.Hkv;
+  int lo = 0, hi = p.B;  // largest b with vstart(b) <= v
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if ((p.cu_seqlens[mid] >> p.log2BT) + mid <= v) lo = mid; else hi = mid;
+  }
+  const int b = lo;
+  const int tokbase = p.cu_seqlens[b];
+  const int n_b = p.cu_seqlens[b + 1] - tokbase;
+  if (n_b <= 0 || tokbase < 0 || tokbase + n_b > p.N) return false;  // flagged by kv_append
+  if (n_b > p.max_seqlen) return false;                               // flagged below
+  const int BT = 1 << p.log2BT;
+  const int ntile = (n_b + BT - 1) >> p.log2BT;
+  const int tfe = v - ((tokbase >> p.log2BT) + b);  // tile index counted from the end
+  if (tfe < 0 || tfe >= ntile) return false;
+  const ReqInfo r = load_request(p.slot_base + b, p.cache_lens + b, p.slot_capacity + b,
+                                 p.num_slots, n_b);
+  if (!r.valid) return false;  // flagged by kv_append
+  it.b = b;
+  it.t0 = (ntile - 1 - tfe) * BT;  // heaviest tile first
+  it.n_b = n_b;
+  it.tokbase = tokbase;
+  it.cached = r.cached;
+  it.slot0 = r.slot0;
+  it.kv_total = r.cached + n_b;
+  it.nk = (r.cached + min(it.t0 + BT, n_b) + kKeys - 1) / kKeys;
+  return true;
 }
 
-// mbarrier wait whose outcome is the same for every lane of the warp, so that
-// warp-collective tcgen05.ld/st after it are never reached by part of a warp.
+// Walks this CTA's items and their KV tiles in order.
+struct TileWalk {
+  int vi;     // current virtual item
+  int k;      // ordinal of the current item within this CTA
+  int j;      // KV tile within the item
+  bool valid;
+  Item it;
+
+  __device__ __forceinline__ void start(const TcPar& p) {
+    vi = blockIdx.x - (int)gridDim.x;
+    k = -1;
+    next_item(p);
+  }
+  __device__ __forceinline__ void next_item(const TcPar& p) {
+    j = 0;
+    for (vi += gridDim.x; vi < p.num_vitems; vi += gridDim.x)
+      if (item_at(p, vi, it)) {
+        ++k;
+        valid = true;
+        return;
+      }
+    valid = false;
+  }
+  __device__ __forceinline__ void next_tile(const TcPar& p) {
+    if (++j >= it.nk) next_item(p);
+  }
+};
+
+// ---------------------------------------------------------------- helpers
 __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity) {
   const bool w = mbar_wait(bar, parity);
   return __all_sync(0xffffffffu, w);
@@ -109,36 +181,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kTmemSlot);
   const uint32_t sbase = smem_u32(smem);
-
-  // ---------------- work item: (sequence b, KV head kh, query tile)
-  const int kh = blockIdx.y, b = blockIdx.z;
-  const int tokbase = p.cu_seqlens[b];
-  const int n_b = p.cu_seqlens[b + 1] - tokbase;
-  if (n_b <= 0) return;
-  if (tokbase < 0 || tokbase + n_b > p.N) {
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) set_status(p.status, ATTN_STATUS_SEQLENS);
-    return;
-  }
-  const ReqInfo r = load_request(p.slot_base + b, p.cache_lens + b, p.slot_capacity + b,
-                                 p.num_slots, n_b);
-  if (!r.valid) return;  // flagged by kv_append
-  const int G = 1 << p.log2G;
-  const int BT = kRows >> p.log2G;  // tokens per CTA
-  const int ntile_b = (n_b + BT - 1) / BT;
-  if (ntile_b > (int)gridDim.x) {
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) set_status(p.status, ATTN_STATUS_BOUNDS);
-    return;
-  }
-  if ((int)blockIdx.x >= ntile_b) return;
-  const int t0 = (ntile_b - 1 - (int)blockIdx.x) * BT;  // heaviest tiles first
-  const int t_hi = min(t0 + BT, n_b);
-  const int kv_total = r.cached + n_b;
-  const int nk = (r.cached + t_hi + kKeys - 1) / kKeys;
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = 1 << p.log2G;
+
+  // Sequences longer than the host bound are left unwritten: flag them once.
+  if (blockIdx.x == 0)
+    for (int b = threadIdx.x; b < p.B; b += kThreads)
+      if (p.cu_seqlens[b + 1] - p.cu_seqlens[b] > p.max_seqlen) set_status(p.status, ATTN_STATUS_BOUNDS);
+
   if (threadIdx.x == 0) {
-    mbar_init(&bars[kQFull], 1);
-    mbar_init(&bars[kQReady], kSoftmaxThreads);
+    for (int s = 0; s < kQBufs; ++s) {
+      mbar_init(&bars[kQFull0 + s], 1);
+      mbar_init(&bars[kQEmpty0 + s], 1);
+    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[kKFull0 + s], 1);
       mbar_init(&bars[kKEmpty0 + s], 1);
@@ -162,43 +217,65 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool ok = true;
 
   if (warp == kProducerWarp) {
-    // ================================================================ TMA producer
-    if (lane == 0) {
-      prefetch_tmap(&qmap);
-      prefetch_tmap(&kmap);
-      prefetch_tmap(&vmap);
-      mbar_arrive_expect_tx(&bars[kQFull], Lay::kTile);
-#pragma unroll
-      for (int rg = 0; rg < Lay::kRegions; ++rg)
-        tma_load_3d(smem + Lay::kQ + rg * kRegionBytes, &qmap, &bars[kQFull], rg * 64, kh * G,
-                    tokbase + t0);
-      int k_issued = 0, v_issued = 0;
-      for (int j = 0; j < nk && ok; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = ((j >> 1) & 1) ^ 1;  // phase of this stage's previous use
-        const int slot = (int)(r.slot0 + j * kKeys);
-        if (j >= 2 && !mbar_wait(&bars[kKEmpty0 + st], ph)) { ok = false; break; }
-        mbar_arrive_expect_tx(&bars[kKFull0 + st], Lay::kTile);
+    // ================================================================ TMA producers
+    if (lane < 2) {
+      const bool kstream = lane == 0;
+      if (kstream) {
+        prefetch_tmap(&qmap);
+        prefetch_tmap(&kmap);
+      } else {
+        prefetch_tmap(&vmap);
+      }
+      TileWalk w, qw;  // K or V tiles; items whose Q tile is loaded next
+      w.start(p);
+      qw.start(p);
+      int g = 0;  // tiles issued so far
+      int q_issued = 0, issued = 0;
+      // Q tile of item qw.k into buffer qw.k % kQBufs (free once the last
+      // Q K^T of item qw.k - kQBufs has completed)
+      auto q_free = [&]() -> bool {
+        return qw.k < kQBufs || mbar_try_wait(&bars[kQEmpty0 + qw.k % kQBufs], (qw.k / kQBufs - 1) & 1);
+      };
+      auto issue_q = [&]() -> bool {
+        const int qs = qw.k % kQBufs;
+        if (qw.k >= kQBufs && !mbar_wait(&bars[kQEmpty0 + qs], (qw.k / kQBufs - 1) & 1)) return false;
+        mbar_arrive_expect_tx(&bars[kQFull0 + qs], Lay::kTile);
 #pragma unroll
         for (int rg = 0; rg < Lay::kRegions; ++rg)
-          tma_load_3d(smem + Lay::kK + st * Lay::kTile + rg * kRegionBytes, &kmap,
-                      &bars[kKFull0 + st], rg * 64, kh, slot);
-        k_issued = j + 1;
-        if (j >= 2 && !mbar_wait(&bars[kVEmpty0 + st], ph)) { ok = false; break; }
-        mbar_arrive_expect_tx(&bars[kVFull0 + st], Lay::kTile);
+          tma_load_3d(smem + Lay::kQ + qs * Lay::kTile + rg * kRegionBytes, &qmap,
+                      &bars[kQFull0 + qs], rg * 64, qw.it.kh * G, qw.it.tokbase + qw.it.t0);
+        q_issued = qw.k + 1;
+        qw.next_item(p);
+        return true;
+      };
+      const int full0 = kstream ? kKFull0 : kVFull0, empty0 = kstream ? kKEmpty0 : kVEmpty0;
+      const int base = kstream ? Lay::kK : Lay::kV;
+      const CUtensorMap* map = kstream ? &kmap : &vmap;
+      while (w.valid && ok) {
+        if (kstream) {
+          while (qw.valid && qw.k <= w.k && ok) ok = issue_q();  // this item's Q
+          if (!ok) break;
+        }
+        const int st = g & 1;
+        if (g >= 2 && !mbar_wait(&bars[empty0 + st], ((g >> 1) & 1) ^ 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(&bars[full0 + st], Lay::kTile);
 #pragma unroll
         for (int rg = 0; rg < Lay::kRegions; ++rg)
-          tma_load_3d(smem + Lay::kV + st * Lay::kTile + rg * kRegionBytes, &vmap,
-                      &bars[kVFull0 + st], rg * 64, kh, slot);
-        v_issued = j + 1;
+          tma_load_3d(smem + base + st * Lay::kTile + rg * kRegionBytes, map, &bars[full0 + st],
+                      rg * 64, w.it.kh, (int)(w.it.slot0 + w.j * kKeys));
+        issued = g + 1;
+        // prefetch the next two items' Q tiles, without waiting for a buffer
+        while (kstream && ok && qw.valid && qw.k <= w.k + kQBufs - 1 && q_free()) ok = issue_q();
+        if (!ok) break;
+        ++g;
+        w.next_tile(p);
       }
       // Every load issued has landed before the CTA may exit (immediate on
       // the normal path, where the consumers already waited for them).
-      (void)mbar_wait(&bars[kQFull], 0);
-      for (int j = max(0, k_issued - 2); j < k_issued; ++j)
-        (void)mbar_wait(&bars[kKFull0 + (j & 1)], (j >> 1) & 1);
-      for (int j = max(0, v_issued - 2); j < v_issued; ++j)
-        (void)mbar_wait(&bars[kVFull0 + (j & 1)], (j >> 1) & 1);
+      for (int k = max(0, q_issued - kQBufs); k < q_issued; ++k)
+        (void)mbar_wait(&bars[kQFull0 + k % kQBufs], (k / kQBufs) & 1);
+      for (int t = max(0, issued - 2); t < issued; ++t)
+        (void)mbar_wait(&bars[full0 + (t & 1)], (t >> 1) & 1);
       if (!ok) set_status(p.status, ATTN_STATUS_TIMEOUT);
     }
   } else if (warp == kMmaWarp) {
@@ -206,42 +283,63 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kRows, kKeys, false);
       constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kRows, D, true);
-      const uint32_t q_addr = sbase + Lay::kQ;
-      const uint32_t p_addr = sbase + Lay::kP;
-      const uint32_t o_tmem = tmem + 256;
-      ok = mbar_wait(&bars[kQReady], 0);
-      tc::fence_after();
-      for (int j = 0; j <= nk && ok; ++j) {
-        if (j < nk) {
-          const int st = j & 1;
-          if (!mbar_wait(&bars[kKFull0 + st], (j >> 1) & 1)) { ok = false; break; }
-          tc::fence_after();
-          const uint32_t k_addr = sbase + Lay::kK + st * Lay::kTile;
+      const uint32_t o_tmem = tmem + kTmemO;
+      TileWalk qk, pv;
+      qk.start(p);
+      pv.start(p);
+      int gq = 0, gp = 0;  // next tile for S = Q K^T, next tile for P.V
+      // S of tile gq may be issued once P of tile gq - 2 has been seen (its S
+      // buffer is free); `ready` reports whether its K (and, on an item's first
+      // tile, its prepared Q) are in shared memory without waiting.
+      auto qk_ready = [&]() -> bool {
+        if (qk.j == 0 && !mbar_try_wait(&bars[kQFull0 + qk.k % kQBufs], (qk.k / kQBufs) & 1)) return false;
+        return mbar_try_wait(&bars[kKFull0 + (gq & 1)], (gq >> 1) & 1);
+      };
+      auto issue_qk = [&]() -> bool {
+        const int st = gq & 1, qs = qk.k % kQBufs;
+        if (qk.j == 0 && !mbar_wait(&bars[kQFull0 + qs], (qk.k / kQBufs) & 1)) return false;
+        if (!mbar_wait(&bars[kKFull0 + st], (gq >> 1) & 1)) return false;
+        tc::fence_after();
+        const uint32_t q_addr = sbase + Lay::kQ + qs * Lay::kTile;
+        const uint32_t k_addr = sbase + Lay::kK + st * Lay::kTile;
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * kRegionBytes + (ks & 3) * 32;
-            tc::mma_f16_ss(tmem + (uint32_t)(j & 1) * 128, tc::sdesc_sw128(q_addr + off, 16, 1024),
-                           tc::sdesc_sw128(k_addr + off, 16, 1024), idesc_s, ks > 0);
-          }
-          tc::commit(&bars[kSFull0 + (j & 1)]);
-          tc::commit(&bars[kKEmpty0 + st]);
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * kRegionBytes + (ks & 3) * 32;
+          tc::mma_f16_ss(tmem + (uint32_t)st * 128, tc::sdesc_sw128(q_addr + off, 16, 1024),
+                         tc::sdesc_sw128(k_addr + off, 16, 1024), idesc_s, ks > 0);
         }
-        if (j >= 1) {
-          const int jj = j - 1, st = jj & 1;
-          if (!mbar_wait(&bars[kPFull], jj & 1)) { ok = false; break; }
-          tc::fence_after();
-          if (!mbar_wait(&bars[kVFull0 + st], (jj >> 1) & 1)) { ok = false; break; }
-          tc::fence_after();
-          const uint32_t v_addr = sbase + Lay::kV + st * Lay::kTile;
+        tc::commit(&bars[kSFull0 + st]);
+        tc::commit(&bars[kKEmpty0 + st]);
+        if (qk.j == qk.it.nk - 1) tc::commit(&bars[kQEmpty0 + qs]);  // last use of this Q tile
+        ++gq;
+        qk.next_tile(p);
+        return true;
+      };
+      while (pv.valid && ok) {
+        // the S that P.V of tile gp consumes must be under way (blocking) ...
+        while (ok && qk.valid && gq <= gp) ok = issue_qk();
+        if (!ok) break;
+        // ... the next one too, if it is loaded
+        if (qk.valid && gq == gp + 1 && qk_ready() && !(ok = issue_qk())) break;
+        if (!mbar_wait(&bars[kPFull], gp & 1)) { ok = false; break; }
+        tc::fence_after();
+        // S buffers of tiles up to gp + 2 are free now: issue what is loaded
+        while (ok && qk.valid && gq <= gp + 2 && qk_ready()) ok = issue_qk();
+        if (!ok) break;
+        const int st = gp & 1;
+        if (!mbar_wait(&bars[kVFull0 + st], (gp >> 1) & 1)) { ok = false; break; }
+        tc::fence_after();
+        const uint32_t v_addr = sbase + Lay::kV + st * Lay::kTile;
+        const uint32_t p_tmem = tmem + kTmemP + (uint32_t)st * 64;
 #pragma unroll
-          for (int kk = 0; kk < kKeys / 16; ++kk) {
-            const uint64_t a = tc::sdesc_sw128(p_addr + (kk >> 2) * kRegionBytes + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = tc::sdesc_sw128(v_addr + kk * 2048, kRegionBytes, 1024);
-            tc::mma_f16_ss(o_tmem, a, bd, idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
-          }
-          tc::commit(&bars[kODone]);
-          tc::commit(&bars[kVEmpty0 + st]);
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          const uint64_t bd = tc::sdesc_sw128(v_addr + kk * 2048, kRegionBytes, 1024);
+          tc::mma_f16_ts(o_tmem, p_tmem + kk * 8, bd, idesc_o, (pv.j > 0 || kk > 0) ? 1u : 0u);
         }
+        tc::commit(&bars[kODone]);
+        tc::commit(&bars[kVEmpty0 + st]);
+        ++gp;
+        pv.next_tile(p);
       }
       // Nothing may still be running on the tensor cores when TMEM is freed.
       tc::commit(&bars[kMmaDone]);
@@ -250,195 +348,134 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ================================================================ softmax warpgroup
-    const int row = threadIdx.x;                 // 0..127 = TMEM lane
-    const int tl = row >> p.log2G;                // token within the tile
-    const int g = row & (G - 1);
-    const int tok = t0 + tl;
-    const int h = kh * G + g;
-    const int lim = tok < n_b ? r.cached + tok : kv_total - 1;  // last key this row may see
+    const int row = threadIdx.x;  // 0..127 = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    const uint32_t q_row = sbase + Lay::kQ;
-    float2* table = reinterpret_cast<float2*>(smem + Lay::kP);  // RoPE table, P buffer reused
-
-    // ---- Q: RMSNorm with q_norm_w, then RoPE at this row's position, in place
-    ok = wait_warp(&bars[kQFull], 0);
-    {
-      float x[D];
-#pragma unroll
-      for (int rg = 0; rg < Lay::kRegions; ++rg)
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 v = lds128(q_row + rg * kRegionBytes + sw128(row, c));
-          const uint32_t* u = reinterpret_cast<const uint32_t*>(&v);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            x[rg * 64 + c * 8 + 2 * e] = bf16_lo(u[e]);
-            x[rg * 64 + c * 8 + 2 * e + 1] = bf16_hi(u[e]);
-          }
-        }
-      float ss = 0.f;
-#pragma unroll
-      for (int d = 0; d < D; ++d) ss = fmaf(x[d], x[d], ss);
-      const float inv = rsqrtf(ss * (1.0f / D) + p.eps);
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        const uint4 wv = __ldg(reinterpret_cast<const uint4*>(p.q_norm_w + c * 8));
-        const uint32_t* u = reinterpret_cast<const uint32_t*>(&wv);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          x[c * 8 + 2 * e] = bf16_lo(u[e]) * (x[c * 8 + 2 * e] * inv);
-          x[c * 8 + 2 * e + 1] = bf16_hi(u[e]) * (x[c * 8 + 2 * e + 1] * inv);
-        }
-      }
-      // cos/sin of (position, pair) for the tile's tokens, kPairsPerPass pairs at a time
-      const float pos0 = (float)(r.cached + t0);
-#pragma unroll
-      for (int pass = 0; pass < D / 2 / kPairsPerPass; ++pass) {
-        for (int e = row; e < BT * kPairsPerPass; e += kSoftmaxThreads) {
-          const int et = e / kPairsPerPass, i = pass * kPairsPerPass + e % kPairsPerPass;
-          float c, s;
-          rope_angle(pos0 + (float)et, p.freqs.hi[i], p.freqs.lo[i], p.freqs, &c, &s);
-          table[e] = make_float2(c, s);
-        }
-        softmax_sync();
-#pragma unroll
-        for (int k = 0; k < kPairsPerPass; ++k) {
-          const int i = pass * kPairsPerPass + k;
-          const float2 cs = table[tl * kPairsPerPass + k];
-          const float x1 = x[i], x2 = x[i + D / 2];
-          x[i] = x1 * cs.x - x2 * cs.y;
-          x[i + D / 2] = x2 * cs.x + x1 * cs.y;
-        }
-        softmax_sync();
-      }
-#pragma unroll
-      for (int rg = 0; rg < Lay::kRegions; ++rg)
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float* y = &x[rg * 64 + c * 8];
-          sts128(q_row + rg * kRegionBytes + sw128(row, c),
-                 make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
-                            pack_bf16(y[6], y[7])));
-        }
-    }
-    tc::fence_proxy_async();
-    mbar_arrive(&bars[kQReady]);
-
-    // ---- main loop over KV tiles
-    float m = kNegInf, l = 0.f;
-    const int cta_min_lim = r.cached + t0;
-    const uint32_t p_row = sbase + Lay::kP;
-    for (int j = 0; j < nk && ok; ++j) {
-      if (!wait_warp(&bars[kSFull0 + (j & 1)], (j >> 1) & 1)) { ok = false; break; }
-      tc::fence_after();
-      float s[kKeys];
-#pragma unroll
-      for (int c = 0; c < kKeys / 32; ++c)
-        tc::ld_32x32b_x32(lane_base + (uint32_t)(j & 1) * 128 + c * 32, reinterpret_cast<uint32_t*>(s + c * 32));
-      tc::wait_ld();
-      const int kv0 = j * kKeys;
-      // raw scores; keys past this row's causal limit become -inf (select, so
-      // arbitrary bits in keys past the sequence end cannot leak through)
-      if (kv0 + kKeys - 1 > cta_min_lim) {
-#pragma unroll
-        for (int c = 0; c < kKeys; ++c) s[c] = (kv0 + c <= lim) ? s[c] : kNegInf;
-      }
-      // row max with 8 independent chains (one warp per SM sub-partition:
-      // latency is hidden by instruction-level parallelism only)
-      float mx[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mx[e] = s[e];
-#pragma unroll
-      for (int c = 8; c < kKeys; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
-      // Reference max for the exponentials: moved only when the row max grows
-      // by more than 2^8 (P stays <= 256, exact after the final division by l),
-      // so O is rescaled in TMEM rarely.  Tile 0 always sets it (key 0 is
-      // visible to every row, so mt is finite there).
-      const bool grow = (j == 0) || (mt > m + kRescaleThreshold);
-      const float m_new = grow ? fmaxf(m, mt) : m;
-      const float alpha = fast_exp2(m - m_new);  // 0 on tile 0, 1 when not growing
-      const float neg_m = -m_new;
-      float acc[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-#pragma unroll
-      for (int c = 0; c < kKeys; ++c) {
-        s[c] = fast_exp2(fmaf(s[c], p.scale_log2, neg_m));  // exp2(-inf) = 0
-        acc[c & 7] += s[c];
-      }
-      const float rs = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-      l = l * alpha + rs;
-      m = m_new;
-      if (j >= 1) {
-        // P.V of the previous tile must be complete before O or P is touched
-        if (!wait_warp(&bars[kODone], (j - 1) & 1)) { ok = false; break; }
+    TileWalk w;
+    w.start(p);
+    int g = 0;  // KV tiles processed so far
+    while (w.valid && ok) {
+      const Item it = w.it;
+      w.next_item(p);  // the next item's bounds load while this item runs
+      const int tl = row >> p.log2G;
+      const int tok = it.t0 + tl;
+      const int h = it.kh * G + (row & (G - 1));
+      const int lim = tok < it.n_b ? it.cached + tok : it.kv_total - 1;  // last key this row sees
+      const int cta_min_lim = it.cached + it.t0;
+      float m = kNegInf, l = 0.f;
+      for (int j = 0; j < it.nk; ++j, ++g) {
+        if (!wait_warp(&bars[kSFull0 + (g & 1)], (g >> 1) & 1)) { ok = false; break; }
         tc::fence_after();
-        // warp-uniform: lanes whose reference max did not move multiply by 1
-        if (__any_sync(0xffffffffu, alpha < 1.f)) {
+        const uint32_t s_tmem = lane_base + (uint32_t)(g & 1) * 128;
+        const int kv0 = j * kKeys;
+        // keys past this row's causal limit count as -inf (select, so arbitrary
+        // bits in keys past the sequence end cannot leak through)
+        const bool masked = kv0 + kKeys - 1 > cta_min_lim;
+        const int lim_rel = lim - kv0;  // columns c <= lim_rel are visible
+        uint32_t sr[kKeys];
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tc::ld_32x32b_x32(lane_base + 256 + c * 32, o);
-            tc::wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tc::st_32x32b_x32(lane_base + 256 + c * 32, o);
-          }
-          tc::wait_st();
-        }
-      }
-      if (kv0 + kKeys > kv_total) {
-        // keys past the end of the sequence hold arbitrary bits: zero those V rows
-        if (!wait_warp(&bars[kVFull0 + (j & 1)], (j >> 1) & 1)) { ok = false; break; }
-        if (kv0 + row >= kv_total) {
-          const uint32_t v_addr = sbase + Lay::kV + (j & 1) * Lay::kTile;
-#pragma unroll
-          for (int rg = 0; rg < Lay::kRegions; ++rg)
-#pragma unroll
-            for (int c = 0; c < 8; ++c) sts128(v_addr + rg * kRegionBytes + sw128(row, c), make_uint4(0, 0, 0, 0));
-        }
-      }
-#pragma unroll
-      for (int rg = 0; rg < 2; ++rg)
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float* y = &s[rg * 64 + c * 8];
-          sts128(p_row + rg * kRegionBytes + sw128(row, c),
-                 make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
-                            pack_bf16(y[6], y[7])));
-        }
-      tc::fence_proxy_async();
-      tc::fence_before();
-      mbar_arrive(&bars[kPFull]);
-    }
-    // ---- epilogue: O / l -> bf16 rows of out
-    if (ok) ok = wait_warp(&bars[kODone], (nk - 1) & 1);
-    tc::fence_after();
-    if (ok) {  // warp-uniform; only the stores depend on the row
-      const float inv_l = 1.f / l;
-      const bool store = tok < n_b;
-      uint16_t* dst = p.out + (int64_t)(tokbase + (store ? tok : 0)) * p.Hq * D + (int64_t)h * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tc::ld_32x32b_x32(lane_base + 256 + c * 32, o);
+        for (int c = 0; c < kKeys / 32; ++c) tc::ld_32x32b_x32(s_tmem + c * 32, sr + c * 32);
         tc::wait_ld();
-        if (!store) continue;
+        if (masked) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+          for (int c = 0; c < kKeys; ++c) sr[c] = c <= lim_rel ? sr[c] : __float_as_uint(kNegInf);
+        }
+        // row max, 8 independent chains (instruction-level parallelism)
+        float mx[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx[e] = __uint_as_float(sr[e]);
+#pragma unroll
+        for (int c = 8; c < kKeys; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(sr[c]));
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
+        // Reference max: moved only when the row max grows by more than 2^8
+        // (P stays <= 256, exact after the final division by l).  The first
+        // tile always sets it (key 0 is visible to every row).
+        const bool grow = (j == 0) || (mt > m + kRescaleThreshold);
+        const float m_new = grow ? fmaxf(m, mt) : m;
+        const float alpha = fast_exp2(m - m_new);  // 0 on the first tile, 1 when not moving
+        const float neg_m = -m_new;
+        // P = exp2(s * scale - m) as bf16 pairs into this tile's TMEM P buffer
+        // (free: the P.V that last read it completed before the previous tile
+        // arrived here), row sum in 8 chains
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        const uint32_t p_tmem = lane_base + kTmemP + (uint32_t)(g & 1) * 64;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int c = h * 64 + 2 * e;
+            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c]), p.scale_log2, neg_m));  // exp2(-inf) = 0
+            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c + 1]), p.scale_log2, neg_m));
+            acc[(2 * e) & 7] += p0;
+            acc[(2 * e + 1) & 7] += p1;
+            pk[e] = pack_bf16(p0, p1);
+          }
+          tc::st_32x32b_x32(p_tmem + h * 32, pk);
+        }
+        const float rs = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+        l = l * alpha + rs;
+        m = m_new;
+        if (j >= 1) {
+          // O may only be rescaled once the previous tile's P.V is complete
+          if (!wait_warp(&bars[kODone], (g - 1) & 1)) { ok = false; break; }
+          tc::fence_after();
+          if (__any_sync(0xffffffffu, alpha < 1.f)) {  // warp-uniform
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tc::ld_32x32b_x32(lane_base + kTmemO + c * 32, o);
+              tc::wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tc::st_32x32b_x32(lane_base + kTmemO + c * 32, o);
+            }
+          }
+        }
+        tc::wait_st();
+        if (kv0 + kKeys > it.kv_total) {
+          // keys past the end of the sequence hold arbitrary bits: zero those V rows
+          if (!wait_warp(&bars[kVFull0 + (g & 1)], (g >> 1) & 1)) { ok = false; break; }
+          if (kv0 + row >= it.kv_total) {
+            const uint32_t v_addr = sbase + Lay::kV + (g & 1) * Lay::kTile;
+#pragma unroll
+            for (int rg = 0; rg < Lay::kRegions; ++rg)
+#pragma unroll
+              for (int c = 0; c < 8; ++c) sts128(v_addr + rg * kRegionBytes + sw128(row, c), make_uint4(0, 0, 0, 0));
+          }
+          tc::fence_proxy_async();
+        }
+        tc::fence_before();
+        mbar_arrive(&bars[kPFull]);
+      }
+      if (!ok) break;
+      // ---- item epilogue: O / l -> bf16 rows of out (P.V of its last tile done)
+      if (!wait_warp(&bars[kODone], (g - 1) & 1)) { ok = false; break; }
+      tc::fence_after();
+      const float inv_l = 1.f / l;
+      const bool store = tok < it.n_b;
+      uint16_t* dst = p.out + (int64_t)(it.tokbase + (store ? tok : 0)) * p.Hq * D + (int64_t)h * D;
+      uint32_t o[D];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tc::ld_32x32b_x32(lane_base + kTmemO + c * 32, o + c * 32);
+      tc::wait_ld();
+      // the O reads above are complete before the next item's first P.V overwrites O
+      tc::fence_before();
+      if (store) {
+#pragma unroll
+        for (int q = 0; q < D / 8; ++q) {
           uint4 v;
           v.x = pack_bf16(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
           v.y = pack_bf16(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
           v.z = pack_bf16(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
           v.w = pack_bf16(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
-          *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) = v;
+          *reinterpret_cast<uint4*>(dst + q * 8) = v;
         }
       }
-    } else {
-      set_status(p.status, ATTN_STATUS_TIMEOUT);
     }
+    if (!ok) set_status(p.status, ATTN_STATUS_TIMEOUT);
   }
 
   tc::fence_before();
@@ -452,11 +489,12 @@ int launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream) {
   using Lay = TcLayout<D>;
   const int Hq = a.cfg.num_q_heads, Hkv = a.cfg.num_kv_heads;
   const int G = Hq / Hkv;
+  const int log2G = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
   const int BT = kRows / G;
   CacheMaps maps;
   if (make_cache_maps(a.kv, Hkv, D, kKeys, &maps) != 0) return ATTN_ELAUNCH;
-  CUtensorMap qmap;
-  if (make_qkv_map(a.qkv, a.N, Hq + 2 * Hkv, D, G, BT, &qmap) != 0) return ATTN_ELAUNCH;
+  CUtensorMap qmap;  // prepared Q viewed as [N, Hq, D]
+  if (make_qkv_map(a.q, a.N, Hq, D, G, BT, &qmap) != 0) return ATTN_ELAUNCH;
   TcPar p;
   p.cu_seqlens = a.cu_seqlens;
   p.slot_base = a.kv.slot_base;
@@ -465,17 +503,25 @@ int launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream) {
   p.num_slots = a.kv.num_slots;
   p.status = a.status;
   p.out = static_cast<uint16_t*>(a.out);
-  p.q_norm_w = static_cast<const uint16_t*>(a.q_norm_w);
-  p.freqs = a.freqs;
-  p.eps = a.cfg.rms_eps;
   p.scale_log2 = 1.4426950408889634f / sqrtf((float)D);
   p.Hq = Hq;
-  p.log2G = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
+  p.Hkv = Hkv;
+  p.log2G = log2G;
+  p.log2BT = 7 - log2G;
   p.N = a.N;
+  p.B = a.B;
+  p.max_seqlen = a.max_seqlen;
+  const int64_t nv = ((int64_t)(a.N >> p.log2BT) + a.B) * Hkv;
+  if (nv > (int64_t(1) << 30)) return ATTN_EINVAL;
+  p.num_vitems = (int)nv;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return ATTN_ELAUNCH;
   if (cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Lay::kSmemBytes) != cudaSuccess)
     return ATTN_ELAUNCH;
-  const dim3 grid((a.max_seqlen + BT - 1) / BT, Hkv, a.B);
+  const int grid = (int)std::min<int64_t>(sms, nv);
   prefill_tc_kernel<D><<<grid, kThreads, Lay::kSmemBytes, stream>>>(qmap, maps.k, maps.v, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
 }

@@ -1,14 +1,13 @@
-// KV append: split the K and V heads out of qkv, RMSNorm + RoPE on K, write
-// K and V to the cache.
+// Prologue of the attention step: split qkv, RMSNorm + RoPE on K (and on Q
+// when a Q output is given), write K and V to the cache (and the prepared Q).
 //
 // Zero-to-sglang Ch.3 code walkthrough, section 3.3: AttentionLayer.forward
-// splits the merged projection into Q, K and V, applies RMSNorm to each K head's
-// last dimension and RoPE at each token's position (V is not rotated);
+// splits the merged projection into Q, K and V, applies RMSNorm to each Q/K
+// head's last dimension and RoPE at each token's position (V is not rotated);
 // transformer-basics "Prefill vs Decode": the new K/V are appended to the
-// per-layer cache (past_key_values.update).  Q is normalised and rotated by
-// the attention kernels themselves when they load it.  One pass: every
-// (token, KV head) vector of D bf16 values is read once with 16-byte loads by
-// a group of D/8 lanes, reduced with warp shuffles, and written once.
+// per-layer cache (past_key_values.update).  One pass: every (token, head)
+// vector of D bf16 values is read once with 16-byte loads by a group of D/8
+// lanes, reduced with warp shuffles, and written once.
 #include "kernels.cuh"
 
 namespace gb300 {
@@ -20,7 +19,9 @@ constexpr int kThreads = 256;
 
 struct ProloguePar {
   const uint16_t* __restrict__ qkv;        // [N, W] bf16
+  const uint16_t* __restrict__ q_norm_w;   // [D] bf16 (used when q_out != NULL)
   const uint16_t* __restrict__ k_norm_w;   // [D] bf16
+  uint16_t* __restrict__ q_out;            // [N, Hq, D] bf16 or NULL
   const int32_t* cu_seqlens;  // [B+1] or NULL: token b is request b (decode)
   uint16_t* __restrict__ k_cache;
   uint16_t* __restrict__ v_cache;
@@ -43,7 +44,7 @@ __global__ void __launch_bounds__(kThreads) kv_append_kernel(const ProloguePar p
   __shared__ float s_sin[kTokPerBlock][HALF];
   __shared__ int64_t s_slot[kTokPerBlock];
   __shared__ float s_pos[kTokPerBlock];
-  __shared__ int s_ok[kTokPerBlock];  // token may write the cache
+  __shared__ int s_ok[kTokPerBlock];  // 1: token exists; 2: it may also write the cache
 
   const int t0 = blockIdx.x * kTokPerBlock;
   if (threadIdx.x < kTokPerBlock) {
@@ -69,10 +70,11 @@ __global__ void __launch_bounds__(kThreads) kv_append_kernel(const ProloguePar p
       if (seq_ok) {
         const ReqInfo r = load_request(p.slot_base + b, p.cache_lens + b, p.slot_capacity + b,
                                        p.num_slots, n);
+        ok = 1;
+        pos = (float)(r.cached + j);
         if (r.valid) {
-          ok = 1;
+          ok = 2;
           slot = r.slot0 + r.cached + j;
-          pos = (float)(r.cached + j);
         } else {
           set_status(p.status, ATTN_STATUS_CAPACITY);
         }
@@ -101,8 +103,11 @@ __global__ void __launch_bounds__(kThreads) kv_append_kernel(const ProloguePar p
   const bool first_half = li < L / 2;
   const int pair0 = (first_half ? li : li - L / 2) * 8;  // first rotation pair of this lane
   const uint4 kw4 = __ldg(reinterpret_cast<const uint4*>(p.k_norm_w + li * 8));
+  const uint4 qw4 = p.q_out ? __ldg(reinterpret_cast<const uint4*>(p.q_norm_w + li * 8)) : kw4;
 
-  const int nhead = 2 * p.Hkv;  // K heads then V heads
+  // heads of a token handled here: K heads, V heads, then (with q_out) Q heads
+  const int nq = p.q_out ? p.Hq : 0;
+  const int nhead = 2 * p.Hkv + nq;
   const int ntask = kTokPerBlock * nhead;
   constexpr int kMaxTasks = 8;  // tasks per group held in flight (loads issued first)
   for (int base = 0; base < ntask; base += kGroups * kMaxTasks) {
@@ -113,9 +118,12 @@ __global__ void __launch_bounds__(kThreads) kv_append_kernel(const ProloguePar p
       raw[k] = make_uint4(0, 0, 0, 0);
       if (task < ntask) {
         const int tk = task / nhead, hd = task % nhead;
-        if (s_ok[tk])
-          raw[k] = __ldg(reinterpret_cast<const uint4*>(
-              p.qkv + (int64_t)(t0 + tk) * W + (int64_t)(p.Hq + hd) * D + li * 8));
+        // Q heads are prepared even for a request whose cache region is too
+        // small (s_ok == 1): only the cache writes are withheld there
+        const int col = hd < 2 * p.Hkv ? p.Hq + hd : hd - 2 * p.Hkv;
+        if (s_ok[tk] == 2 || (s_ok[tk] == 1 && hd >= 2 * p.Hkv))
+          raw[k] = __ldg(reinterpret_cast<const uint4*>(p.qkv + (int64_t)(t0 + tk) * W +
+                                                          (int64_t)col * D + li * 8));
       }
     }
 #pragma unroll
@@ -123,11 +131,13 @@ __global__ void __launch_bounds__(kThreads) kv_append_kernel(const ProloguePar p
       const int task = base + group + k * kGroups;  // whole groups move together
       if (task >= ntask) break;
       const int tk = task / nhead, hd = task % nhead;
-      if (!s_ok[tk]) continue;
+      const bool is_q = hd >= 2 * p.Hkv;
+      if (s_ok[tk] == 0 || (!is_q && s_ok[tk] != 2)) continue;
       const bool is_k = hd < p.Hkv;
       const int kvh = is_k ? hd : hd - p.Hkv;
-      const int64_t dst = (s_slot[tk] * p.Hkv + kvh) * D + li * 8;
-      if (!is_k) {  // V: bit copy into the cache
+      const int64_t dst = is_q ? ((int64_t)(t0 + tk) * p.Hq + (hd - 2 * p.Hkv)) * D + li * 8
+                               : (s_slot[tk] * p.Hkv + kvh) * D + li * 8;
+      if (!is_k && !is_q) {  // V: bit copy into the cache
         *reinterpret_cast<uint4*>(p.v_cache + dst) = raw[k];
         continue;
       }
@@ -144,7 +154,7 @@ __global__ void __launch_bounds__(kThreads) kv_append_kernel(const ProloguePar p
 #pragma unroll
       for (int off = L / 2; off >= 1; off >>= 1) ss += __shfl_xor_sync(gmask, ss, off);
       const float inv = rsqrtf(ss * (1.0f / D) + p.eps);
-      const uint32_t* ww = reinterpret_cast<const uint32_t*>(&kw4);
+      const uint32_t* ww = reinterpret_cast<const uint32_t*>(is_q ? &qw4 : &kw4);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         x[2 * e] = bf16_lo(ww[e]) * (x[2 * e] * inv);
@@ -168,7 +178,7 @@ __global__ void __launch_bounds__(kThreads) kv_append_kernel(const ProloguePar p
         }
         o[e / 2] = pack_bf16(r0, r1);
       }
-      *reinterpret_cast<uint4*>(p.k_cache + dst) = make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>((is_q ? p.q_out : p.k_cache) + dst) = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
 }
@@ -179,7 +189,9 @@ cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t stream) {
   if (a.N <= 0) return cudaSuccess;
   ProloguePar p;
   p.qkv = static_cast<const uint16_t*>(a.qkv);
+  p.q_norm_w = static_cast<const uint16_t*>(a.q_norm_w);
   p.k_norm_w = static_cast<const uint16_t*>(a.k_norm_w);
+  p.q_out = static_cast<uint16_t*>(a.q_out);
   p.cu_seqlens = a.cu_seqlens;
   p.k_cache = static_cast<uint16_t*>(a.kv.k_cache);
   p.v_cache = static_cast<uint16_t*>(a.kv.v_cache);

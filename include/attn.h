@@ -108,8 +108,9 @@ enum {
 /* Workspace bytes needed by any call with at most `max_tokens` new tokens,
  * `max_batch` requests and `max_kv_len` keys per request (c_b + n_b).  The
  * workspace is a caller-owned device buffer, 256-byte aligned: a 256-byte
- * header holding the status word, then (decode only) the split-KV partial
- * results.  Returns 0 for invalid arguments. */
+ * header holding the status word, then the prepared Q of attn_prefill
+ * (N * Hq * D bf16) or the split-KV partial results of attn_decode.  Returns
+ * 0 for invalid arguments. */
 ATTN_API size_t attn_workspace_size(const attn_config_t* cfg, int32_t max_tokens, int32_t max_batch,
                            int32_t max_kv_len);
 
@@ -125,14 +126,25 @@ ATTN_API int attn_kv_append(const attn_config_t* cfg, const void* qkv, const voi
                    const void* k_norm_w, const int32_t* cu_seqlens, int32_t B, int32_t N,
                    const attn_kv_t* kv, void* workspace, size_t ws_bytes, void* stream);
 
-/* Attention half of attn_prefill: the cache must already hold this call's
- * K/V (attn_kv_append with the same arguments, earlier on the stream).  Q is
- * read from qkv and normalised and rotated inside the attention kernel.
- * attn_prefill == attn_kv_append followed by attn_prefill_attend. */
-ATTN_API int attn_prefill_attend(const attn_config_t* cfg, const void* qkv, const void* q_norm_w,
-                                 const int32_t* cu_seqlens, int32_t B, int32_t N,
-                                 int32_t max_seqlen, const attn_kv_t* kv, void* out,
-                                 void* workspace, size_t ws_bytes, void* stream);
+/* First half of attn_prefill: split qkv, RMSNorm + RoPE on Q and K, append
+ * K and V to the cache, and write the prepared (normed, rotated, bf16) Q to
+ * q_out [N, Hq, D] (device, caller-owned, 16-byte aligned).  cu_seqlens,
+ * B, N and kv as for attn_prefill.  Code walkthrough section 3.3; basics
+ * "Attention calculation: part 1" (q_norm / k_norm after .view) and "Prefill
+ * vs Decode" (past_key_values.update). */
+ATTN_API int attn_prefill_prepare(const attn_config_t* cfg, const void* qkv, const void* q_norm_w,
+                                  const void* k_norm_w, const int32_t* cu_seqlens, int32_t B,
+                                  int32_t N, const attn_kv_t* kv, void* q_out, void* workspace,
+                                  size_t ws_bytes, void* stream);
+
+/* Second half of attn_prefill: causal GQA over the prepared Q [N, Hq, D]
+ * (from attn_prefill_prepare) and the cache, which must already hold this
+ * call's K/V.  Writes out [N, Hq*D].  The workspace needs only its 256-byte
+ * header here.  attn_prefill == attn_prefill_prepare (q_out in the workspace)
+ * followed by attn_prefill_attend. */
+ATTN_API int attn_prefill_attend(const attn_config_t* cfg, const void* q, const int32_t* cu_seqlens,
+                                 int32_t B, int32_t N, int32_t max_seqlen, const attn_kv_t* kv,
+                                 void* out, void* workspace, size_t ws_bytes, void* stream);
 
 /* Prefill over ragged packed sequences: the whole step for the N new tokens
  * of B requests (request b's tokens are rows cu_seqlens[b] .. cu_seqlens[b+1]-1

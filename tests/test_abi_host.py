@@ -26,6 +26,7 @@ def declared_functions():
 def test_header_declares_the_calls():
     names = declared_functions()
     for n in ("attn_prefill", "attn_decode", "attn_kv_append", "attn_workspace_size",
+              "attn_prefill_prepare", "attn_prefill_attend", "attn_decode_attend",
               "attn_get_status", "attn_strerror", "attn_workspace_init"):
         assert n in names
 
@@ -49,8 +50,8 @@ def test_strerror(lib):
 def test_workspace_size(lib):
     from causal_gqa_attention_qkv_gb300 import attn
     cfg = attn.config(32, 8, 128)
-    # prefill needs only the 256-byte status header; decode adds split partials
-    assert attn.workspace_size(cfg, 4096, 0, 4096) == 256
+    # prefill: 256-byte status header + the prepared Q; decode: header + split partials
+    assert attn.workspace_size(cfg, 4096, 0, 4096) == 256 + 4096 * 32 * 128 * 2
     c = attn.workspace_size(cfg, 16, 64, 16384)
     d = attn.workspace_size(cfg, 16, 8, 4096)
     assert 256 < d < c
@@ -92,6 +93,7 @@ def test_null_and_alignment_rejected(lib):
     assert call(fake, fake, 1 << 20, n=-1) == -1    # negative N
     assert call(fake, None, 1 << 20) == -3          # no workspace
     assert call(fake, fake, 100) == -3              # workspace too small
+    assert call(fake, fake, 256 + 4 * 8 * 64 * 2 - 16) == -3  # no room for the prepared Q
     assert call(fake, ctypes.c_void_p((1 << 20) + 16), 1 << 20) == -3  # not 256-aligned
     assert call(fake, fake, 1 << 20, kvp=None) == -1  # no cache
     bad_kv = attn.AttnKV(1 << 20, 1 << 20, 0, 1 << 20, 1 << 20, 1 << 20)
@@ -106,4 +108,4 @@ def test_decode_split_mirror_matches_library(lib, B, max_kv):
     ms = attn.decode_max_splits(B, 8, max_kv)
     al = lambda x: (x + 255) // 256 * 256
     expect = 256 + al(B * 32 * ms * 128 * 4) + al(B * 32 * ms * 2 * 4)
-    assert attn.workspace_size(cfg, 1, B, max_kv) == expect
+    assert attn.workspace_size(cfg, 1, B, max_kv) == max(expect, 256 + al(32 * 128 * 2))
