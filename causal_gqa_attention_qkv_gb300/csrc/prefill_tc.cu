@@ -289,24 +289,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       pv.start(p);
       int gq = 0, gp = 0;  // next tile for S = Q K^T, next tile for P.V
       // S of tile gq may be issued once P of tile gq - 2 has been seen (its S
-      // buffer is free); `ready` reports whether its K (and, on an item's first
-      // tile, its prepared Q) are in shared memory without waiting.
-      auto qk_ready = [&]() -> bool {
-        if (qk.j == 0 && !mbar_try_wait(&bars[kQFull0 + qk.k % kQBufs], (qk.k / kQBufs) & 1)) return false;
-        return mbar_try_wait(&bars[kKFull0 + (gq & 1)], (gq >> 1) & 1);
-      };
-      auto issue_qk = [&]() -> bool {
+      // buffer is free).  issue_qk(block): with block == false it returns
+      // false (issuing nothing) when the tile's K, or on an item's first tile
+      // its Q, is not in shared memory yet.
+      auto issue_qk = [&](bool block) -> bool {
         const int st = gq & 1, qs = qk.k % kQBufs;
-        if (qk.j == 0 && !mbar_wait(&bars[kQFull0 + qs], (qk.k / kQBufs) & 1)) return false;
-        if (!mbar_wait(&bars[kKFull0 + st], (gq >> 1) & 1)) return false;
+        if (qk.j == 0) {
+          uint64_t* qb = &bars[kQFull0 + qs];
+          const uint32_t qpar = (qk.k / kQBufs) & 1;
+          if (block ? !mbar_wait(qb, qpar) : !mbar_try_wait(qb, qpar)) {
+            if (block) ok = false;
+            return false;
+          }
+        }
+        uint64_t* kb = &bars[kKFull0 + st];
+        if (block ? !mbar_wait(kb, (gq >> 1) & 1) : !mbar_try_wait(kb, (gq >> 1) & 1)) {
+          if (block) ok = false;
+          return false;
+        }
         tc::fence_after();
         const uint32_t q_addr = sbase + Lay::kQ + qs * Lay::kTile;
         const uint32_t k_addr = sbase + Lay::kK + st * Lay::kTile;
+        const uint64_t qd = tc::sdesc_sw128(q_addr, 16, 1024), kd = tc::sdesc_sw128(k_addr, 16, 1024);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * kRegionBytes + (ks & 3) * 32;
-          tc::mma_f16_ss(tmem + (uint32_t)st * 128, tc::sdesc_sw128(q_addr + off, 16, 1024),
-                         tc::sdesc_sw128(k_addr + off, 16, 1024), idesc_s, ks > 0);
+          const uint64_t off = (uint64_t)(((ks >> 2) * kRegionBytes + (ks & 3) * 32) >> 4);
+          tc::mma_f16_ss(tmem + (uint32_t)st * 128, qd + off, kd + off, idesc_s, ks > 0);
         }
         tc::commit(&bars[kSFull0 + st]);
         tc::commit(&bars[kKEmpty0 + st]);
@@ -316,30 +324,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       while (pv.valid && ok) {
-        // the S that P.V of tile gp consumes must be under way (blocking) ...
-        while (ok && qk.valid && gq <= gp) ok = issue_qk();
+        // the S that P.V of tile gp consumes must be under way (blocking)
+        while (ok && qk.valid && gq <= gp) issue_qk(true);
         if (!ok) break;
-        // ... the next one too, if it is loaded
-        if (qk.valid && gq == gp + 1 && qk_ready() && !(ok = issue_qk())) break;
         if (!mbar_wait(&bars[kPFull], gp & 1)) { ok = false; break; }
         tc::fence_after();
-        // S buffers of tiles up to gp + 2 are free now: issue what is loaded
-        while (ok && qk.valid && gq <= gp + 2 && qk_ready()) ok = issue_qk();
-        if (!ok) break;
+        // P.V of tile gp first: the softmax of the next tile waits for it
         const int st = gp & 1;
         if (!mbar_wait(&bars[kVFull0 + st], (gp >> 1) & 1)) { ok = false; break; }
         tc::fence_after();
-        const uint32_t v_addr = sbase + Lay::kV + st * Lay::kTile;
         const uint32_t p_tmem = tmem + kTmemP + (uint32_t)st * 64;
+        const uint64_t vd = tc::sdesc_sw128(sbase + Lay::kV + st * Lay::kTile, kRegionBytes, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
-          const uint64_t bd = tc::sdesc_sw128(v_addr + kk * 2048, kRegionBytes, 1024);
-          tc::mma_f16_ts(o_tmem, p_tmem + kk * 8, bd, idesc_o, (pv.j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kKeys / 16; ++kk)
+          tc::mma_f16_ts(o_tmem, p_tmem + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), idesc_o,
+                         (pv.j > 0 || kk > 0) ? 1u : 0u);
         tc::commit(&bars[kODone]);
         tc::commit(&bars[kVEmpty0 + st]);
         ++gp;
         pv.next_tile(p);
+        // then S of the tiles up to gp + 1 (their S buffers are free) that are loaded
+        while (ok && qk.valid && gq <= gp + 1 && issue_qk(false)) {
+        }
       }
       // Nothing may still be running on the tensor cores when TMEM is freed.
       tc::commit(&bars[kMmaDone]);
