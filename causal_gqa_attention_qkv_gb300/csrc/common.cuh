@@ -160,8 +160,8 @@ struct RopeFreqs {
 // cos and sin of pos * f for f = hi + lo: float-float product (pos is an
 // exact integer below 2^24, so one fma recovers the rounding error of pos*hi
 // exactly), then Cody-Waite additive range reduction modulo 2*pi with 2*pi
-// split into two floats, then sincosf on |r| <= pi.  The angle keeps about
-// 1e-7 rad absolute error at any position.
+// split into two floats, then the hardware sin/cos on |r| <= pi.  The angle
+// keeps about 1e-7 rad absolute error at any position; cos/sin about 4e-7.
 __device__ __forceinline__ void rope_angle(float pos, float f_hi, float f_lo, const RopeFreqs& fr,
                                            float* c, float* s) {
   const float a_hi = pos * f_hi;
@@ -171,7 +171,7 @@ __device__ __forceinline__ void rope_angle(float pos, float f_hi, float f_lo, co
   float r = fmaf(-k, fr.two_pi_hi, a_hi);
   r = fmaf(-k, fr.two_pi_lo, r);
   r += a_lo;
-  sincosf(r, s, c);
+  __sincosf(r, s, c);  // |r| <= pi + 1e-6: hardware sin/cos, absolute error ~4e-7
 }
 
 // One query row (D bf16 values at `row`) normalised and rotated, delivered in

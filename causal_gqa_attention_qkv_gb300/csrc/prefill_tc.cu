@@ -78,8 +78,12 @@ struct TcLayout {
 
 enum Bar {
   kQFull0 = 0, kQEmpty0 = kQFull0 + kQBufs,
-  kKFull0 = kQEmpty0 + kQBufs, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVEmpty0, kVEmpty1,
-  kSFull0, kSFull1, kPFull, kODone, kMmaDone
+  kKFull0 = kQEmpty0 + kQBufs, kKFull1, kVFull0, kVFull1,
+  // kSFull + st: S of a tile using K stage st is complete, which also frees
+  // that K stage; kPvDone + st: P.V of a tile using V stage st is complete
+  // (O updated, P buffer st and V stage st free).  Each advances one phase per
+  // use of its stage, so no waiter can fall two phases behind.
+  kSFull0, kSFull1, kPvDone0, kPvDone1, kPFull, kMmaDone
 };
 
 // ---------------------------------------------------------------- work items
@@ -196,13 +200,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[kKFull0 + s], 1);
-      mbar_init(&bars[kKEmpty0 + s], 1);
       mbar_init(&bars[kVFull0 + s], 1);
-      mbar_init(&bars[kVEmpty0 + s], 1);
       mbar_init(&bars[kSFull0 + s], 1);
+      mbar_init(&bars[kPvDone0 + s], 1);
     }
     mbar_init(&bars[kPFull], kSoftmaxThreads);
-    mbar_init(&bars[kODone], 1);
     mbar_init(&bars[kMmaDone], 1);
     fence_barrier_init();
   }
@@ -248,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         qw.next_item(p);
         return true;
       };
-      const int full0 = kstream ? kKFull0 : kVFull0, empty0 = kstream ? kKEmpty0 : kVEmpty0;
+      const int full0 = kstream ? kKFull0 : kVFull0, empty0 = kstream ? kSFull0 : kPvDone0;
       const int base = kstream ? Lay::kK : Lay::kV;
       const CUtensorMap* map = kstream ? &kmap : &vmap;
       while (w.valid && ok) {
@@ -316,8 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t off = (uint64_t)(((ks >> 2) * kRegionBytes + (ks & 3) * 32) >> 4);
           tc::mma_f16_ss(tmem + (uint32_t)st * 128, qd + off, kd + off, idesc_s, ks > 0);
         }
-        tc::commit(&bars[kSFull0 + st]);
-        tc::commit(&bars[kKEmpty0 + st]);
+        tc::commit(&bars[kSFull0 + st]);  // S ready, K stage st free
         if (qk.j == qk.it.nk - 1) tc::commit(&bars[kQEmpty0 + qs]);  // last use of this Q tile
         ++gq;
         qk.next_tile(p);
@@ -339,8 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < kKeys / 16; ++kk)
           tc::mma_f16_ts(o_tmem, p_tmem + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), idesc_o,
                          (pv.j > 0 || kk > 0) ? 1u : 0u);
-        tc::commit(&bars[kODone]);
-        tc::commit(&bars[kVEmpty0 + st]);
+        tc::commit(&bars[kPvDone0 + st]);  // O updated, P buffer and V stage st free
         ++gp;
         pv.next_tile(p);
         // then S of the tiles up to gp + 1 (their S buffers are free) that are loaded
@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         m = m_new;
         if (j >= 1) {
           // O may only be rescaled once the previous tile's P.V is complete
-          if (!wait_warp(&bars[kODone], (g - 1) & 1)) { ok = false; break; }
+          if (!wait_warp(&bars[kPvDone0 + ((g - 1) & 1)], ((g - 1) >> 1) & 1)) { ok = false; break; }
           tc::fence_after();
           if (__any_sync(0xffffffffu, alpha < 1.f)) {  // warp-uniform
 #pragma unroll 1
@@ -458,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // ---- item epilogue: O / l -> bf16 rows of out (P.V of its last tile done)
-      if (!wait_warp(&bars[kODone], (g - 1) & 1)) { ok = false; break; }
+      if (!wait_warp(&bars[kPvDone0 + ((g - 1) & 1)], ((g - 1) >> 1) & 1)) { ok = false; break; }
       tc::fence_after();
       const float inv_l = 1.f / l;
       const bool store = tok < it.n_b;

@@ -36,7 +36,7 @@ struct ProloguePar {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads) kv_append_kernel(const ProloguePar p) {
+__global__ void __launch_bounds__(kThreads, 4) kv_append_kernel(const ProloguePar p) {
   constexpr int L = D / 8;     // lanes per head vector (8 bf16 = 16 bytes each)
   constexpr int HALF = D / 2;  // rotation pairs
   constexpr int kGroups = kThreads / L;
@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kThreads) kv_append_kernel(const ProloguePar p
   const int nq = p.q_out ? p.Hq : 0;
   const int nhead = 2 * p.Hkv + nq;
   const int ntask = kTokPerBlock * nhead;
-  constexpr int kMaxTasks = 8;  // tasks per group held in flight (loads issued first)
+  constexpr int kMaxTasks = 6;  // tasks per group held in flight (loads issued first)
   for (int base = 0; base < ntask; base += kGroups * kMaxTasks) {
     uint4 raw[kMaxTasks];
 #pragma unroll
