@@ -22,11 +22,12 @@
 //              lane 1 loads V (2-stage ring), so that waiting for a free V slot
 //              never delays the next K tile.
 //   warp 5     MMA issuer (one thread) and TMEM owner: S = Q K^T into one of
-//              two TMEM buffers and O += P V.  Once P of tile g is ready it
-//              issues the S of tiles up to g + 2 whose K (and Q) are already
-//              loaded, then P.V of tile g (also across item boundaries).
-// TMEM: columns [0,128) and [128,256) hold S (fp32), [256, 256+D) hold O,
-// [384,448) and [448,512) hold P (bf16 pairs) for P.V with A read from TMEM.
+//              three TMEM buffers and O += P V.  It keeps the S of up to two
+//              tiles ahead queued (as their K and Q arrive) and issues P.V of
+//              tile g as soon as its P is in TMEM (also across item boundaries).
+// TMEM: three S buffers (fp32) in columns [0,384), O in [384, 384+D).  P
+// (bf16 pairs, A operand of P.V read from TMEM) overwrites the first 64
+// columns of its tile's S buffer once the softmax holds S in registers.
 #include "kernels.cuh"
 #include "tcgen05.cuh"
 
@@ -40,10 +41,10 @@ constexpr int kThreads = 192;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kQBufs = 3;  // Q tiles in flight: the current item and the next two
+constexpr int kQBufs = 2;  // Q tiles in flight: the current item and the next
+constexpr int kSBufs = 3;  // S buffers in TMEM = K stages in shared memory
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 256;  // O columns
-constexpr uint32_t kTmemP = 384;  // two P buffers of 64 columns
+constexpr uint32_t kTmemO = 384;  // O columns; [0, 384) hold three S buffers
 constexpr int kRegionBytes = 128 * 128;   // 128 rows x 128 bytes (64 bf16)
 constexpr float kRescaleThreshold = 8.f;  // log2 units: move the reference max past 256x growth
 
@@ -65,8 +66,8 @@ struct TcLayout {
   static constexpr int kRegions = D / 64;
   static constexpr int kTile = kRegions * kRegionBytes;  // Q, K or V tile: 128 rows x D
   static constexpr int kQ = 0;                // kQBufs buffers
-  static constexpr int kK = kQ + kQBufs * kTile;  // 2 stages
-  static constexpr int kV = kK + 2 * kTile;   // 2 stages
+  static constexpr int kK = kQ + kQBufs * kTile;  // kSBufs stages
+  static constexpr int kV = kK + kSBufs * kTile;  // 2 stages
   static constexpr int kBar = kV + 2 * kTile;
   static constexpr int kNumBars = 24;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
@@ -78,12 +79,12 @@ struct TcLayout {
 
 enum Bar {
   kQFull0 = 0, kQEmpty0 = kQFull0 + kQBufs,
-  kKFull0 = kQEmpty0 + kQBufs, kKFull1, kVFull0, kVFull1,
-  // kSFull + st: S of a tile using K stage st is complete, which also frees
-  // that K stage; kPvDone + st: P.V of a tile using V stage st is complete
-  // (O updated, P buffer st and V stage st free).  Each advances one phase per
-  // use of its stage, so no waiter can fall two phases behind.
-  kSFull0, kSFull1, kPvDone0, kPvDone1, kPFull, kMmaDone
+  kKFull0 = kQEmpty0 + kQBufs, kVFull0 = kKFull0 + kSBufs, kVFull1,
+  // kSFull + b: S of a tile in S buffer b (K stage b) is complete, which also
+  // frees that K stage; kPvDone + st: P.V of a tile using V stage st is
+  // complete (O updated, V stage st free).  Each advances one phase per use of
+  // its stage, so no waiter can fall two phases behind.
+  kSFull0, kPvDone0 = kSFull0 + kSBufs, kPvDone1, kPFull, kMmaDone
 };
 
 // ---------------------------------------------------------------- work items
@@ -198,10 +199,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars[kQFull0 + s], 1);
       mbar_init(&bars[kQEmpty0 + s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kSBufs; ++s) {
       mbar_init(&bars[kKFull0 + s], 1);
-      mbar_init(&bars[kVFull0 + s], 1);
       mbar_init(&bars[kSFull0 + s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars[kVFull0 + s], 1);
       mbar_init(&bars[kPvDone0 + s], 1);
     }
     mbar_init(&bars[kPFull], kSoftmaxThreads);
@@ -251,6 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       const int full0 = kstream ? kKFull0 : kVFull0, empty0 = kstream ? kSFull0 : kPvDone0;
+      const int nst = kstream ? kSBufs : 2;  // ring stages
       const int base = kstream ? Lay::kK : Lay::kV;
       const CUtensorMap* map = kstream ? &kmap : &vmap;
       while (w.valid && ok) {
@@ -258,8 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           while (qw.valid && qw.k <= w.k && ok) ok = issue_q();  // this item's Q
           if (!ok) break;
         }
-        const int st = g & 1;
-        if (g >= 2 && !mbar_wait(&bars[empty0 + st], ((g >> 1) & 1) ^ 1)) { ok = false; break; }
+        const int st = g % nst;
+        if (g >= nst && !mbar_wait(&bars[empty0 + st], (g / nst - 1) & 1)) { ok = false; break; }
         mbar_arrive_expect_tx(&bars[full0 + st], Lay::kTile);
 #pragma unroll
         for (int rg = 0; rg < Lay::kRegions; ++rg)
@@ -276,8 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the normal path, where the consumers already waited for them).
       for (int k = max(0, q_issued - kQBufs); k < q_issued; ++k)
         (void)mbar_wait(&bars[kQFull0 + k % kQBufs], (k / kQBufs) & 1);
-      for (int t = max(0, issued - 2); t < issued; ++t)
-        (void)mbar_wait(&bars[full0 + (t & 1)], (t >> 1) & 1);
+      for (int t = max(0, issued - nst); t < issued; ++t)
+        (void)mbar_wait(&bars[full0 + t % nst], (t / nst) & 1);
       if (!ok) set_status(p.status, ATTN_STATUS_TIMEOUT);
     }
   } else if (warp == kMmaWarp) {
@@ -290,12 +294,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       qk.start(p);
       pv.start(p);
       int gq = 0, gp = 0;  // next tile for S = Q K^T, next tile for P.V
-      // S of tile gq may be issued once P of tile gq - 2 has been seen (its S
-      // buffer is free).  issue_qk(block): with block == false it returns
-      // false (issuing nothing) when the tile's K, or on an item's first tile
-      // its Q, is not in shared memory yet.
+      // S of tile gq goes to S buffer gq % 3, K stage gq % 3.  It may be issued
+      // once P.V of tile gq - 3 (which reads its P from that buffer) has been
+      // issued: tensor-core operations run in issue order.  With block ==
+      // false issue_qk returns false, issuing nothing, when the tile's K (or,
+      // on an item's first tile, its Q) is not in shared memory yet.
       auto issue_qk = [&](bool block) -> bool {
-        const int st = gq & 1, qs = qk.k % kQBufs;
+        const int sb = gq % kSBufs, qs = qk.k % kQBufs;
         if (qk.j == 0) {
           uint64_t* qb = &bars[kQFull0 + qs];
           const uint32_t qpar = (qk.k / kQBufs) & 1;
@@ -304,48 +309,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             return false;
           }
         }
-        uint64_t* kb = &bars[kKFull0 + st];
-        if (block ? !mbar_wait(kb, (gq >> 1) & 1) : !mbar_try_wait(kb, (gq >> 1) & 1)) {
+        uint64_t* kb = &bars[kKFull0 + sb];
+        const uint32_t kpar = (gq / kSBufs) & 1;
+        if (block ? !mbar_wait(kb, kpar) : !mbar_try_wait(kb, kpar)) {
           if (block) ok = false;
           return false;
         }
         tc::fence_after();
-        const uint32_t q_addr = sbase + Lay::kQ + qs * Lay::kTile;
-        const uint32_t k_addr = sbase + Lay::kK + st * Lay::kTile;
-        const uint64_t qd = tc::sdesc_sw128(q_addr, 16, 1024), kd = tc::sdesc_sw128(k_addr, 16, 1024);
+        const uint64_t qd = tc::sdesc_sw128(sbase + Lay::kQ + qs * Lay::kTile, 16, 1024);
+        const uint64_t kd = tc::sdesc_sw128(sbase + Lay::kK + sb * Lay::kTile, 16, 1024);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint64_t off = (uint64_t)(((ks >> 2) * kRegionBytes + (ks & 3) * 32) >> 4);
-          tc::mma_f16_ss(tmem + (uint32_t)st * 128, qd + off, kd + off, idesc_s, ks > 0);
+          tc::mma_f16_ss(tmem + (uint32_t)sb * 128, qd + off, kd + off, idesc_s, ks > 0);
         }
-        tc::commit(&bars[kSFull0 + st]);  // S ready, K stage st free
+        tc::commit(&bars[kSFull0 + sb]);  // S ready, K stage sb free
         if (qk.j == qk.it.nk - 1) tc::commit(&bars[kQEmpty0 + qs]);  // last use of this Q tile
         ++gq;
         qk.next_tile(p);
         return true;
       };
       while (pv.valid && ok) {
-        // the S that P.V of tile gp consumes must be under way (blocking)
+        // the S that P.V of tile gp consumes must be under way (blocking) ...
         while (ok && qk.valid && gq <= gp) issue_qk(true);
         if (!ok) break;
+        // ... and S of up to two more tiles, as far as they are loaded
+        while (ok && qk.valid && gq <= gp + kSBufs - 1 && issue_qk(false)) {
+        }
         if (!mbar_wait(&bars[kPFull], gp & 1)) { ok = false; break; }
-        tc::fence_after();
-        // P.V of tile gp first: the softmax of the next tile waits for it
         const int st = gp & 1;
         if (!mbar_wait(&bars[kVFull0 + st], (gp >> 1) & 1)) { ok = false; break; }
         tc::fence_after();
-        const uint32_t p_tmem = tmem + kTmemP + (uint32_t)st * 64;
+        const uint32_t p_tmem = tmem + (uint32_t)(gp % kSBufs) * 128;  // P in its S buffer
         const uint64_t vd = tc::sdesc_sw128(sbase + Lay::kV + st * Lay::kTile, kRegionBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk)
           tc::mma_f16_ts(o_tmem, p_tmem + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), idesc_o,
                          (pv.j > 0 || kk > 0) ? 1u : 0u);
-        tc::commit(&bars[kPvDone0 + st]);  // O updated, P buffer and V stage st free
+        tc::commit(&bars[kPvDone0 + st]);  // O updated, V stage st free
         ++gp;
         pv.next_tile(p);
-        // then S of the tiles up to gp + 1 (their S buffers are free) that are loaded
-        while (ok && qk.valid && gq <= gp + 1 && issue_qk(false)) {
-        }
       }
       // Nothing may still be running on the tensor cores when TMEM is freed.
       tc::commit(&bars[kMmaDone]);
@@ -369,9 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int cta_min_lim = it.cached + it.t0;
       float m = kNegInf, l = 0.f;
       for (int j = 0; j < it.nk; ++j, ++g) {
-        if (!wait_warp(&bars[kSFull0 + (g & 1)], (g >> 1) & 1)) { ok = false; break; }
+        if (!wait_warp(&bars[kSFull0 + g % kSBufs], (g / kSBufs) & 1)) { ok = false; break; }
         tc::fence_after();
-        const uint32_t s_tmem = lane_base + (uint32_t)(g & 1) * 128;
+        const uint32_t s_tmem = lane_base + (uint32_t)(g % kSBufs) * 128;
         const int kv0 = j * kKeys;
         // keys past this row's causal limit count as -inf (select, so arbitrary
         // bits in keys past the sequence end cannot leak through)
@@ -400,13 +403,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_new = grow ? fmaxf(m, mt) : m;
         const float alpha = fast_exp2(m - m_new);  // 0 on the first tile, 1 when not moving
         const float neg_m = -m_new;
-        // P = exp2(s * scale - m) as bf16 pairs into this tile's TMEM P buffer
-        // (free: the P.V that last read it completed before the previous tile
-        // arrived here), row sum in 8 chains
+        // P = exp2(s * scale - m) as bf16 pairs into the first 64 columns of
+        // this tile's S buffer (S is in registers now), row sum in 8 chains
         float acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        const uint32_t p_tmem = lane_base + kTmemP + (uint32_t)(g & 1) * 64;
+        const uint32_t p_tmem = s_tmem;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t pk[32];
