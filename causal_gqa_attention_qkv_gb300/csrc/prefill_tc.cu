@@ -43,6 +43,7 @@ constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kQBufs = 2;  // Q tiles in flight: the current item and the next
 constexpr int kSBufs = 3;  // S buffers in TMEM = K stages in shared memory
+constexpr int kMaxSeqSmem = 32;  // sequences whose facts are cached in shared memory
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 384;  // O columns; [0, 384) hold three S buffers
 constexpr int kRegionBytes = 128 * 128;   // 128 rows x 128 bytes (64 bf16)
@@ -70,7 +71,8 @@ struct TcLayout {
   static constexpr int kV = kK + kSBufs * kTile;  // 2 stages
   static constexpr int kBar = kV + 2 * kTile;
   static constexpr int kNumBars = 24;
-  static constexpr int kTmemSlot = kBar + kNumBars * 8;
+  static constexpr int kSeq = kBar + kNumBars * 8;  // SeqInfo[kMaxSeqSmem]
+  static constexpr int kTmemSlot = kSeq + kMaxSeqSmem * 24;
   // + alignment slack; at least 116 KB so that one CTA runs per SM (each CTA
   // allocates all 512 TMEM columns).
   static constexpr int kSmemRaw = kTmemSlot + 16 + 1024;
@@ -97,46 +99,67 @@ struct Item {
   int64_t slot0;
 };
 
-__device__ __forceinline__ bool item_at(const TcPar& p, int vi, Item& it) {
+// Per-sequence facts the item numbering needs, kept in shared memory for
+// batches of up to kMaxSeqSmem sequences (read from global memory otherwise)
+// so that moving to the next item costs no global-memory round trips.
+struct SeqInfo {
+  int64_t slot0;
+  int tokbase, n_b, cached, usable;  // usable: the request's items are computed
+};
+
+__device__ __forceinline__ SeqInfo seq_info(const TcPar& p, int b) {
+  SeqInfo q;
+  q.tokbase = p.cu_seqlens[b];
+  q.n_b = p.cu_seqlens[b + 1] - q.tokbase;
+  const ReqInfo r = load_request(p.slot_base + b, p.cache_lens + b, p.slot_capacity + b,
+                                 p.num_slots, q.n_b);
+  q.slot0 = r.slot0;
+  q.cached = r.cached;
+  // sequences with no tokens, outside [0, N), longer than the host bound or
+  // with a region too small are skipped (flagged by the prologue / below)
+  q.usable = q.n_b > 0 && q.tokbase >= 0 && q.tokbase + q.n_b <= p.N && q.n_b <= p.max_seqlen &&
+             r.valid;
+  return q;
+}
+
+__device__ __forceinline__ bool item_at(const TcPar& p, const SeqInfo* tab, int vi, Item& it) {
   const int v = vi / p.Hkv;
   it.kh = vi - v * p.Hkv;
   int lo = 0, hi = p.B;  // largest b with vstart(b) <= v
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if ((p.cu_seqlens[mid] >> p.log2BT) + mid <= v) lo = mid; else hi = mid;
+    const int cu = tab ? tab[mid].tokbase : p.cu_seqlens[mid];
+    if ((cu >> p.log2BT) + mid <= v) lo = mid; else hi = mid;
   }
   const int b = lo;
-  const int tokbase = p.cu_seqlens[b];
-  const int n_b = p.cu_seqlens[b + 1] - tokbase;
-  if (n_b <= 0 || tokbase < 0 || tokbase + n_b > p.N) return false;  // flagged by kv_append
-  if (n_b > p.max_seqlen) return false;                               // flagged below
+  const SeqInfo q = tab ? tab[b] : seq_info(p, b);
+  if (!q.usable) return false;
   const int BT = 1 << p.log2BT;
-  const int ntile = (n_b + BT - 1) >> p.log2BT;
-  const int tfe = v - ((tokbase >> p.log2BT) + b);  // tile index counted from the end
+  const int ntile = (q.n_b + BT - 1) >> p.log2BT;
+  const int tfe = v - ((q.tokbase >> p.log2BT) + b);  // tile index counted from the end
   if (tfe < 0 || tfe >= ntile) return false;
-  const ReqInfo r = load_request(p.slot_base + b, p.cache_lens + b, p.slot_capacity + b,
-                                 p.num_slots, n_b);
-  if (!r.valid) return false;  // flagged by kv_append
   it.b = b;
   it.t0 = (ntile - 1 - tfe) * BT;  // heaviest tile first
-  it.n_b = n_b;
-  it.tokbase = tokbase;
-  it.cached = r.cached;
-  it.slot0 = r.slot0;
-  it.kv_total = r.cached + n_b;
-  it.nk = (r.cached + min(it.t0 + BT, n_b) + kKeys - 1) / kKeys;
+  it.n_b = q.n_b;
+  it.tokbase = q.tokbase;
+  it.cached = q.cached;
+  it.slot0 = q.slot0;
+  it.kv_total = q.cached + q.n_b;
+  it.nk = (q.cached + min(it.t0 + BT, q.n_b) + kKeys - 1) / kKeys;
   return true;
 }
 
 // Walks this CTA's items and their KV tiles in order.
 struct TileWalk {
+  const SeqInfo* tab;  // shared-memory sequence table or nullptr
   int vi;     // current virtual item
   int k;      // ordinal of the current item within this CTA
   int j;      // KV tile within the item
   bool valid;
   Item it;
 
-  __device__ __forceinline__ void start(const TcPar& p) {
+  __device__ __forceinline__ void start(const TcPar& p, const SeqInfo* table) {
+    tab = table;
     vi = blockIdx.x - (int)gridDim.x;
     k = -1;
     next_item(p);
@@ -144,7 +167,7 @@ struct TileWalk {
   __device__ __forceinline__ void next_item(const TcPar& p) {
     j = 0;
     for (vi += gridDim.x; vi < p.num_vitems; vi += gridDim.x)
-      if (item_at(p, vi, it)) {
+      if (item_at(p, tab, vi, it)) {
         ++k;
         valid = true;
         return;
@@ -215,10 +238,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::alloc(tmem_slot, kTmemCols);
     tc::relinquish();
   }
+  if (p.B <= kMaxSeqSmem && (int)threadIdx.x < p.B)
+    reinterpret_cast<SeqInfo*>(smem + Lay::kSeq)[threadIdx.x] = seq_info(p, threadIdx.x);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
+  const SeqInfo* seq_tab = p.B <= kMaxSeqSmem ? reinterpret_cast<const SeqInfo*>(smem + Lay::kSeq) : nullptr;
   bool ok = true;
 
   if (warp == kProducerWarp) {
@@ -232,8 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&vmap);
       }
       TileWalk w, qw;  // K or V tiles; items whose Q tile is loaded next
-      w.start(p);
-      qw.start(p);
+      w.start(p, seq_tab);
+      qw.start(p, seq_tab);
       int g = 0;  // tiles issued so far
       int q_issued = 0, issued = 0;
       // Q tile of item qw.k into buffer qw.k % kQBufs (free once the last
@@ -291,8 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kRows, D, true);
       const uint32_t o_tmem = tmem + kTmemO;
       TileWalk qk, pv;
-      qk.start(p);
-      pv.start(p);
+      qk.start(p, seq_tab);
+      pv.start(p, seq_tab);
       int gq = 0, gp = 0;  // next tile for S = Q K^T, next tile for P.V
       // S of tile gq goes to S buffer gq % 3, K stage gq % 3.  It may be issued
       // once P.V of tile gq - 3 (which reads its P from that buffer) has been
@@ -360,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = threadIdx.x;  // 0..127 = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     TileWalk w;
-    w.start(p);
+    w.start(p, seq_tab);
     int g = 0;  // KV tiles processed so far
     while (w.valid && ok) {
       const Item it = w.it;
