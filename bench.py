@@ -79,10 +79,15 @@ def decode_bytes(w, lo=0, hi=None) -> float:
 
 
 def source_sha(*names) -> str:
+    """Hash of the kernel sources with // comments and blank lines removed, so
+    that recorded counters stay tied to the code, not to its comments."""
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "causal_gqa_attention_qkv_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "causal_gqa_attention_qkv_gb300", "csrc", n)) as f:
+            for line in f:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:12]
 
 

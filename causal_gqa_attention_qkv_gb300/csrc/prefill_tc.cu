@@ -11,16 +11,15 @@
 // KV head kh, 128-row query tile).  The tile's rows
 // are 128/G tokens x G heads of the group, so every K/V tile loaded serves the
 // whole GQA group.  Items are numbered sequence by sequence, heaviest tile of
-// a sequence first; CTA c takes items c, c + gridDim.x, ...  Roles (256 threads):
+// a sequence first; CTA c takes items c, c + gridDim.x, ...  Roles (192 threads):
 //   warps 0-3  softmax: thread r owns row r = TMEM lane r.  Per KV tile: read
 //              S from TMEM, mask, online softmax in fp32 (exp2 domain), write P
 //              (bf16) to TMEM, rescale O in TMEM when the reference max moves;
 //              per item: O / l -> bf16 rows of out.
-//   warp 4     TMA producers: lane 0 loads Q (one of three Q buffers per item,
-//              up to two items ahead)
-//              and K (2-stage ring of 128-key tiles running across items);
-//              lane 1 loads V (2-stage ring), so that waiting for a free V slot
-//              never delays the next K tile.
+//   warp 4     TMA producers: lane 0 loads Q (two buffers: the current item
+//              and the next) and K (3-stage ring of 128-key tiles running
+//              across items); lane 1 loads V (2-stage ring), so that waiting
+//              for a free V slot never delays the next K tile.
 //   warp 5     MMA issuer (one thread) and TMEM owner: S = Q K^T into one of
 //              three TMEM buffers and O += P V.  It keeps the S of up to two
 //              tiles ahead queued (as their K and Q arrive) and issues P.V of
@@ -43,6 +42,15 @@ constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kQBufs = 2;  // Q tiles in flight: the current item and the next
 constexpr int kSBufs = 3;  // S buffers in TMEM = K stages in shared memory
+#ifndef PREFILL_LOOKAHEAD
+#define PREFILL_LOOKAHEAD 1
+#endif
+// S = Q K^T tiles issued ahead of the P.V that is waiting for its P.  The
+// tensor pipe runs in issue order and tcgen05.mma issue stalls while the pipe
+// is full, so every S queued ahead delays that P.V (and the softmax waiting on
+// it) by one Q K^T.
+constexpr int kLookahead = PREFILL_LOOKAHEAD;
+static_assert(kLookahead >= 1 && kLookahead <= kSBufs - 1, "lookahead");
 constexpr int kMaxSeqSmem = 32;  // sequences whose facts are cached in shared memory
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 384;  // O columns; [0, 384) hold three S buffers
@@ -359,8 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the S that P.V of tile gp consumes must be under way (blocking) ...
         while (ok && qk.valid && gq <= gp) issue_qk(true);
         if (!ok) break;
-        // ... and S of up to two more tiles, as far as they are loaded
-        while (ok && qk.valid && gq <= gp + kSBufs - 1 && issue_qk(false)) {
+        // ... and S of up to kLookahead more tiles, as far as they are loaded
+        while (ok && qk.valid && gq <= gp + kLookahead && issue_qk(false)) {
         }
         if (!mbar_wait(&bars[kPFull], gp & 1)) { ok = false; break; }
         const int st = gp & 1;
