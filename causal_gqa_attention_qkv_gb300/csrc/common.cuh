@@ -71,17 +71,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-suspending check of the same condition (mbarrier.try_wait may suspend
+// the thread for a while before it returns false; test_wait never does).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Gives up after about
 // two seconds (a pipeline that never completes is an internal error): returns
-// false and the caller records ATTN_STATUS_TIMEOUT and leaves its loop.
+// false and the caller records ATTN_STATUS_TIMEOUT and leaves its loop.  The
+// first check is inline; the bounded polling loop is out of line, which keeps
+// the common case (the phase is already complete) short.
 constexpr uint32_t kWaitSpinLimit = 1u << 22;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity) {
   for (uint32_t i = 0; i < kWaitSpinLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (i > 64) __nanosleep(i < 4096 ? 64 : 512);
   }
   return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity);
 }
 
 // ---------------------------------------------------------------- TMA

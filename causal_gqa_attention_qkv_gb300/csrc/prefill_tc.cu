@@ -11,15 +11,18 @@
 // KV head kh, 128-row query tile).  The tile's rows
 // are 128/G tokens x G heads of the group, so every K/V tile loaded serves the
 // whole GQA group.  Items are numbered sequence by sequence, heaviest tile of
-// a sequence first; CTA c takes items c, c + gridDim.x, ...  Roles (192 threads):
+// a sequence first; CTA c takes items c, c + gridDim.x, ...  Roles (224 threads):
 //   warps 0-3  softmax: thread r owns row r = TMEM lane r.  Per KV tile: read
 //              S from TMEM, mask, online softmax in fp32 (exp2 domain), write P
 //              (bf16) to TMEM, rescale O in TMEM when the reference max moves;
 //              per item: O / l -> bf16 rows of out.
-//   warp 4     TMA producers: lane 0 loads Q (two buffers: the current item
+//   warp 4     TMA producer (one thread): Q (two buffers: the current item
 //              and the next) and K (3-stage ring of 128-key tiles running
-//              across items); lane 1 loads V (2-stage ring), so that waiting
-//              for a free V slot never delays the next K tile.
+//              across items).
+//   warp 6     TMA producer (one thread): V (2-stage ring).  A warp of its
+//              own, so that waiting for a free V stage never holds up the K
+//              loads (a waiting thread may be suspended, and diverged lanes
+//              of one warp do not run independently of that).
 //   warp 5     MMA issuer (one thread) and TMEM owner: S = Q K^T into one of
 //              three TMEM buffers and O += P V.  It keeps the S of up to two
 //              tiles ahead queued (as their K and Q arrive) and issues P.V of
@@ -36,10 +39,11 @@ namespace {
 
 constexpr int kRows = 128;  // query rows per item (MMA M)
 constexpr int kKeys = 128;  // keys per KV tile (MMA N of Q K^T)
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kSoftmaxThreads = 128;
-constexpr int kProducerWarp = 4;
+constexpr int kProducerWarp = 4;  // Q and K loads
 constexpr int kMmaWarp = 5;
+constexpr int kVWarp = 6;         // V loads
 constexpr int kQBufs = 2;  // Q tiles in flight: the current item and the next
 constexpr int kSBufs = 3;  // S buffers in TMEM = K stages in shared memory
 #ifndef PREFILL_LOOKAHEAD
@@ -51,6 +55,7 @@ constexpr int kSBufs = 3;  // S buffers in TMEM = K stages in shared memory
 // it) by one Q K^T.
 constexpr int kLookahead = PREFILL_LOOKAHEAD;
 static_assert(kLookahead >= 1 && kLookahead <= kSBufs - 1, "lookahead");
+
 constexpr int kMaxSeqSmem = 32;  // sequences whose facts are cached in shared memory
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 384;  // O columns; [0, 384) hold three S buffers
@@ -193,13 +198,6 @@ __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, w);
 }
 
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
-  return v;
-}
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
@@ -255,10 +253,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const SeqInfo* seq_tab = p.B <= kMaxSeqSmem ? reinterpret_cast<const SeqInfo*>(smem + Lay::kSeq) : nullptr;
   bool ok = true;
 
-  if (warp == kProducerWarp) {
+  if (warp == kProducerWarp || warp == kVWarp) {
     // ================================================================ TMA producers
-    if (lane < 2) {
-      const bool kstream = lane == 0;
+    if (lane == 0) {
+      const bool kstream = warp == kProducerWarp;
       if (kstream) {
         prefetch_tmap(&qmap);
         prefetch_tmap(&kmap);
@@ -273,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Q tile of item qw.k into buffer qw.k % kQBufs (free once the last
       // Q K^T of item qw.k - kQBufs has completed)
       auto q_free = [&]() -> bool {
-        return qw.k < kQBufs || mbar_try_wait(&bars[kQEmpty0 + qw.k % kQBufs], (qw.k / kQBufs - 1) & 1);
+        return qw.k < kQBufs || mbar_test_wait(&bars[kQEmpty0 + qw.k % kQBufs], (qw.k / kQBufs - 1) & 1);
       };
       auto issue_q = [&]() -> bool {
         const int qs = qw.k % kQBufs;
@@ -338,14 +336,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (qk.j == 0) {
           uint64_t* qb = &bars[kQFull0 + qs];
           const uint32_t qpar = (qk.k / kQBufs) & 1;
-          if (block ? !mbar_wait(qb, qpar) : !mbar_try_wait(qb, qpar)) {
+          if (block ? !mbar_wait(qb, qpar) : !mbar_test_wait(qb, qpar)) {
             if (block) ok = false;
             return false;
           }
         }
         uint64_t* kb = &bars[kKFull0 + sb];
         const uint32_t kpar = (gq / kSBufs) & 1;
-        if (block ? !mbar_wait(kb, kpar) : !mbar_try_wait(kb, kpar)) {
+        if (block ? !mbar_wait(kb, kpar) : !mbar_test_wait(kb, kpar)) {
           if (block) ok = false;
           return false;
         }
