@@ -14,8 +14,9 @@ namespace gb300 {
 
 namespace {
 
-constexpr int kTokPerBlock = 8;
-constexpr int kThreads = 256;
+constexpr int kWarpsPerBlock = 8;  // one token per warp
+constexpr int kThreads = kWarpsPerBlock * 32;
+constexpr int kBatch = 12;         // head-vector loads issued per lane before processing
 
 struct ProloguePar {
   const uint16_t* __restrict__ qkv;        // [N, W] bf16
@@ -35,110 +36,134 @@ struct ProloguePar {
   RopeFreqs freqs;
 };
 
+// One warp per token.  The token's head vectors (D bf16 = D/8 lanes x 16 bytes)
+// are taken HPI = 32 / (D/8) at a time, lane l holding 8 values of head
+// hd0 + j*HPI + l / (D/8): each load instruction reads 512 contiguous bytes of
+// the qkv row and each store writes whole head vectors.  cos/sin of the
+// token's D/2 rotation angles are computed once (D/64 per lane) and handed to
+// the lanes that need them with shuffles.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 4) kv_append_kernel(const ProloguePar p) {
-  constexpr int L = D / 8;     // lanes per head vector (8 bf16 = 16 bytes each)
-  constexpr int HALF = D / 2;  // rotation pairs
-  constexpr int kGroups = kThreads / L;
-  __shared__ float s_cos[kTokPerBlock][HALF];
-  __shared__ float s_sin[kTokPerBlock][HALF];
-  __shared__ int64_t s_slot[kTokPerBlock];
-  __shared__ float s_pos[kTokPerBlock];
-  __shared__ int s_ok[kTokPerBlock];  // 1: token exists; 2: it may also write the cache
-
-  const int t0 = blockIdx.x * kTokPerBlock;
-  if (threadIdx.x < kTokPerBlock) {
-    const int tk = threadIdx.x, t = t0 + tk;
-    int ok = 0;
-    int64_t slot = 0;
-    float pos = 0.f;
-    if (t < p.N) {
-      int b = t, j = 0, n = 1;
-      bool seq_ok = true;
-      if (p.cu_seqlens) {
-        int lo = 0, hi = p.B;  // largest b with cu[b] <= t
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if (p.cu_seqlens[mid] <= t) lo = mid; else hi = mid;
-        }
-        b = lo;
-        j = t - p.cu_seqlens[b];
-        n = p.cu_seqlens[b + 1] - p.cu_seqlens[b];
-        seq_ok = j >= 0 && j < n;
-        if (!seq_ok) set_status(p.status, ATTN_STATUS_SEQLENS);
-      }
-      if (seq_ok) {
-        const ReqInfo r = load_request(p.slot_base + b, p.cache_lens + b, p.slot_capacity + b,
-                                       p.num_slots, n);
-        ok = 1;
-        pos = (float)(r.cached + j);
-        if (r.valid) {
-          ok = 2;
-          slot = r.slot0 + r.cached + j;
-        } else {
-          set_status(p.status, ATTN_STATUS_CAPACITY);
-        }
-      }
-    }
-    if (p.cu_seqlens && t == 0 && p.cu_seqlens[p.B] != p.N) set_status(p.status, ATTN_STATUS_SEQLENS);
-    s_ok[tk] = ok;
-    s_slot[tk] = slot;
-    s_pos[tk] = pos;
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < kTokPerBlock * HALF; i += kThreads) {
-    const int tk = i / HALF, pr = i % HALF;
-    float c, s;
-    rope_angle(s_pos[tk], p.freqs.hi[pr], p.freqs.lo[pr], p.freqs, &c, &s);
-    s_cos[tk][pr] = c;
-    s_sin[tk][pr] = s;
-  }
-  __syncthreads();
-
-  const int64_t W = (int64_t)(p.Hq + 2 * p.Hkv) * D;
+__global__ void __launch_bounds__(kThreads, 2) kv_append_kernel(const ProloguePar p) {
+  constexpr int L = D / 8;      // lanes per head vector
+  constexpr int HPI = 32 / L;   // head vectors per warp-wide step
+  constexpr int PPL = D / 64;   // rotation pairs computed per lane
   const int lane = threadIdx.x & 31;
-  const int li = lane % L;  // lane within the head group
-  const int group = threadIdx.x / L;
-  const unsigned gmask = (L == 32) ? 0xffffffffu : (((1u << L) - 1u) << (lane - li));
-  const bool first_half = li < L / 2;
-  const int pair0 = (first_half ? li : li - L / 2) * 8;  // first rotation pair of this lane
-  const uint4 kw4 = __ldg(reinterpret_cast<const uint4*>(p.k_norm_w + li * 8));
-  const uint4 qw4 = p.q_out ? __ldg(reinterpret_cast<const uint4*>(p.q_norm_w + li * 8)) : kw4;
+  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  if (t >= p.N) return;
 
-  // heads of a token handled here: K heads, V heads, then (with q_out) Q heads
-  const int nq = p.q_out ? p.Hq : 0;
-  const int nhead = 2 * p.Hkv + nq;
-  const int ntask = kTokPerBlock * nhead;
-  constexpr int kMaxTasks = 6;  // tasks per group held in flight (loads issued first)
-  for (int base = 0; base < ntask; base += kGroups * kMaxTasks) {
-    uint4 raw[kMaxTasks];
+  const bool with_q = p.q_out != nullptr;
+  const int hd0 = with_q ? 0 : p.Hq;               // first head handled (Q heads only with q_out)
+  const int nhead = p.Hq + 2 * p.Hkv - hd0;
+  const int nstep = (nhead + HPI - 1) / HPI;
+  const int64_t W = (int64_t)(p.Hq + 2 * p.Hkv) * D;
+  const int li = lane % L;
+  const int sub = lane / L;                        // head slot within a step
+  const uint16_t* row = p.qkv + (int64_t)t * W + (int64_t)hd0 * D + li * 8;
+
+  // first batch of loads before anything that depends on the request lookup
+  uint4 raw[kBatch];
 #pragma unroll
-    for (int k = 0; k < kMaxTasks; ++k) {
-      const int task = base + group + k * kGroups;
-      raw[k] = make_uint4(0, 0, 0, 0);
-      if (task < ntask) {
-        const int tk = task / nhead, hd = task % nhead;
-        // Q heads are prepared even for a request whose cache region is too
-        // small (s_ok == 1): only the cache writes are withheld there
-        const int col = hd < 2 * p.Hkv ? p.Hq + hd : hd - 2 * p.Hkv;
-        if (s_ok[tk] == 2 || (s_ok[tk] == 1 && hd >= 2 * p.Hkv))
-          raw[k] = __ldg(reinterpret_cast<const uint4*>(p.qkv + (int64_t)(t0 + tk) * W +
-                                                          (int64_t)col * D + li * 8));
+  for (int k = 0; k < kBatch; ++k) {
+    const int hd = k * HPI + sub;
+    raw[k] = (k < nstep && hd < nhead) ? __ldg(reinterpret_cast<const uint4*>(row + (int64_t)hd * D))
+                                       : make_uint4(0, 0, 0, 0);
+  }
+
+  // request of this token: 0 = none, 1 = Q only (region too small), 2 = Q and cache
+  int ok = 0;
+  int64_t slot = 0;
+  float pos = 0.f;
+  {
+    int b = t, j = 0, n = 1;
+    bool seq_ok = true;
+    if (p.cu_seqlens) {
+      int lo = 0, hi = p.B;  // largest b with cu[b] <= t
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(p.cu_seqlens + mid) <= t) lo = mid; else hi = mid;
+      }
+      b = lo;
+      const int c0 = __ldg(p.cu_seqlens + b);
+      j = t - c0;
+      n = __ldg(p.cu_seqlens + b + 1) - c0;
+      seq_ok = j >= 0 && j < n;
+      if (!seq_ok && lane == 0) set_status(p.status, ATTN_STATUS_SEQLENS);
+      if (t == 0 && lane == 0 && __ldg(p.cu_seqlens + p.B) != p.N) set_status(p.status, ATTN_STATUS_SEQLENS);
+    }
+    if (seq_ok) {
+      const ReqInfo r = load_request(p.slot_base + b, p.cache_lens + b, p.slot_capacity + b,
+                                     p.num_slots, n);
+      ok = 1;
+      pos = (float)(r.cached + j);
+      if (r.valid) {
+        ok = 2;
+        slot = r.slot0 + r.cached + j;
+      } else if (lane == 0) {
+        set_status(p.status, ATTN_STATUS_CAPACITY);
+      }
+    }
+  }
+  if (ok == 0) return;  // warp-uniform
+
+  // cos/sin of the 8 rotation pairs this lane's values belong to
+  float cs[8], sn[8];
+  {
+    float c_own[PPL], s_own[PPL];
+#pragma unroll
+    for (int e = 0; e < PPL; ++e) {
+      const int pr = lane * PPL + e;
+      rope_angle(pos, p.freqs.hi[pr], p.freqs.lo[pr], p.freqs, &c_own[e], &s_own[e]);
+    }
+    const int pair0 = (li % (L / 2)) * 8;
+    const bool first_half = li < L / 2;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int pr = pair0 + e;
+      float c = __shfl_sync(0xffffffffu, c_own[e % PPL], pr / PPL);
+      float s = __shfl_sync(0xffffffffu, s_own[e % PPL], pr / PPL);
+      cs[e] = c;
+      sn[e] = first_half ? -s : s;  // x_i c - x_{i+D/2} s  /  x_{i+D/2} c + x_i s
+    }
+  }
+  float qw[8], kw[8];
+  {
+    const uint4 k4 = __ldg(reinterpret_cast<const uint4*>(p.k_norm_w + li * 8));
+    const uint4 q4 = with_q ? __ldg(reinterpret_cast<const uint4*>(p.q_norm_w + li * 8)) : k4;
+    const uint32_t* kr = reinterpret_cast<const uint32_t*>(&k4);
+    const uint32_t* qr = reinterpret_cast<const uint32_t*>(&q4);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      kw[2 * e] = bf16_lo(kr[e]);
+      kw[2 * e + 1] = bf16_hi(kr[e]);
+      qw[2 * e] = bf16_lo(qr[e]);
+      qw[2 * e + 1] = bf16_hi(qr[e]);
+    }
+  }
+  uint16_t* q_row = with_q ? p.q_out + (int64_t)t * p.Hq * D + li * 8 : nullptr;
+  const int64_t cache_row = slot * p.Hkv * D + li * 8;
+
+  for (int base = 0; base < nstep; base += kBatch) {
+    if (base > 0) {
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int hd = (base + k) * HPI + sub;
+        raw[k] = (base + k < nstep && hd < nhead)
+                     ? __ldg(reinterpret_cast<const uint4*>(row + (int64_t)hd * D))
+                     : make_uint4(0, 0, 0, 0);
       }
     }
 #pragma unroll
-    for (int k = 0; k < kMaxTasks; ++k) {
-      const int task = base + group + k * kGroups;  // whole groups move together
-      if (task >= ntask) break;
-      const int tk = task / nhead, hd = task % nhead;
-      const bool is_q = hd >= 2 * p.Hkv;
-      if (s_ok[tk] == 0 || (!is_q && s_ok[tk] != 2)) continue;
-      const bool is_k = hd < p.Hkv;
-      const int kvh = is_k ? hd : hd - p.Hkv;
-      const int64_t dst = is_q ? ((int64_t)(t0 + tk) * p.Hq + (hd - 2 * p.Hkv)) * D + li * 8
-                               : (s_slot[tk] * p.Hkv + kvh) * D + li * 8;
-      if (!is_k && !is_q) {  // V: bit copy into the cache
-        *reinterpret_cast<uint4*>(p.v_cache + dst) = raw[k];
+    for (int k = 0; k < kBatch; ++k) {
+      if (base + k >= nstep) break;  // warp-uniform
+      const int hd = hd0 + (base + k) * HPI + sub;  // head index in the qkv row
+      const bool live = hd < p.Hq + 2 * p.Hkv;
+      const bool is_q = hd < p.Hq;
+      const bool is_v = hd >= p.Hq + p.Hkv;
+      // steps made only of V heads: bit copies into the cache
+      const bool step_all_v = hd0 + (base + k) * HPI >= p.Hq + p.Hkv;
+      if (step_all_v) {
+        if (live && ok == 2)
+          *reinterpret_cast<uint4*>(p.v_cache + cache_row + (int64_t)(hd - p.Hq - p.Hkv) * D) = raw[k];
         continue;
       }
       float x[8];
@@ -152,33 +177,26 @@ __global__ void __launch_bounds__(kThreads, 4) kv_append_kernel(const ProloguePa
 #pragma unroll
       for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
 #pragma unroll
-      for (int off = L / 2; off >= 1; off >>= 1) ss += __shfl_xor_sync(gmask, ss, off);
+      for (int off = L / 2; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
       const float inv = rsqrtf(ss * (1.0f / D) + p.eps);
-      const uint32_t* ww = reinterpret_cast<const uint32_t*>(is_q ? &qw4 : &kw4);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        x[2 * e] = bf16_lo(ww[e]) * (x[2 * e] * inv);
-        x[2 * e + 1] = bf16_hi(ww[e]) * (x[2 * e + 1] * inv);
-      }
+      for (int e = 0; e < 8; ++e) x[e] = (is_q ? qw[e] : kw[e]) * (x[e] * inv);
       uint32_t o[4];
 #pragma unroll
       for (int e = 0; e < 8; e += 2) {
-        const float y0 = x[e], y1 = x[e + 1];
-        const float q0 = __shfl_xor_sync(gmask, y0, L / 2);
-        const float q1 = __shfl_xor_sync(gmask, y1, L / 2);
-        const float c0 = s_cos[tk][pair0 + e], s0 = s_sin[tk][pair0 + e];
-        const float c1 = s_cos[tk][pair0 + e + 1], s1 = s_sin[tk][pair0 + e + 1];
-        float r0, r1;
-        if (first_half) {
-          r0 = y0 * c0 - q0 * s0;
-          r1 = y1 * c1 - q1 * s1;
-        } else {
-          r0 = y0 * c0 + q0 * s0;
-          r1 = y1 * c1 + q1 * s1;
-        }
-        o[e / 2] = pack_bf16(r0, r1);
+        const float q0 = __shfl_xor_sync(0xffffffffu, x[e], L / 2);
+        const float q1 = __shfl_xor_sync(0xffffffffu, x[e + 1], L / 2);
+        o[e / 2] = pack_bf16(fmaf(q0, sn[e], x[e] * cs[e]), fmaf(q1, sn[e + 1], x[e + 1] * cs[e + 1]));
       }
-      *reinterpret_cast<uint4*>((is_q ? p.q_out : p.k_cache) + dst) = make_uint4(o[0], o[1], o[2], o[3]);
+      const uint4 v4 = is_v ? raw[k] : make_uint4(o[0], o[1], o[2], o[3]);
+      if (!live) continue;
+      if (is_q) {
+        *reinterpret_cast<uint4*>(q_row + (int64_t)hd * D) = v4;
+      } else if (ok == 2) {
+        uint16_t* dst = is_v ? p.v_cache + cache_row + (int64_t)(hd - p.Hq - p.Hkv) * D
+                             : p.k_cache + cache_row + (int64_t)(hd - p.Hq) * D;
+        *reinterpret_cast<uint4*>(dst) = v4;
+      }
     }
   }
 }
@@ -206,7 +224,7 @@ cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t stream) {
   p.Hkv = a.cfg.num_kv_heads;
   p.eps = a.cfg.rms_eps;
   p.freqs = a.freqs;
-  const dim3 grid((a.N + kTokPerBlock - 1) / kTokPerBlock);
+  const dim3 grid((a.N + kWarpsPerBlock - 1) / kWarpsPerBlock);
   if (a.cfg.head_dim == 128)
     kv_append_kernel<128><<<grid, kThreads, 0, stream>>>(p);
   else
