@@ -494,25 +494,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- item epilogue: O / l -> bf16 rows of out (P.V of its last tile done)
       if (!wait_warp(&bars[kPvDone0 + ((g - 1) & 1)], ((g - 1) >> 1) & 1)) { ok = false; break; }
       tc::fence_after();
-      const float inv_l = 1.f / l;
-      const bool store = tok < it.n_b;
-      uint16_t* dst = p.out + (int64_t)(it.tokbase + (store ? tok : 0)) * p.Hq * D + (int64_t)h * D;
-      uint32_t o[D];
+      {
+        const float inv_l = 1.f / l;
+        const bool store = tok < it.n_b;
+        uint16_t* dst = p.out + (int64_t)(it.tokbase + (store ? tok : 0)) * p.Hq * D + (int64_t)h * D;
+        // 32 columns at a time in a rolled loop: this code runs once per item,
+        // so it is kept short (it competes for instruction cache with the tile loop)
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tc::ld_32x32b_x32(lane_base + kTmemO + c * 32, o);
+          tc::wait_ld();
+          if (store) {
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) tc::ld_32x32b_x32(lane_base + kTmemO + c * 32, o + c * 32);
-      tc::wait_ld();
-      // the O reads above are complete before the next item's first P.V overwrites O
-      tc::fence_before();
-      if (store) {
-#pragma unroll
-        for (int q = 0; q < D / 8; ++q) {
-          uint4 v;
-          v.x = pack_bf16(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
-          v.y = pack_bf16(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
-          v.z = pack_bf16(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
-          v.w = pack_bf16(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
-          *reinterpret_cast<uint4*>(dst + q * 8) = v;
+            for (int q = 0; q < 4; ++q) {
+              uint4 v;
+              v.x = pack_bf16(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
+              v.y = pack_bf16(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
+              v.z = pack_bf16(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
+              v.w = pack_bf16(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
+              *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) = v;
+            }
+          }
         }
+        // the O reads above are complete before the next item's first P.V overwrites O
+        tc::fence_before();
       }
     }
     if (!ok) set_status(p.status, ATTN_STATUS_TIMEOUT);
@@ -554,6 +560,7 @@ int launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream) {
   const int64_t nv = ((int64_t)(a.N >> p.log2BT) + a.B) * Hkv;
   if (nv > (int64_t(1) << 30)) return ATTN_EINVAL;
   p.num_vitems = (int)nv;
+
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)

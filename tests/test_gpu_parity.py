@@ -103,6 +103,27 @@ def test_deterministic_and_idempotent():
     assert torch.equal(k1.view(torch.int16), ds.k_cache.view(torch.int16))
 
 
+def test_prefill_output_only_16_byte_aligned():
+    """An output that starts 16 bytes past a 32-byte boundary (allowed by the
+    ABI) gets the same bits as a 32-byte-aligned one."""
+    from causal_gqa_attention_qkv_gb300 import attn, step
+    w = gen.custom("align16", 32, 8, 128, [200, 33, 96], [0, 70, 0], seed=6)
+    host = gen.make_inputs(w)
+    ds = step.upload(w, host)
+    ds.run()
+    torch.cuda.synchronize()
+    ref = ds.out.clone()
+    n, width = ds.out.shape
+    buf = torch.full((n * width + 16,), float("nan"), dtype=torch.bfloat16, device=ds.out.device)
+    out = buf[8:8 + n * width].view(n, width)  # 16 bytes past the allocation start
+    assert out.data_ptr() % 32 == 16
+    attn.prefill(ds.cfg, ds.qkv, ds.q_norm_w, ds.k_norm_w, ds.cu_seqlens, ds.max_seqlen, ds.kv_prefill,
+                 out, ds.workspace)
+    torch.cuda.synchronize()
+    assert ds.status() == 0
+    assert torch.equal(ref.view(torch.int16), out.view(torch.int16))
+
+
 def test_status_capacity_and_seqlens():
     from causal_gqa_attention_qkv_gb300 import attn, step
     w = gen.custom("cap", 8, 2, 64, [10, 6], [0, 4], seed=8)
