@@ -8,28 +8,32 @@
 // way (flash attention), never materialising the score matrix.
 //
 // Q arrives normed and rotated (prologue kernel).  Work item = (sequence b,
-// KV head kh, 128-row query tile).  The tile's rows
-// are 128/G tokens x G heads of the group, so every K/V tile loaded serves the
-// whole GQA group.  Items are numbered sequence by sequence, heaviest tile of
-// a sequence first; CTA c takes items c, c + gridDim.x, ...  Roles (224 threads):
-//   warps 0-3  softmax: thread r owns row r = TMEM lane r.  Per KV tile: read
-//              S from TMEM, mask, online softmax in fp32 (exp2 domain), write P
-//              (bf16) to TMEM, rescale O in TMEM when the reference max moves;
-//              per item: O / l -> bf16 rows of out.
-//   warp 4     TMA producer (one thread): Q (two buffers: the current item
-//              and the next) and K (3-stage ring of 128-key tiles running
-//              across items).
-//   warp 6     TMA producer (one thread): V (2-stage ring).  A warp of its
-//              own, so that waiting for a free V stage never holds up the K
-//              loads (a waiting thread may be suspended, and diverged lanes
-//              of one warp do not run independently of that).
-//   warp 5     MMA issuer (one thread) and TMEM owner: S = Q K^T into one of
-//              three TMEM buffers and O += P V.  It keeps the S of up to two
-//              tiles ahead queued (as their K and Q arrive) and issues P.V of
-//              tile g as soon as its P is in TMEM (also across item boundaries).
-// TMEM: three S buffers (fp32) in columns [0,384), O in [384, 384+D).  P
-// (bf16 pairs, A operand of P.V read from TMEM) overwrites the first 64
-// columns of its tile's S buffer once the softmax holds S in registers.
+// KV head kh, block of 2 x 128 query rows).  A 128-row Q tile is 128/G tokens
+// x the G heads of the group, so every K/V tile loaded serves the whole GQA
+// group; the item's two Q tiles (A: its first 128/G tokens, B: the next
+// 128/G) share every K/V tile.  Items are numbered sequence by sequence,
+// heaviest block of a sequence first; CTA c takes items c, c + gridDim.x, ...
+//
+// Roles (384 threads, three warpgroups):
+//   warps 0-3   softmax of Q tile A, warps 4-7 softmax of Q tile B: thread r
+//               of a warpgroup owns row r = TMEM lane r of its tile.  Per KV
+//               tile: read S from TMEM, mask, online softmax in fp32 (exp2
+//               domain), P (bf16) written over S in TMEM, O rescaled in TMEM
+//               when the reference max moves; per item: O / l -> out.
+//   warp 8      TMA: K tiles (3-stage ring of 128 keys, across items).
+//   warp 9      MMA issuer (one thread) and TMEM owner.
+//   warp 10     TMA: V tiles (2-stage ring).
+//   warp 11     TMA: the item's two Q tiles (one buffer each).
+// Each producer runs in a warp of its own: a thread waiting for a free stage
+// may be suspended, and diverged lanes of one warp do not run independently.
+//
+// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,256+D),
+// O_B [384,384+D).  Issue order per KV tile j:
+//   P.V_A(j), S_A(j+1) = Q_A K(j+1)^T, P.V_B(j), S_B(j+1)
+// so the tensor cores compute tile B's products while the softmax of tile A
+// runs and the other way round.  Because the tensor-core operations of one
+// thread complete in issue order, S_X(j+1) being complete means P.V_X(j) is
+// complete: the softmax may rescale O_X as soon as it sees S_X(j+1).
 #include "kernels.cuh"
 #include "tcgen05.cuh"
 
@@ -37,28 +41,19 @@ namespace gb300 {
 
 namespace {
 
-constexpr int kRows = 128;  // query rows per item (MMA M)
-constexpr int kKeys = 128;  // keys per KV tile (MMA N of Q K^T)
-constexpr int kThreads = 224;
-constexpr int kSoftmaxThreads = 128;
-constexpr int kProducerWarp = 4;  // Q and K loads
-constexpr int kMmaWarp = 5;
-constexpr int kVWarp = 6;         // V loads
-constexpr int kQBufs = 2;  // Q tiles in flight: the current item and the next
-constexpr int kSBufs = 3;  // S buffers in TMEM = K stages in shared memory
-#ifndef PREFILL_LOOKAHEAD
-#define PREFILL_LOOKAHEAD 1
-#endif
-// S = Q K^T tiles issued ahead of the P.V that is waiting for its P.  The
-// tensor pipe runs in issue order and tcgen05.mma issue stalls while the pipe
-// is full, so every S queued ahead delays that P.V (and the softmax waiting on
-// it) by one Q K^T.
-constexpr int kLookahead = PREFILL_LOOKAHEAD;
-static_assert(kLookahead >= 1 && kLookahead <= kSBufs - 1, "lookahead");
-
+constexpr int kTileRows = 128;  // query rows per Q tile (MMA M)
+constexpr int kKeys = 128;      // keys per KV tile (MMA N of Q K^T)
+constexpr int kThreads = 384;
+constexpr int kSoftmaxThreads = 128;  // per Q tile
+constexpr int kKWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kVWarp = 10;
+constexpr int kQWarp = 11;
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
 constexpr int kMaxSeqSmem = 32;  // sequences whose facts are cached in shared memory
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 384;  // O columns; [0, 384) hold three S buffers
+constexpr uint32_t kTmemO = 256;  // O_A at 256, O_B at 384; S_A at 0, S_B at 128
 constexpr int kRegionBytes = 128 * 128;   // 128 rows x 128 bytes (64 bf16)
 constexpr float kRescaleThreshold = 8.f;  // log2 units: move the reference max past 256x growth
 
@@ -72,41 +67,45 @@ struct TcPar {
   uint16_t* out;
   float scale_log2;  // log2(e) / sqrt(D)
   int32_t Hq, Hkv, log2G, log2BT, N, B, max_seqlen;
-  int32_t num_vitems;  // ((N >> log2BT) + B) * Hkv: size of the item numbering
+  int32_t num_vitems;  // ((N >> (log2BT + 1)) + B) * Hkv: size of the item numbering
 };
 
 template <int D>
 struct TcLayout {
   static constexpr int kRegions = D / 64;
   static constexpr int kTile = kRegions * kRegionBytes;  // Q, K or V tile: 128 rows x D
-  static constexpr int kQ = 0;                // kQBufs buffers
-  static constexpr int kK = kQ + kQBufs * kTile;  // kSBufs stages
-  static constexpr int kV = kK + kSBufs * kTile;  // 2 stages
-  static constexpr int kBar = kV + 2 * kTile;
-  static constexpr int kNumBars = 24;
+  static constexpr int kQ = 0;                       // Q tiles A, B
+  static constexpr int kK = kQ + 2 * kTile;          // kKStages
+  static constexpr int kV = kK + kKStages * kTile;   // kVStages
+  static constexpr int kBar = kV + kVStages * kTile;
+  static constexpr int kNumBars = 32;
   static constexpr int kSeq = kBar + kNumBars * 8;  // SeqInfo[kMaxSeqSmem]
   static constexpr int kTmemSlot = kSeq + kMaxSeqSmem * 24;
   // + alignment slack; at least 116 KB so that one CTA runs per SM (each CTA
   // allocates all 512 TMEM columns).
   static constexpr int kSmemRaw = kTmemSlot + 16 + 1024;
   static constexpr int kSmemBytes = kSmemRaw > 116 * 1024 ? kSmemRaw : 116 * 1024;
+  static_assert(kSmemRaw <= 227 * 1024, "shared memory");
 };
 
 enum Bar {
-  kQFull0 = 0, kQEmpty0 = kQFull0 + kQBufs,
-  kKFull0 = kQEmpty0 + kQBufs, kVFull0 = kKFull0 + kSBufs, kVFull1,
-  // kSFull + b: S of a tile in S buffer b (K stage b) is complete, which also
-  // frees that K stage; kPvDone + st: P.V of a tile using V stage st is
-  // complete (O updated, V stage st free).  Each advances one phase per use of
-  // its stage, so no waiter can fall two phases behind.
-  kSFull0, kPvDone0 = kSFull0 + kSBufs, kPvDone1, kPFull, kMmaDone
+  // Every barrier advances one phase per use of its buffer, so no waiter can
+  // fall two phases behind.
+  kQFullA = 0, kQFullB, kQEmptyA, kQEmptyB,   // Q tiles (empty: the item's last S_X done)
+  kKFull0, kKEmpty0 = kKFull0 + kKStages,     // K stages (empty: S_A and S_B of the tile done)
+  kVFull0 = kKEmpty0 + kKStages, kVEmpty0 = kVFull0 + kVStages,  // V stages (empty: both P.V done)
+  kSFullA = kVEmpty0 + kVStages, kSFullB,     // S_X of a tile complete (and every earlier MMA)
+  kPFullA, kPFullB,                           // P_X of a tile in TMEM (128 arrivals)
+  kODoneA, kODoneB,                           // the item's last P.V_X complete
+  kMmaDone
 };
 
 // ---------------------------------------------------------------- work items
-// Item numbering without a table: sequence b owns the "virtual tiles"
-// [vstart(b), vstart(b) + ntiles(b)) with vstart(b) = cu_seqlens[b] / BT + b
-// (these ranges never overlap; each sequence leaves at most one slot empty).
-// Virtual item i = (virtual tile i / Hkv, KV head i % Hkv).
+// Item numbering without a table: sequence b owns the "virtual blocks"
+// [vstart(b), vstart(b) + nblocks(b)) with vstart(b) = cu_seqlens[b] / IT + b
+// (IT = 2 x 128/G tokens per item; these ranges never overlap, each sequence
+// leaves at most one slot empty).  Virtual item i = (virtual block i / Hkv,
+// KV head i % Hkv).
 struct Item {
   int b, kh, t0, n_b, tokbase, cached, nk, kv_total;
   int64_t slot0;
@@ -138,57 +137,50 @@ __device__ __forceinline__ SeqInfo seq_info(const TcPar& p, int b) {
 __device__ __forceinline__ bool item_at(const TcPar& p, const SeqInfo* tab, int vi, Item& it) {
   const int v = vi / p.Hkv;
   it.kh = vi - v * p.Hkv;
+  const int log2IT = p.log2BT + 1;
   int lo = 0, hi = p.B;  // largest b with vstart(b) <= v
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     const int cu = tab ? tab[mid].tokbase : p.cu_seqlens[mid];
-    if ((cu >> p.log2BT) + mid <= v) lo = mid; else hi = mid;
+    if ((cu >> log2IT) + mid <= v) lo = mid; else hi = mid;
   }
   const int b = lo;
   const SeqInfo q = tab ? tab[b] : seq_info(p, b);
   if (!q.usable) return false;
-  const int BT = 1 << p.log2BT;
-  const int ntile = (q.n_b + BT - 1) >> p.log2BT;
-  const int tfe = v - ((q.tokbase >> p.log2BT) + b);  // tile index counted from the end
-  if (tfe < 0 || tfe >= ntile) return false;
+  const int IT = 1 << log2IT;
+  const int nblk = (q.n_b + IT - 1) >> log2IT;
+  const int bfe = v - ((q.tokbase >> log2IT) + b);  // block index counted from the end
+  if (bfe < 0 || bfe >= nblk) return false;
   it.b = b;
-  it.t0 = (ntile - 1 - tfe) * BT;  // heaviest tile first
+  it.t0 = (nblk - 1 - bfe) * IT;  // heaviest block first
   it.n_b = q.n_b;
   it.tokbase = q.tokbase;
   it.cached = q.cached;
   it.slot0 = q.slot0;
   it.kv_total = q.cached + q.n_b;
-  it.nk = (q.cached + min(it.t0 + BT, q.n_b) + kKeys - 1) / kKeys;
+  it.nk = (q.cached + min(it.t0 + IT, q.n_b) + kKeys - 1) / kKeys;
   return true;
 }
 
-// Walks this CTA's items and their KV tiles in order.
-struct TileWalk {
+// Walks this CTA's items in order.
+struct ItemWalk {
   const SeqInfo* tab;  // shared-memory sequence table or nullptr
-  int vi;     // current virtual item
-  int k;      // ordinal of the current item within this CTA
-  int j;      // KV tile within the item
+  int vi;              // current virtual item
   bool valid;
   Item it;
 
   __device__ __forceinline__ void start(const TcPar& p, const SeqInfo* table) {
     tab = table;
     vi = blockIdx.x - (int)gridDim.x;
-    k = -1;
-    next_item(p);
+    next(p);
   }
-  __device__ __forceinline__ void next_item(const TcPar& p) {
-    j = 0;
+  __device__ __forceinline__ void next(const TcPar& p) {
     for (vi += gridDim.x; vi < p.num_vitems; vi += gridDim.x)
       if (item_at(p, tab, vi, it)) {
-        ++k;
         valid = true;
         return;
       }
     valid = false;
-  }
-  __device__ __forceinline__ void next_tile(const TcPar& p) {
-    if (++j >= it.nk) next_item(p);
   }
 };
 
@@ -198,10 +190,351 @@ __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, w);
 }
 
+// Packed pairs of fp32 values (the low half is the first element) and the
+// paired fp32 operations of this architecture.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f2_lo(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo;
+}
+__device__ __forceinline__ float f2_hi(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return hi;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
                : "memory");
+}
+
+
+// ---------------------------------------------------------------- roles
+// One TMA producer ring (K or V tiles): tile g of the CTA's tile sequence goes
+// to stage g % stages once the stage's previous tile has been consumed.
+template <int D>
+__device__ void produce_kv(const TcPar& p, const SeqInfo* seq_tab, const CUtensorMap* map,
+                           uint8_t* smem, uint64_t* bars, int base, int full0, int empty0,
+                           int stages, bool& ok) {
+  using Lay = TcLayout<D>;
+  prefetch_tmap(map);
+  ItemWalk w;
+  w.start(p, seq_tab);
+  int g = 0;
+  while (w.valid && ok) {
+    for (int j = 0; j < w.it.nk; ++j, ++g) {
+      const int st = g % stages;
+      if (g >= stages && !mbar_wait(&bars[empty0 + st], (g / stages - 1) & 1)) { ok = false; break; }
+      mbar_arrive_expect_tx(&bars[full0 + st], Lay::kTile);
+#pragma unroll
+      for (int rg = 0; rg < Lay::kRegions; ++rg)
+        tma_load_3d(smem + base + st * Lay::kTile + rg * kRegionBytes, map, &bars[full0 + st],
+                    rg * 64, w.it.kh, (int)(w.it.slot0 + j * kKeys));
+    }
+    w.next(p);
+  }
+  // Every load issued has landed before the CTA may exit (immediate on the
+  // normal path, where the consumers already waited for them).
+  for (int t = max(0, g - stages); t < g; ++t) (void)mbar_wait(&bars[full0 + t % stages], (t / stages) & 1);
+}
+
+template <int D>
+__device__ void produce_q(const TcPar& p, const SeqInfo* seq_tab, const CUtensorMap* qmap,
+                          uint8_t* smem, uint64_t* bars, bool& ok) {
+  using Lay = TcLayout<D>;
+  prefetch_tmap(qmap);
+  const int G = 1 << p.log2G, BT = 1 << p.log2BT;
+  ItemWalk w;
+  w.start(p, seq_tab);
+  int k = 0;
+  while (w.valid && ok) {
+    for (int x = 0; x < 2; ++x) {
+      if (k >= 1 && !mbar_wait(&bars[kQEmptyA + x], (k - 1) & 1)) { ok = false; break; }
+      mbar_arrive_expect_tx(&bars[kQFullA + x], Lay::kTile);
+#pragma unroll
+      for (int rg = 0; rg < Lay::kRegions; ++rg)
+        tma_load_3d(smem + Lay::kQ + x * Lay::kTile + rg * kRegionBytes, qmap, &bars[kQFullA + x],
+                    rg * 64, w.it.kh * G, w.it.tokbase + w.it.t0 + x * BT);
+    }
+    if (!ok) break;
+    ++k;
+    w.next(p);
+  }
+  if (k >= 1)
+    for (int x = 0; x < 2; ++x) (void)mbar_wait(&bars[kQFullA + x], (k - 1) & 1);
+}
+
+template <int D>
+__device__ void issue_mma(const TcPar& p, const SeqInfo* seq_tab, uint32_t sbase, uint32_t tmem,
+                          uint64_t* bars, bool& ok) {
+  using Lay = TcLayout<D>;
+  constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kTileRows, kKeys, false);
+  constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kTileRows, D, true);
+  // S_X = Q_X K(st)^T into TMEM columns 128 x
+  auto qk = [&](int x, int st) {
+    const uint64_t qd = tc::sdesc_sw128(sbase + Lay::kQ + x * Lay::kTile, 16, 1024);
+    const uint64_t kd = tc::sdesc_sw128(sbase + Lay::kK + st * Lay::kTile, 16, 1024);
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const uint64_t off = (uint64_t)(((ks >> 2) * kRegionBytes + (ks & 3) * 32) >> 4);
+      tc::mma_f16_ss(tmem + (uint32_t)x * 128, qd + off, kd + off, idesc_s, ks > 0);
+    }
+  };
+  // O_X (+)= P_X V(sv), P_X (bf16) read from the first 64 columns of S_X
+  auto pv = [&](int x, int sv, bool acc) {
+    const uint64_t vd = tc::sdesc_sw128(sbase + Lay::kV + sv * Lay::kTile, kRegionBytes, 1024);
+#pragma unroll
+    for (int kk = 0; kk < kKeys / 16; ++kk)
+      tc::mma_f16_ts(tmem + kTmemO + (uint32_t)x * 128, tmem + (uint32_t)x * 128 + kk * 8,
+                     vd + (uint64_t)((kk * 2048) >> 4), idesc_o, (acc || kk > 0) ? 1u : 0u);
+  };
+  ItemWalk w;
+  w.start(p, seq_tab);
+  int g = 0;  // KV tiles of this CTA so far
+  int k = 0;  // items so far
+  while (w.valid && ok) {
+    const int nk = w.it.nk;
+    if (!mbar_wait(&bars[kQFullA], k & 1) || !mbar_wait(&bars[kQFullB], k & 1)) { ok = false; break; }
+    {
+      const int st = g % kKStages;
+      if (!mbar_wait(&bars[kKFull0 + st], (g / kKStages) & 1)) { ok = false; break; }
+      tc::fence_after();
+      qk(0, st);
+      tc::commit(&bars[kSFullA]);
+      if (nk == 1) tc::commit(&bars[kQEmptyA]);
+      qk(1, st);
+      tc::commit(&bars[kSFullB]);
+      tc::commit(&bars[kKEmpty0 + st]);
+      if (nk == 1) tc::commit(&bars[kQEmptyB]);
+    }
+    for (int j = 0; j < nk; ++j) {
+      const int gj = g + j;
+      const int sv = gj % kVStages;
+      const bool last = j == nk - 1;
+      const int st1 = (gj + 1) % kKStages;  // K stage of tile j + 1
+      // ---- tile A
+      if (!mbar_wait(&bars[kPFullA], gj & 1)) { ok = false; break; }
+      if (!mbar_wait(&bars[kVFull0 + sv], (gj / kVStages) & 1)) { ok = false; break; }
+      tc::fence_after();
+      pv(0, sv, j > 0);
+      if (last) tc::commit(&bars[kODoneA]);
+      if (!last) {
+        if (!mbar_wait(&bars[kKFull0 + st1], ((gj + 1) / kKStages) & 1)) { ok = false; break; }
+        tc::fence_after();
+        qk(0, st1);
+        tc::commit(&bars[kSFullA]);
+        if (j + 1 == nk - 1) tc::commit(&bars[kQEmptyA]);
+      }
+      // ---- tile B
+      if (!mbar_wait(&bars[kPFullB], gj & 1)) { ok = false; break; }
+      tc::fence_after();
+      pv(1, sv, j > 0);
+      tc::commit(&bars[kVEmpty0 + sv]);
+      if (last) tc::commit(&bars[kODoneB]);
+      if (!last) {
+        qk(1, st1);
+        tc::commit(&bars[kSFullB]);
+        tc::commit(&bars[kKEmpty0 + st1]);
+        if (j + 1 == nk - 1) tc::commit(&bars[kQEmptyB]);
+      }
+    }
+    g += nk;
+    ++k;
+    w.next(p);
+  }
+  // Nothing may still be running on the tensor cores when TMEM is freed.
+  tc::commit(&bars[kMmaDone]);
+  (void)mbar_wait(&bars[kMmaDone], 0);
+}
+
+// Softmax and epilogue of Q tile x (0: A, 1: B) of every item.
+template <int D>
+__device__ void softmax_tile(const TcPar& p, const SeqInfo* seq_tab, uint32_t sbase, uint32_t tmem,
+                             uint64_t* bars, int x, bool& ok) {
+  using Lay = TcLayout<D>;
+  const int row = threadIdx.x & (kSoftmaxThreads - 1);  // = TMEM lane
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+  const uint32_t s_col = (uint32_t)x * 128, o_col = kTmemO + (uint32_t)x * 128;
+  const int G = 1 << p.log2G, BT = 1 << p.log2BT;
+  ItemWalk w;
+  w.start(p, seq_tab);
+  int g = 0;  // KV tiles processed so far
+  int k = 0;  // items processed so far
+  while (w.valid && ok) {
+    const Item it = w.it;
+    w.next(p);  // the next item's bounds load while this item runs
+    const int tok = it.t0 + x * BT + (row >> p.log2G);
+    const int h = it.kh * G + (row & (G - 1));
+    const int lim = tok < it.n_b ? it.cached + tok : it.kv_total - 1;  // last key this row sees
+    const int tile_min_lim = it.cached + it.t0 + x * BT;
+    float m = kNegInf, l = 0.f;
+    for (int j = 0; j < it.nk; ++j, ++g) {
+      // S_X(j) complete; so is P.V_X(j - 1) (issued earlier by the same thread)
+      if (!wait_warp(&bars[kSFullA + x], g & 1)) { ok = false; break; }
+      tc::fence_after();
+      const uint32_t s_tmem = lane_base + s_col;
+      const int kv0 = j * kKeys;
+      // keys past this row's causal limit count as -inf (select, so arbitrary
+      // bits in keys past the sequence end cannot leak through)
+      const bool masked = kv0 + kKeys - 1 > tile_min_lim;
+      const int lim_rel = lim - kv0;  // columns c <= lim_rel are visible
+      // pass 1: row max over the visible columns, 32 columns at a time
+      float mx[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) mx[e] = kNegInf;
+      if (masked) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < kKeys; c0 += 32) {
+          uint32_t sr[32];
+          tc::ld_32x32b_x32(s_tmem + c0, sr);
+          tc::wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float v0 = c0 + c <= lim_rel ? __uint_as_float(sr[c]) : kNegInf;
+            const float v1 = c0 + c + 1 <= lim_rel ? __uint_as_float(sr[c + 1]) : kNegInf;
+            mx[(c >> 1) & 3] = max3f(mx[(c >> 1) & 3], v0, v1);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int c0 = 0; c0 < kKeys; c0 += 32) {
+          uint32_t sr[32];
+          tc::ld_32x32b_x32(s_tmem + c0, sr);
+          tc::wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; c += 2)
+            mx[(c >> 1) & 3] = max3f(mx[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+        }
+      }
+      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
+      // Reference max: moved only when the row max grows by more than 2^8
+      // (P stays <= 256, exact after the final division by l).  The first
+      // tile always sets it (key 0 is visible to every row).
+      const bool grow = (j == 0) || (mt > m + kRescaleThreshold);
+      const float m_new = grow ? fmaxf(m, mt) : m;
+      const float alpha = fast_exp2(m - m_new);  // 0 on the first tile, 1 when not moving
+      // pass 2: P = exp2(s * scale - m) as bf16 pairs into the first 64
+      // columns of S_X, 32 keys at a time (P of keys [32q, 32q + 32) goes to
+      // columns [16q, 16q + 16), which hold keys this pass has already read);
+      // pairs of columns go through the packed fp32 unit, row sum in 4 pairs
+      // of chains
+      const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
+      const uint64_t negm2 = f2_pack(-m_new, -m_new);
+      uint64_t acc2[4] = {0, 0, 0, 0};
+      auto chunk = [&](int q, bool msk) {
+        uint32_t sr[32];
+        tc::ld_32x32b_x32(s_tmem + q * 32, sr);
+        tc::wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float s0 = __uint_as_float(sr[2 * e]), s1 = __uint_as_float(sr[2 * e + 1]);
+          if (msk) {
+            s0 = q * 32 + 2 * e <= lim_rel ? s0 : kNegInf;
+            s1 = q * 32 + 2 * e + 1 <= lim_rel ? s1 : kNegInf;
+          }
+          const uint64_t t = f2_fma(f2_pack(s0, s1), scale2, negm2);
+          const float p0 = fast_exp2(f2_lo(t));  // exp2(-inf) = 0
+          const float p1 = fast_exp2(f2_hi(t));
+          acc2[e & 3] = f2_add(acc2[e & 3], f2_pack(p0, p1));
+          pk[e] = pack_bf16(p0, p1);
+        }
+        tc::st_32x32b_x16(s_tmem + q * 16, pk);
+      };
+      if (masked) {
+#pragma unroll 1
+        for (int q = 0; q < kKeys / 32; ++q) chunk(q, true);
+      } else {
+#pragma unroll 2
+        for (int q = 0; q < kKeys / 32; ++q) chunk(q, false);
+      }
+      const uint64_t a01 = f2_add(acc2[0], acc2[1]), a23 = f2_add(acc2[2], acc2[3]);
+      const uint64_t a4 = f2_add(a01, a23);
+      const float rs = f2_lo(a4) + f2_hi(a4);
+      l = l * alpha + rs;
+      m = m_new;
+      if (j >= 1 && __any_sync(0xffffffffu, alpha < 1.f)) {  // warp-uniform
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tc::ld_32x32b_x32(lane_base + o_col + c * 32, o);
+          tc::wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tc::st_32x32b_x32(lane_base + o_col + c * 32, o);
+        }
+      }
+      tc::wait_st();
+      if (x == 0 && kv0 + kKeys > it.kv_total) {
+        // keys past the end of the sequence hold arbitrary bits: zero those V
+        // rows (before P.V_A, which the tile's P.V_B follows)
+        if (!wait_warp(&bars[kVFull0 + g % kVStages], (g / kVStages) & 1)) { ok = false; break; }
+        if (kv0 + row >= it.kv_total) {
+          const uint32_t v_addr = sbase + Lay::kV + (g % kVStages) * Lay::kTile;
+#pragma unroll
+          for (int rg = 0; rg < Lay::kRegions; ++rg)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) sts128(v_addr + rg * kRegionBytes + sw128(row, c), make_uint4(0, 0, 0, 0));
+        }
+        tc::fence_proxy_async();
+      }
+      tc::fence_before();
+      mbar_arrive(&bars[kPFullA + x]);
+    }
+    if (!ok) break;
+    // ---- item epilogue: O / l -> bf16 rows of out (the item's last P.V_X done)
+    if (!wait_warp(&bars[kODoneA + x], k & 1)) { ok = false; break; }
+    tc::fence_after();
+    {
+      const float inv_l = 1.f / l;
+      const bool store = tok < it.n_b;
+      uint16_t* dst = p.out + (int64_t)(it.tokbase + (store ? tok : 0)) * p.Hq * D + (int64_t)h * D;
+      // 32 columns at a time in a rolled loop: this code runs once per item,
+      // so it is kept short (it competes for instruction cache with the tile loop)
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tc::ld_32x32b_x32(lane_base + o_col + c * 32, o);
+        tc::wait_ld();
+        if (store) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 v;
+            v.x = pack_bf16(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
+            v.y = pack_bf16(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
+            v.z = pack_bf16(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
+            v.w = pack_bf16(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
+            *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) = v;
+          }
+        }
+      }
+      // the O reads above are complete before the next item's first P.V_X overwrites O_X
+      tc::fence_before();
+    }
+    ++k;
+  }
 }
 
 template <int D>
@@ -216,7 +549,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kTmemSlot);
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = 1 << p.log2G;
 
   // Sequences longer than the host bound are left unwritten: flag them once.
   if (blockIdx.x == 0)
@@ -224,19 +556,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.cu_seqlens[b + 1] - p.cu_seqlens[b] > p.max_seqlen) set_status(p.status, ATTN_STATUS_BOUNDS);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kQBufs; ++s) {
-      mbar_init(&bars[kQFull0 + s], 1);
-      mbar_init(&bars[kQEmpty0 + s], 1);
-    }
-    for (int s = 0; s < kSBufs; ++s) {
-      mbar_init(&bars[kKFull0 + s], 1);
-      mbar_init(&bars[kSFull0 + s], 1);
-    }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars[kVFull0 + s], 1);
-      mbar_init(&bars[kPvDone0 + s], 1);
+      mbar_init(&bars[kQFullA + s], 1);
+      mbar_init(&bars[kQEmptyA + s], 1);
+      mbar_init(&bars[kSFullA + s], 1);
+      mbar_init(&bars[kPFullA + s], kSoftmaxThreads);
+      mbar_init(&bars[kODoneA + s], 1);
     }
-    mbar_init(&bars[kPFull], kSoftmaxThreads);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&bars[kKFull0 + s], 1);
+      mbar_init(&bars[kKEmpty0 + s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&bars[kVFull0 + s], 1);
+      mbar_init(&bars[kVEmpty0 + s], 1);
+    }
     mbar_init(&bars[kMmaDone], 1);
     fence_barrier_init();
   }
@@ -253,276 +587,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const SeqInfo* seq_tab = p.B <= kMaxSeqSmem ? reinterpret_cast<const SeqInfo*>(smem + Lay::kSeq) : nullptr;
   bool ok = true;
 
-  if (warp == kProducerWarp || warp == kVWarp) {
-    // ================================================================ TMA producers
-    if (lane == 0) {
-      const bool kstream = warp == kProducerWarp;
-      if (kstream) {
-        prefetch_tmap(&qmap);
-        prefetch_tmap(&kmap);
-      } else {
-        prefetch_tmap(&vmap);
-      }
-      TileWalk w, qw;  // K or V tiles; items whose Q tile is loaded next
-      w.start(p, seq_tab);
-      qw.start(p, seq_tab);
-      int g = 0;  // tiles issued so far
-      int q_issued = 0, issued = 0;
-      // Q tile of item qw.k into buffer qw.k % kQBufs (free once the last
-      // Q K^T of item qw.k - kQBufs has completed)
-      auto q_free = [&]() -> bool {
-        return qw.k < kQBufs || mbar_test_wait(&bars[kQEmpty0 + qw.k % kQBufs], (qw.k / kQBufs - 1) & 1);
-      };
-      auto issue_q = [&]() -> bool {
-        const int qs = qw.k % kQBufs;
-        if (qw.k >= kQBufs && !mbar_wait(&bars[kQEmpty0 + qs], (qw.k / kQBufs - 1) & 1)) return false;
-        mbar_arrive_expect_tx(&bars[kQFull0 + qs], Lay::kTile);
-#pragma unroll
-        for (int rg = 0; rg < Lay::kRegions; ++rg)
-          tma_load_3d(smem + Lay::kQ + qs * Lay::kTile + rg * kRegionBytes, &qmap,
-                      &bars[kQFull0 + qs], rg * 64, qw.it.kh * G, qw.it.tokbase + qw.it.t0);
-        q_issued = qw.k + 1;
-        qw.next_item(p);
-        return true;
-      };
-      const int full0 = kstream ? kKFull0 : kVFull0, empty0 = kstream ? kSFull0 : kPvDone0;
-      const int nst = kstream ? kSBufs : 2;  // ring stages
-      const int base = kstream ? Lay::kK : Lay::kV;
-      const CUtensorMap* map = kstream ? &kmap : &vmap;
-      while (w.valid && ok) {
-        if (kstream) {
-          while (qw.valid && qw.k <= w.k && ok) ok = issue_q();  // this item's Q
-          if (!ok) break;
-        }
-        const int st = g % nst;
-        if (g >= nst && !mbar_wait(&bars[empty0 + st], (g / nst - 1) & 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(&bars[full0 + st], Lay::kTile);
-#pragma unroll
-        for (int rg = 0; rg < Lay::kRegions; ++rg)
-          tma_load_3d(smem + base + st * Lay::kTile + rg * kRegionBytes, map, &bars[full0 + st],
-                      rg * 64, w.it.kh, (int)(w.it.slot0 + w.j * kKeys));
-        issued = g + 1;
-        // prefetch the next two items' Q tiles, without waiting for a buffer
-        while (kstream && ok && qw.valid && qw.k <= w.k + kQBufs - 1 && q_free()) ok = issue_q();
-        if (!ok) break;
-        ++g;
-        w.next_tile(p);
-      }
-      // Every load issued has landed before the CTA may exit (immediate on
-      // the normal path, where the consumers already waited for them).
-      for (int k = max(0, q_issued - kQBufs); k < q_issued; ++k)
-        (void)mbar_wait(&bars[kQFull0 + k % kQBufs], (k / kQBufs) & 1);
-      for (int t = max(0, issued - nst); t < issued; ++t)
-        (void)mbar_wait(&bars[full0 + t % nst], (t / nst) & 1);
-      if (!ok) set_status(p.status, ATTN_STATUS_TIMEOUT);
-    }
-  } else if (warp == kMmaWarp) {
-    // ================================================================ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kRows, kKeys, false);
-      constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kRows, D, true);
-      const uint32_t o_tmem = tmem + kTmemO;
-      TileWalk qk, pv;
-      qk.start(p, seq_tab);
-      pv.start(p, seq_tab);
-      int gq = 0, gp = 0;  // next tile for S = Q K^T, next tile for P.V
-      // S of tile gq goes to S buffer gq % 3, K stage gq % 3.  It may be issued
-      // once P.V of tile gq - 3 (which reads its P from that buffer) has been
-      // issued: tensor-core operations run in issue order.  With block ==
-      // false issue_qk returns false, issuing nothing, when the tile's K (or,
-      // on an item's first tile, its Q) is not in shared memory yet.
-      auto issue_qk = [&](bool block) -> bool {
-        const int sb = gq % kSBufs, qs = qk.k % kQBufs;
-        if (qk.j == 0) {
-          uint64_t* qb = &bars[kQFull0 + qs];
-          const uint32_t qpar = (qk.k / kQBufs) & 1;
-          if (block ? !mbar_wait(qb, qpar) : !mbar_test_wait(qb, qpar)) {
-            if (block) ok = false;
-            return false;
-          }
-        }
-        uint64_t* kb = &bars[kKFull0 + sb];
-        const uint32_t kpar = (gq / kSBufs) & 1;
-        if (block ? !mbar_wait(kb, kpar) : !mbar_test_wait(kb, kpar)) {
-          if (block) ok = false;
-          return false;
-        }
-        tc::fence_after();
-        const uint64_t qd = tc::sdesc_sw128(sbase + Lay::kQ + qs * Lay::kTile, 16, 1024);
-        const uint64_t kd = tc::sdesc_sw128(sbase + Lay::kK + sb * Lay::kTile, 16, 1024);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t off = (uint64_t)(((ks >> 2) * kRegionBytes + (ks & 3) * 32) >> 4);
-          tc::mma_f16_ss(tmem + (uint32_t)sb * 128, qd + off, kd + off, idesc_s, ks > 0);
-        }
-        tc::commit(&bars[kSFull0 + sb]);  // S ready, K stage sb free
-        if (qk.j == qk.it.nk - 1) tc::commit(&bars[kQEmpty0 + qs]);  // last use of this Q tile
-        ++gq;
-        qk.next_tile(p);
-        return true;
-      };
-      while (pv.valid && ok) {
-        // the S that P.V of tile gp consumes must be under way (blocking) ...
-        while (ok && qk.valid && gq <= gp) issue_qk(true);
-        if (!ok) break;
-        // ... and S of up to kLookahead more tiles, as far as they are loaded
-        while (ok && qk.valid && gq <= gp + kLookahead && issue_qk(false)) {
-        }
-        if (!mbar_wait(&bars[kPFull], gp & 1)) { ok = false; break; }
-        const int st = gp & 1;
-        if (!mbar_wait(&bars[kVFull0 + st], (gp >> 1) & 1)) { ok = false; break; }
-        tc::fence_after();
-        const uint32_t p_tmem = tmem + (uint32_t)(gp % kSBufs) * 128;  // P in its S buffer
-        const uint64_t vd = tc::sdesc_sw128(sbase + Lay::kV + st * Lay::kTile, kRegionBytes, 1024);
-#pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk)
-          tc::mma_f16_ts(o_tmem, p_tmem + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), idesc_o,
-                         (pv.j > 0 || kk > 0) ? 1u : 0u);
-        tc::commit(&bars[kPvDone0 + st]);  // O updated, V stage st free
-        ++gp;
-        pv.next_tile(p);
-      }
-      // Nothing may still be running on the tensor cores when TMEM is freed.
-      tc::commit(&bars[kMmaDone]);
-      (void)mbar_wait(&bars[kMmaDone], 0);
-      if (!ok) set_status(p.status, ATTN_STATUS_TIMEOUT);
-    }
+  if (warp < 8) {
+    softmax_tile<D>(p, seq_tab, sbase, tmem, bars, warp >> 2, ok);
   } else {
-    // ================================================================ softmax warpgroup
-    const int row = threadIdx.x;  // 0..127 = TMEM lane
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    TileWalk w;
-    w.start(p, seq_tab);
-    int g = 0;  // KV tiles processed so far
-    while (w.valid && ok) {
-      const Item it = w.it;
-      w.next_item(p);  // the next item's bounds load while this item runs
-      const int tl = row >> p.log2G;
-      const int tok = it.t0 + tl;
-      const int h = it.kh * G + (row & (G - 1));
-      const int lim = tok < it.n_b ? it.cached + tok : it.kv_total - 1;  // last key this row sees
-      const int cta_min_lim = it.cached + it.t0;
-      float m = kNegInf, l = 0.f;
-      for (int j = 0; j < it.nk; ++j, ++g) {
-        if (!wait_warp(&bars[kSFull0 + g % kSBufs], (g / kSBufs) & 1)) { ok = false; break; }
-        tc::fence_after();
-        const uint32_t s_tmem = lane_base + (uint32_t)(g % kSBufs) * 128;
-        const int kv0 = j * kKeys;
-        // keys past this row's causal limit count as -inf (select, so arbitrary
-        // bits in keys past the sequence end cannot leak through)
-        const bool masked = kv0 + kKeys - 1 > cta_min_lim;
-        const int lim_rel = lim - kv0;  // columns c <= lim_rel are visible
-        uint32_t sr[kKeys];
-#pragma unroll
-        for (int c = 0; c < kKeys / 32; ++c) tc::ld_32x32b_x32(s_tmem + c * 32, sr + c * 32);
-        tc::wait_ld();
-        if (masked) {
-#pragma unroll
-          for (int c = 0; c < kKeys; ++c) sr[c] = c <= lim_rel ? sr[c] : __float_as_uint(kNegInf);
-        }
-        // row max, 8 independent chains (instruction-level parallelism)
-        float mx[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mx[e] = __uint_as_float(sr[e]);
-#pragma unroll
-        for (int c = 8; c < kKeys; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(sr[c]));
-        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
-        // Reference max: moved only when the row max grows by more than 2^8
-        // (P stays <= 256, exact after the final division by l).  The first
-        // tile always sets it (key 0 is visible to every row).
-        const bool grow = (j == 0) || (mt > m + kRescaleThreshold);
-        const float m_new = grow ? fmaxf(m, mt) : m;
-        const float alpha = fast_exp2(m - m_new);  // 0 on the first tile, 1 when not moving
-        const float neg_m = -m_new;
-        // P = exp2(s * scale - m) as bf16 pairs into the first 64 columns of
-        // this tile's S buffer (S is in registers now), row sum in 8 chains
-        float acc[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        const uint32_t p_tmem = s_tmem;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int c = h * 64 + 2 * e;
-            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c]), p.scale_log2, neg_m));  // exp2(-inf) = 0
-            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c + 1]), p.scale_log2, neg_m));
-            acc[(2 * e) & 7] += p0;
-            acc[(2 * e + 1) & 7] += p1;
-            pk[e] = pack_bf16(p0, p1);
-          }
-          tc::st_32x32b_x32(p_tmem + h * 32, pk);
-        }
-        const float rs = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-        l = l * alpha + rs;
-        m = m_new;
-        if (j >= 1) {
-          // O may only be rescaled once the previous tile's P.V is complete
-          if (!wait_warp(&bars[kPvDone0 + ((g - 1) & 1)], ((g - 1) >> 1) & 1)) { ok = false; break; }
-          tc::fence_after();
-          if (__any_sync(0xffffffffu, alpha < 1.f)) {  // warp-uniform
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t o[32];
-              tc::ld_32x32b_x32(lane_base + kTmemO + c * 32, o);
-              tc::wait_ld();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-              tc::st_32x32b_x32(lane_base + kTmemO + c * 32, o);
-            }
-          }
-        }
-        tc::wait_st();
-        if (kv0 + kKeys > it.kv_total) {
-          // keys past the end of the sequence hold arbitrary bits: zero those V rows
-          if (!wait_warp(&bars[kVFull0 + (g & 1)], (g >> 1) & 1)) { ok = false; break; }
-          if (kv0 + row >= it.kv_total) {
-            const uint32_t v_addr = sbase + Lay::kV + (g & 1) * Lay::kTile;
-#pragma unroll
-            for (int rg = 0; rg < Lay::kRegions; ++rg)
-#pragma unroll
-              for (int c = 0; c < 8; ++c) sts128(v_addr + rg * kRegionBytes + sw128(row, c), make_uint4(0, 0, 0, 0));
-          }
-          tc::fence_proxy_async();
-        }
-        tc::fence_before();
-        mbar_arrive(&bars[kPFull]);
-      }
-      if (!ok) break;
-      // ---- item epilogue: O / l -> bf16 rows of out (P.V of its last tile done)
-      if (!wait_warp(&bars[kPvDone0 + ((g - 1) & 1)], ((g - 1) >> 1) & 1)) { ok = false; break; }
-      tc::fence_after();
-      {
-        const float inv_l = 1.f / l;
-        const bool store = tok < it.n_b;
-        uint16_t* dst = p.out + (int64_t)(it.tokbase + (store ? tok : 0)) * p.Hq * D + (int64_t)h * D;
-        // 32 columns at a time in a rolled loop: this code runs once per item,
-        // so it is kept short (it competes for instruction cache with the tile loop)
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tc::ld_32x32b_x32(lane_base + kTmemO + c * 32, o);
-          tc::wait_ld();
-          if (store) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 v;
-              v.x = pack_bf16(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
-              v.y = pack_bf16(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
-              v.z = pack_bf16(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
-              v.w = pack_bf16(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
-              *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) = v;
-            }
-          }
-        }
-        // the O reads above are complete before the next item's first P.V overwrites O
-        tc::fence_before();
-      }
+    if (lane == 0) {
+      if (warp == kKWarp)
+        produce_kv<D>(p, seq_tab, &kmap, smem, bars, Lay::kK, kKFull0, kKEmpty0, kKStages, ok);
+      else if (warp == kVWarp)
+        produce_kv<D>(p, seq_tab, &vmap, smem, bars, Lay::kV, kVFull0, kVEmpty0, kVStages, ok);
+      else if (warp == kQWarp)
+        produce_q<D>(p, seq_tab, &qmap, smem, bars, ok);
+      else
+        issue_mma<D>(p, seq_tab, sbase, tmem, bars, ok);
     }
-    if (!ok) set_status(p.status, ATTN_STATUS_TIMEOUT);
   }
+  if (!ok) set_status(p.status, ATTN_STATUS_TIMEOUT);
 
   tc::fence_before();
   __syncthreads();
@@ -536,7 +615,7 @@ int launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream) {
   const int Hq = a.cfg.num_q_heads, Hkv = a.cfg.num_kv_heads;
   const int G = Hq / Hkv;
   const int log2G = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
-  const int BT = kRows / G;
+  const int BT = kTileRows / G;
   CacheMaps maps;
   if (make_cache_maps(a.kv, Hkv, D, kKeys, &maps) != 0) return ATTN_ELAUNCH;
   CUtensorMap qmap;  // prepared Q viewed as [N, Hq, D]
@@ -557,10 +636,9 @@ int launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream) {
   p.N = a.N;
   p.B = a.B;
   p.max_seqlen = a.max_seqlen;
-  const int64_t nv = ((int64_t)(a.N >> p.log2BT) + a.B) * Hkv;
+  const int64_t nv = ((int64_t)(a.N >> (p.log2BT + 1)) + a.B) * Hkv;
   if (nv > (int64_t(1) << 30)) return ATTN_EINVAL;
   p.num_vitems = (int)nv;
-
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
