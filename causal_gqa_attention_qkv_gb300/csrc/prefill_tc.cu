@@ -20,7 +20,7 @@
 //               tile: read S from TMEM, mask, online softmax in fp32 (exp2
 //               domain), P (bf16) written over S in TMEM, O rescaled in TMEM
 //               when the reference max moves; per item: O / l -> out.
-//   warp 8      TMA: K tiles (3-stage ring of 128 keys, across items).
+//   warp 8      TMA: K tiles (2-stage ring of 128 keys, across items).
 //   warp 9      MMA issuer (one thread) and TMEM owner.
 //   warp 10     TMA: V tiles (2-stage ring).
 //   warp 11     TMA: the item's two Q tiles (one buffer each).
@@ -49,7 +49,7 @@ constexpr int kKWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kVWarp = 10;
 constexpr int kQWarp = 11;
-constexpr int kKStages = 3;
+constexpr int kKStages = 2;
 constexpr int kVStages = 2;
 constexpr int kMaxSeqSmem = 32;  // sequences whose facts are cached in shared memory
 constexpr uint32_t kTmemCols = 512;
@@ -77,7 +77,9 @@ struct TcLayout {
   static constexpr int kQ = 0;                       // Q tiles A, B
   static constexpr int kK = kQ + 2 * kTile;          // kKStages
   static constexpr int kV = kK + kKStages * kTile;   // kVStages
-  static constexpr int kBar = kV + kVStages * kTile;
+  // output staging for TMA stores: 4 KB (32 rows x 64 columns bf16) per softmax warp
+  static constexpr int kStg = kV + kVStages * kTile;
+  static constexpr int kBar = kStg + 8 * 4096;
   static constexpr int kNumBars = 32;
   static constexpr int kSeq = kBar + kNumBars * 8;  // SeqInfo[kMaxSeqSmem]
   static constexpr int kTmemSlot = kSeq + kMaxSeqSmem * 24;
@@ -371,7 +373,7 @@ __device__ void issue_mma(const TcPar& p, const SeqInfo* seq_tab, uint32_t sbase
 // Softmax and epilogue of Q tile x (0: A, 1: B) of every item.
 template <int D>
 __device__ void softmax_tile(const TcPar& p, const SeqInfo* seq_tab, uint32_t sbase, uint32_t tmem,
-                             uint64_t* bars, int x, bool& ok) {
+                             uint64_t* bars, const CUtensorMap* omap, int x, bool& ok) {
   using Lay = TcLayout<D>;
   const int row = threadIdx.x & (kSoftmaxThreads - 1);  // = TMEM lane
   const int warp = threadIdx.x >> 5;
@@ -509,24 +511,52 @@ __device__ void softmax_tile(const TcPar& p, const SeqInfo* seq_tab, uint32_t sb
     tc::fence_after();
     {
       const float inv_l = 1.f / l;
+      // This warp's 32 rows are 32/G whole tokens.  When all of them belong to
+      // the sequence they leave through this warp's staging slot (128-byte
+      // swizzled, the layout of a 64 d x G heads x 32/G tokens box) by TMA
+      // stores, 64 columns at a time; otherwise row by row (rows inside the
+      // sequence only).
+      const int tpw = 32 >> p.log2G;
+      const int wtok0 = it.t0 + x * BT + (warp & 3) * tpw;
+      const bool full = wtok0 + tpw <= it.n_b;  // warp-uniform
+      const uint32_t slot = sbase + Lay::kStg + warp * 4096;
+      const int lane = threadIdx.x & 31;
       const bool store = tok < it.n_b;
       uint16_t* dst = p.out + (int64_t)(it.tokbase + (store ? tok : 0)) * p.Hq * D + (int64_t)h * D;
-      // 32 columns at a time in a rolled loop: this code runs once per item,
-      // so it is kept short (it competes for instruction cache with the tile loop)
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tc::ld_32x32b_x32(lane_base + o_col + c * 32, o);
+      for (int half = 0; half < D / 64; ++half) {
+        uint32_t o[64];
+        tc::ld_32x32b_x32(lane_base + o_col + half * 64, o);
+        tc::ld_32x32b_x32(lane_base + o_col + half * 64 + 32, o + 32);
         tc::wait_ld();
-        if (store) {
+        if (full) {
+          // the slot's previous contents have been read by their TMA store
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int c = 0; c < 8; ++c) {
             uint4 v;
-            v.x = pack_bf16(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
-            v.y = pack_bf16(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
-            v.z = pack_bf16(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
-            v.w = pack_bf16(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
-            *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) = v;
+            v.x = pack_bf16(__uint_as_float(o[8 * c + 0]) * inv_l, __uint_as_float(o[8 * c + 1]) * inv_l);
+            v.y = pack_bf16(__uint_as_float(o[8 * c + 2]) * inv_l, __uint_as_float(o[8 * c + 3]) * inv_l);
+            v.z = pack_bf16(__uint_as_float(o[8 * c + 4]) * inv_l, __uint_as_float(o[8 * c + 5]) * inv_l);
+            v.w = pack_bf16(__uint_as_float(o[8 * c + 6]) * inv_l, __uint_as_float(o[8 * c + 7]) * inv_l);
+            sts128(slot + sw128(lane, c), v);
+          }
+          tc::fence_proxy_async();  // the rows are visible to the TMA engine
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(omap, slot, half * 64, it.kh * G, it.tokbase + wtok0);
+            bulk_commit_group();
+          }
+        } else if (store) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4 v;
+            v.x = pack_bf16(__uint_as_float(o[8 * c + 0]) * inv_l, __uint_as_float(o[8 * c + 1]) * inv_l);
+            v.y = pack_bf16(__uint_as_float(o[8 * c + 2]) * inv_l, __uint_as_float(o[8 * c + 3]) * inv_l);
+            v.z = pack_bf16(__uint_as_float(o[8 * c + 4]) * inv_l, __uint_as_float(o[8 * c + 5]) * inv_l);
+            v.w = pack_bf16(__uint_as_float(o[8 * c + 6]) * inv_l, __uint_as_float(o[8 * c + 7]) * inv_l);
+            *reinterpret_cast<uint4*>(dst + half * 64 + c * 8) = v;
           }
         }
       }
@@ -535,13 +565,15 @@ __device__ void softmax_tile(const TcPar& p, const SeqInfo* seq_tab, uint32_t sb
     }
     ++k;
   }
+  if ((threadIdx.x & 31) == 0) bulk_wait_all();  // every output store has completed
 }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                       const __grid_constant__ CUtensorMap kmap,
-                      const __grid_constant__ CUtensorMap vmap, const TcPar p) {
+                      const __grid_constant__ CUtensorMap vmap,
+                      const __grid_constant__ CUtensorMap omap, const TcPar p) {
   using Lay = TcLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -588,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool ok = true;
 
   if (warp < 8) {
-    softmax_tile<D>(p, seq_tab, sbase, tmem, bars, warp >> 2, ok);
+    softmax_tile<D>(p, seq_tab, sbase, tmem, bars, &omap, warp >> 2, ok);
   } else {
     if (lane == 0) {
       if (warp == kKWarp)
@@ -620,6 +652,8 @@ int launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream) {
   if (make_cache_maps(a.kv, Hkv, D, kKeys, &maps) != 0) return ATTN_ELAUNCH;
   CUtensorMap qmap;  // prepared Q viewed as [N, Hq, D]
   if (make_qkv_map(a.q, a.N, Hq, D, G, BT, &qmap) != 0) return ATTN_ELAUNCH;
+  CUtensorMap omap;  // out viewed as [N, Hq, D]; one softmax warp's 32 rows per box
+  if (make_qkv_map(a.out, a.N, Hq, D, G, 32 / G, &omap) != 0) return ATTN_ELAUNCH;
   TcPar p;
   p.cu_seqlens = a.cu_seqlens;
   p.slot_base = a.kv.slot_base;
@@ -647,7 +681,7 @@ int launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream) {
                            Lay::kSmemBytes) != cudaSuccess)
     return ATTN_ELAUNCH;
   const int grid = (int)std::min<int64_t>(sms, nv);
-  prefill_tc_kernel<D><<<grid, kThreads, Lay::kSmemBytes, stream>>>(qmap, maps.k, maps.v, p);
+  prefill_tc_kernel<D><<<grid, kThreads, Lay::kSmemBytes, stream>>>(qmap, maps.k, maps.v, omap, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
 }
 
