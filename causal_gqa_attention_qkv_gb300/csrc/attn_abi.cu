@@ -79,6 +79,8 @@ size_t partial_bytes(const attn_config_t& c, int64_t B, int max_splits) {
 }
 
 int32_t* status_of(void* ws) { return static_cast<int32_t*>(ws); }
+// prefill work-item counters: 64 bytes into the header
+int32_t* work_of(void* ws) { return static_cast<int32_t*>(ws) + 16; }
 
 }  // namespace
 
@@ -168,6 +170,7 @@ int prefill_attend(const attn_config_t* cfg, const void* q, const int32_t* cu_se
   pa.q = q;
   pa.out = out;
   pa.status = status_of(workspace);
+  pa.work = work_of(workspace);
   return launch_prefill(pa, s);
 }
 

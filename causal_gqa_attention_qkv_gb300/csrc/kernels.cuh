@@ -67,6 +67,9 @@ struct PrefillArgs {
   const void* q;  // [N, Hq, D] bf16, normed and rotated
   void* out;      // [N, Hq*D] bf16
   int32_t* status;
+  // two int32 in the workspace header: next work item, CTAs finished; zero
+  // before the launch, left zero by it
+  int32_t* work;
 };
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 

@@ -11,8 +11,11 @@
 // KV head kh, block of 2 x 128 query rows).  A 128-row Q tile is 128/G tokens
 // x the G heads of the group, so every K/V tile loaded serves the whole GQA
 // group; the item's two Q tiles (A: its first 128/G tokens, B: the next
-// 128/G) share every K/V tile.  Items are numbered sequence by sequence,
-// heaviest block of a sequence first; CTA c takes items c, c + gridDim.x, ...
+// 128/G) share every K/V tile.  Items are numbered round-major: round r holds
+// block r counted from the end of every sequence (the heaviest blocks come
+// first, the last ones claimed are light), and are handed out dynamically: a
+// CTA's Q producer claims the next number from a counter in the workspace and
+// publishes it to the CTA's other roles through a ring in shared memory.
 //
 // Roles (384 threads, three warpgroups):
 //   warps 0-3   softmax of Q tile A, warps 4-7 softmax of Q tile B: thread r
@@ -23,7 +26,7 @@
 //   warp 8      TMA: K tiles (2-stage ring of 128 keys, across items).
 //   warp 9      MMA issuer (one thread) and TMEM owner.
 //   warp 10     TMA: V tiles (2-stage ring).
-//   warp 11     TMA: the item's two Q tiles (one buffer each).
+//   warp 11     claims items; TMA: the item's two Q tiles (one buffer each).
 // Each producer runs in a warp of its own: a thread waiting for a free stage
 // may be suspended, and diverged lanes of one warp do not run independently.
 //
@@ -52,6 +55,9 @@ constexpr int kQWarp = 11;
 constexpr int kKStages = 2;
 constexpr int kVStages = 2;
 constexpr int kMaxSeqSmem = 32;  // sequences whose facts are cached in shared memory
+constexpr int kRing = 4;         // claimed items published ahead of their use
+// readers of each ring slot: K, V and MMA threads, one per softmax warp
+constexpr int kRingReaders = 3 + 8;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 256;  // O_A at 256, O_B at 384; S_A at 0, S_B at 128
 constexpr int kRegionBytes = 128 * 128;   // 128 rows x 128 bytes (64 bf16)
@@ -64,10 +70,11 @@ struct TcPar {
   const int32_t* slot_capacity;
   int64_t num_slots;
   int32_t* status;
+  int32_t* work;  // [0]: next item to claim, [1]: CTAs finished
   uint16_t* out;
   float scale_log2;  // log2(e) / sqrt(D)
   int32_t Hq, Hkv, log2G, log2BT, N, B, max_seqlen;
-  int32_t num_vitems;  // ((N >> (log2BT + 1)) + B) * Hkv: size of the item numbering
+  int32_t num_vitems;  // rounds x B x Hkv, rounds = ceil(max_seqlen / (2 x 128/G))
 };
 
 template <int D>
@@ -82,7 +89,8 @@ struct TcLayout {
   static constexpr int kBar = kStg + 8 * 4096;
   static constexpr int kNumBars = 32;
   static constexpr int kSeq = kBar + kNumBars * 8;  // SeqInfo[kMaxSeqSmem]
-  static constexpr int kTmemSlot = kSeq + kMaxSeqSmem * 24;
+  static constexpr int kRingOff = kSeq + kMaxSeqSmem * 24;  // int[kRing]
+  static constexpr int kTmemSlot = kRingOff + kRing * 4;
   // + alignment slack; at least 116 KB so that one CTA runs per SM (each CTA
   // allocates all 512 TMEM columns).
   static constexpr int kSmemRaw = kTmemSlot + 16 + 1024;
@@ -99,15 +107,15 @@ enum Bar {
   kSFullA = kVEmpty0 + kVStages, kSFullB,     // S_X of a tile complete (and every earlier MMA)
   kPFullA, kPFullB,                           // P_X of a tile in TMEM (128 arrivals)
   kODoneA, kODoneB,                           // the item's last P.V_X complete
-  kMmaDone
+  kMmaDone,
+  kItemFull0, kItemFree0 = kItemFull0 + kRing,  // item ring: slot written / read by every role
+  kBarCount = kItemFree0 + kRing
 };
+static_assert(kBarCount <= TcLayout<64>::kNumBars, "barriers");
 
 // ---------------------------------------------------------------- work items
-// Item numbering without a table: sequence b owns the "virtual blocks"
-// [vstart(b), vstart(b) + nblocks(b)) with vstart(b) = cu_seqlens[b] / IT + b
-// (IT = 2 x 128/G tokens per item; these ranges never overlap, each sequence
-// leaves at most one slot empty).  Virtual item i = (virtual block i / Hkv,
-// KV head i % Hkv).
+// Item number vi = (r * B + b) * Hkv + kh: block r counted from the end of
+// sequence b (an empty slot when sequence b has r blocks or fewer), KV head kh.
 struct Item {
   int b, kh, t0, n_b, tokbase, cached, nk, kv_total;
   int64_t slot0;
@@ -137,24 +145,18 @@ __device__ __forceinline__ SeqInfo seq_info(const TcPar& p, int b) {
 }
 
 __device__ __forceinline__ bool item_at(const TcPar& p, const SeqInfo* tab, int vi, Item& it) {
-  const int v = vi / p.Hkv;
-  it.kh = vi - v * p.Hkv;
-  const int log2IT = p.log2BT + 1;
-  int lo = 0, hi = p.B;  // largest b with vstart(b) <= v
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    const int cu = tab ? tab[mid].tokbase : p.cu_seqlens[mid];
-    if ((cu >> log2IT) + mid <= v) lo = mid; else hi = mid;
-  }
-  const int b = lo;
+  const int rb = vi / p.Hkv;
+  it.kh = vi - rb * p.Hkv;
+  const int r = rb / p.B;
+  const int b = rb - r * p.B;
   const SeqInfo q = tab ? tab[b] : seq_info(p, b);
   if (!q.usable) return false;
+  const int log2IT = p.log2BT + 1;
   const int IT = 1 << log2IT;
   const int nblk = (q.n_b + IT - 1) >> log2IT;
-  const int bfe = v - ((q.tokbase >> log2IT) + b);  // block index counted from the end
-  if (bfe < 0 || bfe >= nblk) return false;
+  if (r >= nblk) return false;
   it.b = b;
-  it.t0 = (nblk - 1 - bfe) * IT;  // heaviest block first
+  it.t0 = (nblk - 1 - r) * IT;
   it.n_b = q.n_b;
   it.tokbase = q.tokbase;
   it.cached = q.cached;
@@ -164,25 +166,43 @@ __device__ __forceinline__ bool item_at(const TcPar& p, const SeqInfo* tab, int 
   return true;
 }
 
-// Walks this CTA's items in order.
+// Reads this CTA's items from the ring in order.  A number < 0 ends the walk.
+// Single-thread roles acknowledge each slot themselves; in a softmax warp all
+// lanes read it and lane 0 acknowledges.
 struct ItemWalk {
   const SeqInfo* tab;  // shared-memory sequence table or nullptr
-  int vi;              // current virtual item
+  const int* ring;
+  uint64_t* bars;
+  int k;               // items read so far
+  bool warp_wide;
   bool valid;
   Item it;
 
-  __device__ __forceinline__ void start(const TcPar& p, const SeqInfo* table) {
+  __device__ __forceinline__ void start(const TcPar& p, const SeqInfo* table, const int* ring_,
+                                        uint64_t* bars_, bool warp_wide_, bool& ok) {
     tab = table;
-    vi = blockIdx.x - (int)gridDim.x;
-    next(p);
+    ring = ring_;
+    bars = bars_;
+    k = 0;
+    warp_wide = warp_wide_;
+    next(p, ok);
   }
-  __device__ __forceinline__ void next(const TcPar& p) {
-    for (vi += gridDim.x; vi < p.num_vitems; vi += gridDim.x)
-      if (item_at(p, tab, vi, it)) {
-        valid = true;
-        return;
-      }
-    valid = false;
+  __device__ __forceinline__ void next(const TcPar& p, bool& ok) {
+    const int slot = k % kRing;
+    uint64_t* full = &bars[kItemFull0 + slot];
+    const uint32_t par = (k / kRing) & 1;
+    bool got = mbar_wait(full, par);
+    if (warp_wide) got = __all_sync(0xffffffffu, got);
+    if (!got) {
+      ok = false;
+      valid = false;
+      return;
+    }
+    const int vi = *reinterpret_cast<const volatile int*>(&ring[slot]);
+    if (warp_wide) __syncwarp();
+    if (!warp_wide || (threadIdx.x & 31) == 0) mbar_arrive(&bars[kItemFree0 + slot]);
+    ++k;
+    valid = vi >= 0 && item_at(p, tab, vi, it);
   }
 };
 
@@ -236,13 +256,13 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
 // One TMA producer ring (K or V tiles): tile g of the CTA's tile sequence goes
 // to stage g % stages once the stage's previous tile has been consumed.
 template <int D>
-__device__ void produce_kv(const TcPar& p, const SeqInfo* seq_tab, const CUtensorMap* map,
-                           uint8_t* smem, uint64_t* bars, int base, int full0, int empty0,
-                           int stages, bool& ok) {
+__device__ void produce_kv(const TcPar& p, const SeqInfo* seq_tab, const int* ring,
+                           const CUtensorMap* map, uint8_t* smem, uint64_t* bars, int base,
+                           int full0, int empty0, int stages, bool& ok) {
   using Lay = TcLayout<D>;
   prefetch_tmap(map);
   ItemWalk w;
-  w.start(p, seq_tab);
+  w.start(p, seq_tab, ring, bars, false, ok);
   int g = 0;
   while (w.valid && ok) {
     for (int j = 0; j < w.it.nk; ++j, ++g) {
@@ -254,42 +274,54 @@ __device__ void produce_kv(const TcPar& p, const SeqInfo* seq_tab, const CUtenso
         tma_load_3d(smem + base + st * Lay::kTile + rg * kRegionBytes, map, &bars[full0 + st],
                     rg * 64, w.it.kh, (int)(w.it.slot0 + j * kKeys));
     }
-    w.next(p);
+    if (!ok) break;
+    w.next(p, ok);
   }
   // Every load issued has landed before the CTA may exit (immediate on the
   // normal path, where the consumers already waited for them).
   for (int t = max(0, g - stages); t < g; ++t) (void)mbar_wait(&bars[full0 + t % stages], (t / stages) & 1);
 }
 
+// Claims items from the counter in the workspace, publishes each to the
+// ring and loads its two Q tiles.  The last slot written holds -1.
 template <int D>
-__device__ void produce_q(const TcPar& p, const SeqInfo* seq_tab, const CUtensorMap* qmap,
-                          uint8_t* smem, uint64_t* bars, bool& ok) {
+__device__ void produce_q(const TcPar& p, const SeqInfo* seq_tab, int* ring,
+                          const CUtensorMap* qmap, uint8_t* smem, uint64_t* bars, bool& ok) {
   using Lay = TcLayout<D>;
   prefetch_tmap(qmap);
   const int G = 1 << p.log2G, BT = 1 << p.log2BT;
-  ItemWalk w;
-  w.start(p, seq_tab);
   int k = 0;
-  while (w.valid && ok) {
+  while (ok) {
+    int vi;
+    Item it;
+    bool have = false;
+    while ((vi = atomicAdd(p.work, 1)) < p.num_vitems)
+      if (item_at(p, seq_tab, vi, it)) {
+        have = true;
+        break;
+      }
+    const int slot = k % kRing;
+    if (k >= kRing && !mbar_wait(&bars[kItemFree0 + slot], (k / kRing - 1) & 1)) { ok = false; break; }
+    ring[slot] = have ? vi : -1;
+    mbar_arrive(&bars[kItemFull0 + slot]);  // release: the slot's value is visible to its readers
+    if (!have) break;
     for (int x = 0; x < 2; ++x) {
       if (k >= 1 && !mbar_wait(&bars[kQEmptyA + x], (k - 1) & 1)) { ok = false; break; }
       mbar_arrive_expect_tx(&bars[kQFullA + x], Lay::kTile);
 #pragma unroll
       for (int rg = 0; rg < Lay::kRegions; ++rg)
         tma_load_3d(smem + Lay::kQ + x * Lay::kTile + rg * kRegionBytes, qmap, &bars[kQFullA + x],
-                    rg * 64, w.it.kh * G, w.it.tokbase + w.it.t0 + x * BT);
+                    rg * 64, it.kh * G, it.tokbase + it.t0 + x * BT);
     }
-    if (!ok) break;
     ++k;
-    w.next(p);
   }
   if (k >= 1)
     for (int x = 0; x < 2; ++x) (void)mbar_wait(&bars[kQFullA + x], (k - 1) & 1);
 }
 
 template <int D>
-__device__ void issue_mma(const TcPar& p, const SeqInfo* seq_tab, uint32_t sbase, uint32_t tmem,
-                          uint64_t* bars, bool& ok) {
+__device__ void issue_mma(const TcPar& p, const SeqInfo* seq_tab, const int* ring, uint32_t sbase,
+                          uint32_t tmem, uint64_t* bars, bool& ok) {
   using Lay = TcLayout<D>;
   constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kTileRows, kKeys, false);
   constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kTileRows, D, true);
@@ -312,7 +344,7 @@ __device__ void issue_mma(const TcPar& p, const SeqInfo* seq_tab, uint32_t sbase
                      vd + (uint64_t)((kk * 2048) >> 4), idesc_o, (acc || kk > 0) ? 1u : 0u);
   };
   ItemWalk w;
-  w.start(p, seq_tab);
+  w.start(p, seq_tab, ring, bars, false, ok);
   int g = 0;  // KV tiles of this CTA so far
   int k = 0;  // items so far
   while (w.valid && ok) {
@@ -361,9 +393,10 @@ __device__ void issue_mma(const TcPar& p, const SeqInfo* seq_tab, uint32_t sbase
         if (j + 1 == nk - 1) tc::commit(&bars[kQEmptyB]);
       }
     }
+    if (!ok) break;
     g += nk;
     ++k;
-    w.next(p);
+    w.next(p, ok);
   }
   // Nothing may still be running on the tensor cores when TMEM is freed.
   tc::commit(&bars[kMmaDone]);
@@ -372,8 +405,8 @@ __device__ void issue_mma(const TcPar& p, const SeqInfo* seq_tab, uint32_t sbase
 
 // Softmax and epilogue of Q tile x (0: A, 1: B) of every item.
 template <int D>
-__device__ void softmax_tile(const TcPar& p, const SeqInfo* seq_tab, uint32_t sbase, uint32_t tmem,
-                             uint64_t* bars, const CUtensorMap* omap, int x, bool& ok) {
+__device__ void softmax_tile(const TcPar& p, const SeqInfo* seq_tab, const int* ring, uint32_t sbase,
+                             uint32_t tmem, uint64_t* bars, const CUtensorMap* omap, int x, bool& ok) {
   using Lay = TcLayout<D>;
   const int row = threadIdx.x & (kSoftmaxThreads - 1);  // = TMEM lane
   const int warp = threadIdx.x >> 5;
@@ -381,12 +414,12 @@ __device__ void softmax_tile(const TcPar& p, const SeqInfo* seq_tab, uint32_t sb
   const uint32_t s_col = (uint32_t)x * 128, o_col = kTmemO + (uint32_t)x * 128;
   const int G = 1 << p.log2G, BT = 1 << p.log2BT;
   ItemWalk w;
-  w.start(p, seq_tab);
+  w.start(p, seq_tab, ring, bars, true, ok);
   int g = 0;  // KV tiles processed so far
   int k = 0;  // items processed so far
   while (w.valid && ok) {
     const Item it = w.it;
-    w.next(p);  // the next item's bounds load while this item runs
+    w.next(p, ok);  // the next item's bounds load while this item runs
     const int tok = it.t0 + x * BT + (row >> p.log2G);
     const int h = it.kh * G + (row & (G - 1));
     const int lim = tok < it.n_b ? it.cached + tok : it.kv_total - 1;  // last key this row sees
@@ -604,6 +637,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars[kVEmpty0 + s], 1);
     }
     mbar_init(&bars[kMmaDone], 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&bars[kItemFull0 + s], 1);
+      mbar_init(&bars[kItemFree0 + s], kRingReaders);
+    }
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -617,20 +654,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
   const SeqInfo* seq_tab = p.B <= kMaxSeqSmem ? reinterpret_cast<const SeqInfo*>(smem + Lay::kSeq) : nullptr;
+  int* ring = reinterpret_cast<int*>(smem + Lay::kRingOff);
   bool ok = true;
 
   if (warp < 8) {
-    softmax_tile<D>(p, seq_tab, sbase, tmem, bars, &omap, warp >> 2, ok);
+    softmax_tile<D>(p, seq_tab, ring, sbase, tmem, bars, &omap, warp >> 2, ok);
   } else {
     if (lane == 0) {
       if (warp == kKWarp)
-        produce_kv<D>(p, seq_tab, &kmap, smem, bars, Lay::kK, kKFull0, kKEmpty0, kKStages, ok);
+        produce_kv<D>(p, seq_tab, ring, &kmap, smem, bars, Lay::kK, kKFull0, kKEmpty0, kKStages, ok);
       else if (warp == kVWarp)
-        produce_kv<D>(p, seq_tab, &vmap, smem, bars, Lay::kV, kVFull0, kVEmpty0, kVStages, ok);
+        produce_kv<D>(p, seq_tab, ring, &vmap, smem, bars, Lay::kV, kVFull0, kVEmpty0, kVStages, ok);
       else if (warp == kQWarp)
-        produce_q<D>(p, seq_tab, &qmap, smem, bars, ok);
+        produce_q<D>(p, seq_tab, ring, &qmap, smem, bars, ok);
       else
-        issue_mma<D>(p, seq_tab, sbase, tmem, bars, ok);
+        issue_mma<D>(p, seq_tab, ring, sbase, tmem, bars, ok);
     }
   }
   if (!ok) set_status(p.status, ATTN_STATUS_TIMEOUT);
@@ -639,6 +677,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after();
   if (warp == kMmaWarp) tc::dealloc(tmem, kTmemCols);
+  // The last CTA to finish leaves the counters at zero for the next launch
+  // (every CTA has stopped claiming by now).
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.work + 1, 1) == (int)gridDim.x - 1) {
+      atomicExch(p.work, 0);
+      atomicExch(p.work + 1, 0);
+    }
+  }
 }
 
 template <int D>
@@ -661,6 +708,7 @@ int launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream) {
   p.slot_capacity = a.kv.slot_capacity;
   p.num_slots = a.kv.num_slots;
   p.status = a.status;
+  p.work = a.work;
   p.out = static_cast<uint16_t*>(a.out);
   p.scale_log2 = 1.4426950408889634f / sqrtf((float)D);
   p.Hq = Hq;
@@ -670,7 +718,8 @@ int launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream) {
   p.N = a.N;
   p.B = a.B;
   p.max_seqlen = a.max_seqlen;
-  const int64_t nv = ((int64_t)(a.N >> (p.log2BT + 1)) + a.B) * Hkv;
+  const int64_t rounds = ((int64_t)a.max_seqlen + (2 * BT) - 1) / (2 * BT);
+  const int64_t nv = rounds * a.B * Hkv;
   if (nv > (int64_t(1) << 30)) return ATTN_EINVAL;
   p.num_vitems = (int)nv;
   int dev = 0, sms = 0;

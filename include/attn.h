@@ -108,14 +108,17 @@ enum {
 /* Workspace bytes needed by any call with at most `max_tokens` new tokens,
  * `max_batch` requests and `max_kv_len` keys per request (c_b + n_b).  The
  * workspace is a caller-owned device buffer, 256-byte aligned: a 256-byte
- * header holding the status word, then the prepared Q of attn_prefill
- * (N * Hq * D bf16) or the split-KV partial results of attn_decode.  Returns
- * 0 for invalid arguments. */
+ * header holding the status word and the prefill work-item counters (the
+ * prefill attention kernel hands its work items out through them and leaves
+ * them at zero), then the prepared Q of attn_prefill (N * Hq * D bf16) or the
+ * split-KV partial results of attn_decode.  Calls that share a workspace must
+ * be ordered on one stream.  Returns 0 for invalid arguments. */
 ATTN_API size_t attn_workspace_size(const attn_config_t* cfg, int32_t max_tokens, int32_t max_batch,
                            int32_t max_kv_len);
 
-/* Zero the workspace's status word (asynchronous).  Call once after
- * allocating a workspace; attn_get_status clears it again. */
+/* Zero the workspace header: the status word and the work-item counters
+ * (asynchronous).  Call once after allocating a workspace; attn_get_status
+ * clears the status word again. */
 ATTN_API int attn_workspace_init(void* workspace, size_t ws_bytes, void* stream);
 
 /* KV append only: split, K RMSNorm + RoPE, write K and V of the N new tokens
