@@ -124,6 +124,21 @@ def test_prefill_output_only_16_byte_aligned():
     assert torch.equal(ref.view(torch.int16), out.view(torch.int16))
 
 
+def test_prefill_leaves_work_counters_zero():
+    """The prefill attention kernel hands out work items through two counters
+    in the workspace header (bytes 64..71) and must leave them at zero, so the
+    next call on the same workspace starts from item 0."""
+    w = gen.custom("counters", 16, 4, 128, [300, 77, 513], [0, 40, 0], seed=8)
+    from causal_gqa_attention_qkv_gb300 import step
+    ds = step.upload(w, gen.make_inputs(w))
+    for _ in range(3):
+        ds.run()
+        torch.cuda.synchronize()
+        header = ds.workspace[:256].view(torch.int32).cpu()
+        assert int(header[16]) == 0 and int(header[17]) == 0, header[16:18].tolist()
+    assert ds.status() == 0
+
+
 def test_status_capacity_and_seqlens():
     from causal_gqa_attention_qkv_gb300 import attn, step
     w = gen.custom("cap", 8, 2, 64, [10, 6], [0, 4], seed=8)
