@@ -31,7 +31,9 @@ class AttnConfig(ctypes.Structure):
 class AttnKV(ctypes.Structure):
     _fields_ = [("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
                 ("num_slots", ctypes.c_int64), ("slot_base", ctypes.c_void_p),
-                ("cache_lens", ctypes.c_void_p), ("slot_capacity", ctypes.c_void_p)]
+                ("cache_lens", ctypes.c_void_p), ("slot_capacity", ctypes.c_void_p),
+                ("page_table", ctypes.c_void_p), ("page_size", ctypes.c_int32),
+                ("pages_per_req", ctypes.c_int32)]
 
 
 class AttnError(RuntimeError):
@@ -103,9 +105,11 @@ class KVCache:
 
     k_cache: torch.Tensor       # bf16 [num_slots, Hkv, D]
     v_cache: torch.Tensor       # bf16 [num_slots, Hkv, D]
-    slot_base: torch.Tensor     # int64 [B]
+    slot_base: torch.Tensor     # int64 [B] (contiguous layout)
     cache_lens: torch.Tensor    # int32 [B]
     slot_capacity: torch.Tensor  # int32 [B]
+    page_table: torch.Tensor | None = None  # int32 [B, pages_per_req] (paged layout)
+    page_size: int = 0
 
     def struct(self) -> AttnKV:
         for name in ("k_cache", "v_cache"):
@@ -114,9 +118,14 @@ class KVCache:
         assert self.slot_base.dtype == torch.int64 and self.slot_base.is_contiguous()
         assert self.cache_lens.dtype == torch.int32 and self.cache_lens.is_contiguous()
         assert self.slot_capacity.dtype == torch.int32 and self.slot_capacity.is_contiguous()
+        pt, ps, ppr = None, 0, 0
+        if self.page_table is not None:
+            assert self.page_table.dtype == torch.int32 and self.page_table.is_contiguous()
+            assert self.page_table.dim() == 2
+            pt, ps, ppr = self.page_table.data_ptr(), int(self.page_size), int(self.page_table.shape[1])
         return AttnKV(self.k_cache.data_ptr(), self.v_cache.data_ptr(), self.k_cache.shape[0],
                       self.slot_base.data_ptr(), self.cache_lens.data_ptr(),
-                      self.slot_capacity.data_ptr())
+                      self.slot_capacity.data_ptr(), pt, ps, ppr)
 
 
 def decode_max_splits(B: int, num_kv_heads: int, max_kv_len: int) -> int:

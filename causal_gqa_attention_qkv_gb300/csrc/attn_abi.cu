@@ -53,9 +53,15 @@ int check_config(const attn_config_t* cfg) {
 }
 
 int check_kv(const attn_kv_t* kv) {
-  if (!kv || !kv->k_cache || !kv->v_cache || !kv->slot_base || !kv->cache_lens ||
-      !kv->slot_capacity)
+  if (!kv || !kv->k_cache || !kv->v_cache || !kv->cache_lens || !kv->slot_capacity)
     return ATTN_EINVAL;
+  if (kv->page_table) {
+    const int ps = kv->page_size;
+    if (ps < 64 || ps > (1 << 20) || (ps & (ps - 1)) != 0 || kv->pages_per_req <= 0)
+      return ATTN_EINVAL;
+  } else if (!kv->slot_base) {
+    return ATTN_EINVAL;
+  }
   if (kv->num_slots <= 0 || kv->num_slots >= (int64_t(1) << 31)) return ATTN_EINVAL;
   if ((reinterpret_cast<uintptr_t>(kv->k_cache) | reinterpret_cast<uintptr_t>(kv->v_cache)) & 15)
     return ATTN_EINVAL;

@@ -271,25 +271,51 @@ __device__ __forceinline__ void q_row_frags(const uint16_t* row, bool valid, con
 }
 
 // ---------------------------------------------------------------- requests
-// Per-request facts every kernel derives the same way from the arguments.
-struct ReqInfo {
-  int64_t slot0;   // slot of position 0 of the request
-  int32_t cached;  // c_b
-  int32_t n_new;   // n_b
-  bool valid;      // region can hold c_b + n_b entries and cu_seqlens is sane
+// How kernels find cache entries (the attn_kv_t indexing fields).
+struct KvIndex {
+  const int64_t* slot_base;      // contiguous layout
+  const int32_t* cache_lens;
+  const int32_t* slot_capacity;
+  const int32_t* page_table;     // nullptr: contiguous layout
+  int64_t num_slots;
+  int32_t log2_page;             // log2(page_size) (paged layout)
+  int32_t pages_per_req;
 };
 
-__device__ __forceinline__ ReqInfo load_request(const int64_t* slot_base, const int32_t* cache_lens,
-                                                const int32_t* slot_capacity, int64_t num_slots,
-                                                int32_t n_new) {
+// Per-request facts every kernel derives the same way from the arguments.
+struct ReqInfo {
+  int64_t slot0;         // contiguous layout: slot of position 0
+  const int32_t* pages;  // paged layout: the request's page-table row, else nullptr
+  int32_t cached;        // c_b
+  int32_t n_new;         // n_b
+  bool valid;            // the request can hold c_b + n_b entries and cu_seqlens is sane
+};
+
+__device__ __forceinline__ ReqInfo load_request(const KvIndex& kv, int b, int32_t n_new) {
   ReqInfo r;
-  r.slot0 = slot_base[0];
-  r.cached = cache_lens[0];
+  r.cached = kv.cache_lens[b];
   r.n_new = n_new;
-  int64_t end = (int64_t)r.cached + (int64_t)n_new;
-  r.valid = n_new >= 0 && r.cached >= 0 && r.slot0 >= 0 && end <= (int64_t)slot_capacity[0] &&
-            r.slot0 + end <= num_slots && end <= (1 << 24);
+  const int64_t end = (int64_t)r.cached + (int64_t)n_new;
+  const bool sizes = n_new >= 0 && r.cached >= 0 && end <= (int64_t)kv.slot_capacity[b] && end <= (1 << 24);
+  if (kv.page_table) {
+    r.pages = kv.page_table + (int64_t)b * kv.pages_per_req;
+    r.slot0 = 0;
+    r.valid = sizes && end <= ((int64_t)kv.pages_per_req << kv.log2_page);
+  } else {
+    r.pages = nullptr;
+    r.slot0 = kv.slot_base[b];
+    r.valid = sizes && r.slot0 >= 0 && r.slot0 + end <= kv.num_slots;
+  }
   return r;
+}
+
+// Slot of the entry at position pos of a request, or -1 when its page number
+// is outside the cache (paged layout; pos < pages_per_req * page_size).
+__device__ __forceinline__ int64_t cache_slot(const KvIndex& kv, const ReqInfo& r, int pos) {
+  if (!r.pages) return r.slot0 + pos;
+  const int64_t pg = __ldg(r.pages + (pos >> kv.log2_page));
+  const int64_t slot = (pg << kv.log2_page) + (pos & ((1 << kv.log2_page) - 1));
+  return (pg >= 0 && slot < kv.num_slots) ? slot : -1;
 }
 
 }  // namespace gb300

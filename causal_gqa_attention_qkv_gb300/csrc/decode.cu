@@ -30,10 +30,7 @@ struct DecodePar {
   uint16_t* out;
   float* part_o;
   float* part_ml;
-  const int64_t* slot_base;
-  const int32_t* cache_lens;
-  const int32_t* slot_capacity;
-  int64_t num_slots;
+  KvIndex kv;
   int32_t* status;
   int32_t Hq, G, split_len, max_splits;
   float scale_log2;  // log2(e) / sqrt(D)
@@ -66,8 +63,7 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ int s_cons_abort;  // written by consumers only, read after their barrier
 
   const int split = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
-  const ReqInfo r = load_request(p.slot_base + b, p.cache_lens + b, p.slot_capacity + b,
-                                 p.num_slots, 1);
+  const ReqInfo r = load_request(p.kv, b, 1);
   if (!r.valid) return;  // flagged by the prologue
   const int kv_len = r.cached + 1;
   const int n_splits = (kv_len + p.split_len - 1) / p.split_len;
@@ -106,11 +102,16 @@ __global__ void __launch_bounds__(kThreads)
         mbar_arrive_expect_tx(&full[st], Lay::kStageBytes);
         uint8_t* kt = smem + st * Lay::kStageBytes;
         uint8_t* vt = kt + Lay::kTileBytes;
-        const int slot = (int)(r.slot0 + k0 + i * kKeysPerTile);
+        // a 64-key tile lies in one page; a page outside the cache reads as zeros
+        int64_t slot = cache_slot(p.kv, r, k0 + i * kKeysPerTile);
+        if (slot < 0) {
+          set_status(p.status, ATTN_STATUS_CAPACITY);
+          slot = 0;
+        }
 #pragma unroll
         for (int rg = 0; rg < Lay::kRegions; ++rg) {
-          tma_load_3d(kt + rg * Lay::kRegionBytes, &kmap, &full[st], rg * 64, kh, slot);
-          tma_load_3d(vt + rg * Lay::kRegionBytes, &vmap, &full[st], rg * 64, kh, slot);
+          tma_load_3d(kt + rg * Lay::kRegionBytes, &kmap, &full[st], rg * 64, kh, (int)slot);
+          tma_load_3d(vt + rg * Lay::kRegionBytes, &vmap, &full[st], rg * 64, kh, (int)slot);
         }
         issued = i + 1;
       }
@@ -263,8 +264,7 @@ __global__ void __launch_bounds__(kThreads)
 template <int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodePar p) {
   const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
-  const ReqInfo r = load_request(p.slot_base + b, p.cache_lens + b, p.slot_capacity + b,
-                                 p.num_slots, 1);
+  const ReqInfo r = load_request(p.kv, b, 1);
   if (!r.valid) return;
   const int n = (r.cached + 1 + p.split_len - 1) / p.split_len;
   if (n <= 1 || n > p.max_splits) return;  // written directly / flagged by the split kernel
@@ -296,10 +296,7 @@ int launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
   p.out = static_cast<uint16_t*>(a.out);
   p.part_o = a.part_o;
   p.part_ml = a.part_ml;
-  p.slot_base = a.kv.slot_base;
-  p.cache_lens = a.kv.cache_lens;
-  p.slot_capacity = a.kv.slot_capacity;
-  p.num_slots = a.kv.num_slots;
+  p.kv = kv_index(a.kv);
   p.status = a.status;
   p.Hq = a.cfg.num_q_heads;
   p.G = a.cfg.num_q_heads / a.cfg.num_kv_heads;

@@ -7,6 +7,21 @@ namespace gb300 {
 
 void make_rope_freqs(float theta, int head_dim, RopeFreqs* out);
 
+// The indexing fields of a (checked) attn_kv_t, as the kernels use them.
+inline KvIndex kv_index(const attn_kv_t& kv) {
+  KvIndex x;
+  x.slot_base = kv.slot_base;
+  x.cache_lens = kv.cache_lens;
+  x.slot_capacity = kv.slot_capacity;
+  x.page_table = kv.page_table;
+  x.num_slots = kv.num_slots;
+  x.log2_page = 0;
+  if (kv.page_table)
+    while ((1 << x.log2_page) < kv.page_size) ++x.log2_page;
+  x.pages_per_req = kv.pages_per_req;
+  return x;
+}
+
 // Host-side argument checks of the C ABI (ATTN_OK or an ATTN_E* code).
 int abi_check_config(const attn_config_t* cfg);
 int abi_check_kv(const attn_kv_t* kv);

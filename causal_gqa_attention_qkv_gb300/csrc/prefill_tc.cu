@@ -65,10 +65,8 @@ constexpr float kRescaleThreshold = 8.f;  // log2 units: move the reference max 
 
 struct TcPar {
   const int32_t* cu_seqlens;
-  const int64_t* slot_base;
-  const int32_t* cache_lens;
-  const int32_t* slot_capacity;
-  int64_t num_slots;
+  KvIndex kv;
+  int32_t half_boxes;  // paged cache with 64-slot pages: a K/V tile is two 64-row boxes
   int32_t* status;
   int32_t* work;  // [0]: next item to claim, [1]: CTAs finished
   uint16_t* out;
@@ -133,8 +131,7 @@ __device__ __forceinline__ SeqInfo seq_info(const TcPar& p, int b) {
   SeqInfo q;
   q.tokbase = p.cu_seqlens[b];
   q.n_b = p.cu_seqlens[b + 1] - q.tokbase;
-  const ReqInfo r = load_request(p.slot_base + b, p.cache_lens + b, p.slot_capacity + b,
-                                 p.num_slots, q.n_b);
+  const ReqInfo r = load_request(p.kv, b, q.n_b);
   q.slot0 = r.slot0;
   q.cached = r.cached;
   // sequences with no tokens, outside [0, N), longer than the host bound or
@@ -255,6 +252,23 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
 // ---------------------------------------------------------------- roles
 // One TMA producer ring (K or V tiles): tile g of the CTA's tile sequence goes
 // to stage g % stages once the stage's previous tile has been consumed.
+// First cache row of the rows [pos, pos + rows) of item it's sequence (rows
+// within one page in the paged layout).  A page outside the cache sets
+// ATTN_STATUS_CAPACITY and is read from row 0 instead (its keys are wrong,
+// nothing is out of bounds).
+__device__ __forceinline__ int kv_row(const TcPar& p, const Item& it, int pos) {
+  if (!p.kv.page_table) return (int)(it.slot0 + pos);
+  ReqInfo r;
+  r.slot0 = 0;
+  r.pages = p.kv.page_table + (int64_t)it.b * p.kv.pages_per_req;
+  const int64_t s = cache_slot(p.kv, r, pos);
+  if (s < 0) {
+    set_status(p.status, ATTN_STATUS_CAPACITY);
+    return 0;
+  }
+  return (int)s;
+}
+
 template <int D>
 __device__ void produce_kv(const TcPar& p, const SeqInfo* seq_tab, const int* ring,
                            const CUtensorMap* map, uint8_t* smem, uint64_t* bars, int base,
@@ -269,10 +283,23 @@ __device__ void produce_kv(const TcPar& p, const SeqInfo* seq_tab, const int* ri
       const int st = g % stages;
       if (g >= stages && !mbar_wait(&bars[empty0 + st], (g / stages - 1) & 1)) { ok = false; break; }
       mbar_arrive_expect_tx(&bars[full0 + st], Lay::kTile);
+      uint8_t* dst = smem + base + st * Lay::kTile;
+      if (!p.half_boxes) {
+        const int row = kv_row(p, w.it, j * kKeys);
 #pragma unroll
-      for (int rg = 0; rg < Lay::kRegions; ++rg)
-        tma_load_3d(smem + base + st * Lay::kTile + rg * kRegionBytes, map, &bars[full0 + st],
-                    rg * 64, w.it.kh, (int)(w.it.slot0 + j * kKeys));
+        for (int rg = 0; rg < Lay::kRegions; ++rg)
+          tma_load_3d(dst + rg * kRegionBytes, map, &bars[full0 + st], rg * 64, w.it.kh, row);
+      } else {
+        // two 64-key pages; a second half past the sequence end re-reads the
+        // last page (those keys are masked and their V rows zeroed)
+        const int pos1 = min(j * kKeys + 64, ((w.it.kv_total - 1) >> 6) << 6);
+        const int row0 = kv_row(p, w.it, j * kKeys), row1 = kv_row(p, w.it, pos1);
+#pragma unroll
+        for (int rg = 0; rg < Lay::kRegions; ++rg) {
+          tma_load_3d(dst + rg * kRegionBytes, map, &bars[full0 + st], rg * 64, w.it.kh, row0);
+          tma_load_3d(dst + rg * kRegionBytes + 64 * 128, map, &bars[full0 + st], rg * 64, w.it.kh, row1);
+        }
+      }
     }
     if (!ok) break;
     w.next(p, ok);
@@ -695,18 +722,18 @@ int launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream) {
   const int G = Hq / Hkv;
   const int log2G = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
   const int BT = kTileRows / G;
+  const KvIndex kvi = kv_index(a.kv);
+  const bool half_boxes = kvi.page_table != nullptr && kvi.log2_page < 7;
   CacheMaps maps;
-  if (make_cache_maps(a.kv, Hkv, D, kKeys, &maps) != 0) return ATTN_ELAUNCH;
+  if (make_cache_maps(a.kv, Hkv, D, half_boxes ? 64 : kKeys, &maps) != 0) return ATTN_ELAUNCH;
   CUtensorMap qmap;  // prepared Q viewed as [N, Hq, D]
   if (make_qkv_map(a.q, a.N, Hq, D, G, BT, &qmap) != 0) return ATTN_ELAUNCH;
   CUtensorMap omap;  // out viewed as [N, Hq, D]; one softmax warp's 32 rows per box
   if (make_qkv_map(a.out, a.N, Hq, D, G, 32 / G, &omap) != 0) return ATTN_ELAUNCH;
   TcPar p;
   p.cu_seqlens = a.cu_seqlens;
-  p.slot_base = a.kv.slot_base;
-  p.cache_lens = a.kv.cache_lens;
-  p.slot_capacity = a.kv.slot_capacity;
-  p.num_slots = a.kv.num_slots;
+  p.kv = kvi;
+  p.half_boxes = half_boxes ? 1 : 0;
   p.status = a.status;
   p.work = a.work;
   p.out = static_cast<uint16_t*>(a.out);

@@ -16,7 +16,14 @@ namespace {
 
 constexpr int kWarpsPerBlock = 8;  // one token per warp
 constexpr int kThreads = kWarpsPerBlock * 32;
-constexpr int kBatch = 12;         // head-vector loads issued per lane before processing
+#ifndef PROLOGUE_BATCH
+#define PROLOGUE_BATCH 12
+#endif
+#ifndef PROLOGUE_MIN_BLOCKS
+#define PROLOGUE_MIN_BLOCKS 2
+#endif
+constexpr int kBatch = PROLOGUE_BATCH;  // head-vector loads issued per lane before processing
+constexpr int kMinBlocks = PROLOGUE_MIN_BLOCKS;  // resident blocks per SM the registers allow
 
 struct ProloguePar {
   const uint16_t* __restrict__ qkv;        // [N, W] bf16
@@ -26,10 +33,7 @@ struct ProloguePar {
   const int32_t* cu_seqlens;  // [B+1] or NULL: token b is request b (decode)
   uint16_t* __restrict__ k_cache;
   uint16_t* __restrict__ v_cache;
-  const int64_t* slot_base;
-  const int32_t* cache_lens;
-  const int32_t* slot_capacity;
-  int64_t num_slots;
+  KvIndex kv;
   int32_t* status;
   int32_t B, N, Hq, Hkv;
   float eps;
@@ -43,7 +47,7 @@ struct ProloguePar {
 // token's D/2 rotation angles are computed once (D/64 per lane) and handed to
 // the lanes that need them with shuffles.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2) kv_append_kernel(const ProloguePar p) {
+__global__ void __launch_bounds__(kThreads, kMinBlocks) kv_append_kernel(const ProloguePar p) {
   constexpr int L = D / 8;      // lanes per head vector
   constexpr int HPI = 32 / L;   // head vectors per warp-wide step
   constexpr int PPL = D / 64;   // rotation pairs computed per lane
@@ -91,16 +95,14 @@ __global__ void __launch_bounds__(kThreads, 2) kv_append_kernel(const ProloguePa
       if (t == 0 && lane == 0 && __ldg(p.cu_seqlens + p.B) != p.N) set_status(p.status, ATTN_STATUS_SEQLENS);
     }
     if (seq_ok) {
-      const ReqInfo r = load_request(p.slot_base + b, p.cache_lens + b, p.slot_capacity + b,
-                                     p.num_slots, n);
+      const ReqInfo r = load_request(p.kv, b, n);
       ok = 1;
       pos = (float)(r.cached + j);
-      if (r.valid) {
+      slot = r.valid ? cache_slot(p.kv, r, r.cached + j) : -1;
+      if (slot >= 0)
         ok = 2;
-        slot = r.slot0 + r.cached + j;
-      } else if (lane == 0) {
+      else if (lane == 0)
         set_status(p.status, ATTN_STATUS_CAPACITY);
-      }
     }
   }
   if (ok == 0) return;  // warp-uniform
@@ -213,10 +215,7 @@ cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t stream) {
   p.cu_seqlens = a.cu_seqlens;
   p.k_cache = static_cast<uint16_t*>(a.kv.k_cache);
   p.v_cache = static_cast<uint16_t*>(a.kv.v_cache);
-  p.slot_base = a.kv.slot_base;
-  p.cache_lens = a.kv.cache_lens;
-  p.slot_capacity = a.kv.slot_capacity;
-  p.num_slots = a.kv.num_slots;
+  p.kv = kv_index(a.kv);
   p.status = a.status;
   p.B = a.B;
   p.N = a.N;

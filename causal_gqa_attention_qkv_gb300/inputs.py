@@ -154,12 +154,18 @@ def _fill_bits(t: torch.Tensor, bits: int) -> None:
 
 
 def make_inputs(w: Workload, extra_capacity: Sequence[int] | None = None,
-                unused_fill: str = "nan") -> dict:
+                unused_fill: str = "nan", page_size: int = 0) -> dict:
     """Draw all inputs of one call of workload ``w`` (host tensors).
 
     ``extra_capacity[b]`` is the number of free slots left after request b's
     new tokens (default: one, so that one decode step can follow).
     ``unused_fill`` is ``"nan"`` (quiet-NaN bits) or ``"sentinel"``.
+    ``page_size`` > 0 lays the cache out in pages of that many slots: request b
+    gets ceil(capacity_b / page_size) pages drawn from a seeded random
+    permutation of the pool (plus three pages no request owns), listed in
+    ``page_table`` (int32 [B, max pages]; unused entries -1).  The logical
+    contents (qkv, weights, prior cache entries by position) are the same as
+    with the contiguous layout for the same workload.
     """
     g = _gen(1000 + w.seed)
     B, H, Hkv, D = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
@@ -175,6 +181,18 @@ def make_inputs(w: Workload, extra_capacity: Sequence[int] | None = None,
         base.append(s)
         s += cap[b] + GUARD_SLOTS
     num_slots = s
+    page_table = None
+    if page_size:
+        npg = [(c + page_size - 1) // page_size for c in cap]
+        total = sum(npg) + 3
+        perm = torch.randperm(total, generator=_gen(5000 + w.seed)).tolist()
+        page_table = torch.full((B, max(npg + [1])), -1, dtype=torch.int32)
+        k = 0
+        for b in range(B):
+            page_table[b, :npg[b]] = torch.tensor(perm[k:k + npg[b]], dtype=torch.int32)
+            k += npg[b]
+        num_slots = total * page_size
+        base = [0] * B
     k_cache = torch.empty((num_slots, Hkv, D), dtype=torch.bfloat16)
     v_cache = torch.empty((num_slots, Hkv, D), dtype=torch.bfloat16)
     bits = BF16_QNAN_BITS if unused_fill == "nan" else BF16_SENTINEL_BITS
@@ -183,8 +201,15 @@ def make_inputs(w: Workload, extra_capacity: Sequence[int] | None = None,
     for b in range(B):
         c = w.cache_lens[b]
         if c:
-            k_cache[base[b]:base[b] + c] = _bf16_normal(g, (c, Hkv, D))
-            v_cache[base[b]:base[b] + c] = _bf16_normal(g, (c, Hkv, D))
+            kp, vp = _bf16_normal(g, (c, Hkv, D)), _bf16_normal(g, (c, Hkv, D))
+            if page_table is None:
+                k_cache[base[b]:base[b] + c] = kp
+                v_cache[base[b]:base[b] + c] = vp
+            else:
+                pos = torch.arange(c)
+                slots = page_table[b, pos // page_size].long() * page_size + pos % page_size
+                k_cache[slots] = kp
+                v_cache[slots] = vp
     cu = [0]
     for n in w.new_lens:
         cu.append(cu[-1] + n)
@@ -199,6 +224,8 @@ def make_inputs(w: Workload, extra_capacity: Sequence[int] | None = None,
         "k_cache": k_cache,
         "v_cache": v_cache,
         "num_slots": num_slots,
+        "page_table": page_table,
+        "page_size": page_size,
     }
 
 

@@ -74,16 +74,31 @@ typedef struct attn_config {
 
 /* The KV cache of one layer (host struct holding device pointers).
  * k_cache, v_cache: bf16 [num_slots, Hkv, D], contiguous, row = one slot.
- * Request b owns slots [slot_base[b], slot_base[b] + slot_capacity[b]).
- * cache_lens[b] is read, never written: the caller advances it after the
- * call (the transformer-basics "Prefill vs Decode" cache goes 0 -> 12 -> 13). */
+ * The entry at position p of request b lives in one slot:
+ *   contiguous (page_table == NULL): slot slot_base[b] + p; request b owns
+ *     slots [slot_base[b], slot_base[b] + slot_capacity[b]);
+ *   paged (page_table != NULL): slot page_table[b * pages_per_req + p / page_size]
+ *     * page_size + p % page_size, i.e. the cache is num_slots / page_size
+ *     pages of page_size slots and page_table row b lists request b's pages in
+ *     position order; slot_base is unused (may be NULL).  page_size is a power
+ *     of two >= 64 (every 64-key tile of a request lies in one page).  A page
+ *     number outside [0, num_slots / page_size) sets ATTN_STATUS_CAPACITY: the
+ *     entry is not written and reads of it return zeros.
+ * In both layouts c_b + n_b <= slot_capacity[b] (paged: also
+ * <= pages_per_req * page_size), else the request is skipped
+ * (ATTN_STATUS_CAPACITY).  cache_lens[b] is read, never written: the caller
+ * advances it after the call (the transformer-basics "Prefill vs Decode"
+ * cache goes 0 -> 12 -> 13). */
 typedef struct attn_kv {
   void* k_cache;
   void* v_cache;
   int64_t num_slots;
-  const int64_t* slot_base;     /* [B] */
+  const int64_t* slot_base;     /* [B] (contiguous layout) */
   const int32_t* cache_lens;    /* [B] */
   const int32_t* slot_capacity; /* [B] */
+  const int32_t* page_table;    /* NULL, or [B, pages_per_req] page numbers (paged layout) */
+  int32_t page_size;            /* slots per page (paged layout) */
+  int32_t pages_per_req;        /* row length of page_table (paged layout) */
 } attn_kv_t;
 
 enum {

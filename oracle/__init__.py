@@ -59,11 +59,12 @@ def _load():
         lib.oracle_prologue.restype = ctypes.c_int
         lib.oracle_prologue.argtypes = [
             ctypes.c_int, ctypes.c_int, ctypes.c_int, _D, _D,
-            _P, _I64, _P, _P, ctypes.c_int, _P, _P, _P, _P, _I64, _P, _P, _I64, _P, _P, _P]
+            _P, _I64, _P, _P, ctypes.c_int, _P, _P, _P, _P, _P, ctypes.c_int, ctypes.c_int,
+            _I64, _P, _P, _I64, _P, _P, _P]
         lib.oracle_attention.restype = None
         lib.oracle_attention.argtypes = [
             ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P, _P,
-            _I64, _P, _P, _P, _P]
+            _P, ctypes.c_int, ctypes.c_int, _I64, _P, _P, _P, _P]
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -112,6 +113,16 @@ def rope(x, pos: float, theta: float) -> np.ndarray:
     return y
 
 
+def _pages(inputs: dict):
+    """(page table int32 [B, P] flattened, page size, P) of a paged cache, or a
+    dummy table and page size 0 for the contiguous layout."""
+    pt = inputs.get("page_table")
+    if pt is None:
+        return np.zeros(1, dtype=np.int32), 0, 0
+    pt = np.ascontiguousarray(pt.numpy().astype(np.int32))
+    return pt.reshape(-1), int(inputs["page_size"]), int(pt.shape[1])
+
+
 def prologue(cfg: dict, inputs: dict, q_rows=None):
     """Steps 1-4.  Returns (k_cache, v_cache, q, bad) where the caches are new
     bf16 tensors (the inputs are not modified), q is fp64 ``[N, Hq, D]`` (or
@@ -129,6 +140,7 @@ def prologue(cfg: dict, inputs: dict, q_rows=None):
     cl = np.ascontiguousarray(inputs["cache_lens"].numpy().astype(np.int32))
     sb = np.ascontiguousarray(inputs["slot_base"].numpy().astype(np.int64))
     cap = np.ascontiguousarray(inputs["slot_capacity"].numpy().astype(np.int32))
+    pt, ps, ppr = _pages(inputs)
     B = cl.shape[0]
     if q_rows is None:
         nq = -1
@@ -142,8 +154,8 @@ def prologue(cfg: dict, inputs: dict, q_rows=None):
         q = np.zeros((nq, D), dtype=np.float64)
     bad = lib.oracle_prologue(Hq, Hkv, D, float(cfg["rms_eps"]), float(cfg["rope_theta"]),
                               _ptr(qkv), N, _ptr(qw), _ptr(kw), B, _ptr(cu), _ptr(cl), _ptr(sb),
-                              _ptr(cap), kc.shape[0], _ptr(kc), _ptr(vc), nq, _ptr(qt), _ptr(qh),
-                              _ptr(q))
+                              _ptr(cap), _ptr(pt), ps, ppr, kc.shape[0], _ptr(kc), _ptr(vc), nq,
+                              _ptr(qt), _ptr(qh), _ptr(q))
     return bits_to_bf16(kc), bits_to_bf16(vc), q, bad
 
 
@@ -162,9 +174,10 @@ def attention(cfg: dict, k_cache: torch.Tensor, v_cache: torch.Tensor, inputs: d
     cu = np.ascontiguousarray(inputs["cu_seqlens"].numpy().astype(np.int32))
     cl = np.ascontiguousarray(inputs["cache_lens"].numpy().astype(np.int32))
     sb = np.ascontiguousarray(inputs["slot_base"].numpy().astype(np.int64))
+    pt, ps, ppr = _pages(inputs)
     out = np.zeros((R, D), dtype=np.float64)
     lib.oracle_attention(Hq, Hkv, D, _ptr(kc), _ptr(vc), cl.shape[0], _ptr(cu), _ptr(cl), _ptr(sb),
-                         R, _ptr(tok), _ptr(head), _ptr(q), _ptr(out))
+                         _ptr(pt), ps, ppr, R, _ptr(tok), _ptr(head), _ptr(q), _ptr(out))
     return out
 
 

@@ -100,14 +100,27 @@ static int find_request(const int32_t* cu, int B, int64_t t) {
   return lo;
 }
 
+/*
+ * Slot of the entry at position pos of request b.  page_size == 0: the
+ * request's contiguous region, slot_base[b] + pos.  Otherwise the paged
+ * layout: page page_table[b * pages_per_req + pos / page_size], entry
+ * pos % page_size of that page.
+ */
+static int64_t slot_of(const int64_t* slot_base, const int32_t* page_table, int page_size,
+                       int pages_per_req, int b, int64_t pos) {
+  if (page_size == 0) return slot_base[b] + pos;
+  return (int64_t)page_table[(int64_t)b * pages_per_req + pos / page_size] * page_size +
+         pos % page_size;
+}
+
 static void load_head(const uint16_t* row, int64_t col0, int D, double* out) {
   for (int i = 0; i < D; ++i) out[i] = bf16_bits_to_double(row[col0 + i]);
 }
 
 /*
  * Steps 1-4 for all N tokens.  The cache (k_cache, v_cache: bf16 bits
- * [num_slots, Hkv, D]) is updated in place: token j of request b goes to slot
- * slot_base[b] + cache_lens[b] + j.  Q rows (normed, rotated, fp64) are written
+ * [num_slots, Hkv, D]) is updated in place: token j of request b goes to the
+ * slot of position cache_lens[b] + j (slot_of).  Q rows (normed, rotated, fp64) are written
  * to q_out: all N*Hq rows as [N, Hq, D] when nq < 0, otherwise the nq rows
  * (q_tok[r], q_head[r]) as [nq, D].  Returns the number of requests whose
  * region cannot hold cache_lens + new tokens (those write nothing).
@@ -116,7 +129,8 @@ int oracle_prologue(int Hq, int Hkv, int D, double eps, double theta,
                     const uint16_t* qkv, int64_t N, const uint16_t* q_norm_w,
                     const uint16_t* k_norm_w, int B, const int32_t* cu_seqlens,
                     const int32_t* cache_lens, const int64_t* slot_base,
-                    const int32_t* slot_capacity, int64_t num_slots, uint16_t* k_cache,
+                    const int32_t* slot_capacity, const int32_t* page_table, int page_size,
+                    int pages_per_req, int64_t num_slots, uint16_t* k_cache,
                     uint16_t* v_cache, int64_t nq, const int32_t* q_tok,
                     const int32_t* q_head, double* q_out) {
   const int64_t W = (int64_t)(Hq + 2 * Hkv) * D;
@@ -128,7 +142,16 @@ int oracle_prologue(int Hq, int Hkv, int D, double eps, double theta,
   for (int b = 0; b < B; ++b) {
     int64_t n = cu_seqlens[b + 1] - cu_seqlens[b];
     int64_t end = (int64_t)cache_lens[b] + n;
-    if (n < 0 || end > slot_capacity[b] || slot_base[b] < 0 || slot_base[b] + end > num_slots) {
+    int fits = n >= 0 && end <= slot_capacity[b];
+    if (fits && page_size == 0) fits = slot_base[b] >= 0 && slot_base[b] + end <= num_slots;
+    if (fits && page_size != 0) {
+      fits = end <= (int64_t)pages_per_req * page_size;
+      for (int64_t pg = 0; fits && pg * page_size < end; ++pg) {
+        int64_t page = page_table[(int64_t)b * pages_per_req + pg];
+        fits = page >= 0 && (page + 1) * page_size <= num_slots;
+      }
+    }
+    if (!fits) {
       ++bad;
       continue;
     }
@@ -136,7 +159,7 @@ int oracle_prologue(int Hq, int Hkv, int D, double eps, double theta,
     for (int64_t j = 0; j < n; ++j) {
       int64_t t = cu_seqlens[b] + j;
       double pos = (double)cache_lens[b] + (double)j;
-      int64_t slot = slot_base[b] + cache_lens[b] + j;
+      int64_t slot = slot_of(slot_base, page_table, page_size, pages_per_req, b, cache_lens[b] + j);
       const uint16_t* row = qkv + t * W;
       double x[256], y[256];
       for (int kh = 0; kh < Hkv; ++kh) {
@@ -177,7 +200,8 @@ int oracle_prologue(int Hq, int Hkv, int D, double eps, double theta,
  */
 void oracle_attention(int Hq, int Hkv, int D, const uint16_t* k_cache, const uint16_t* v_cache,
                       int B, const int32_t* cu_seqlens, const int32_t* cache_lens,
-                      const int64_t* slot_base, int64_t nrows, const int32_t* tok,
+                      const int64_t* slot_base, const int32_t* page_table, int page_size,
+                      int pages_per_req, int64_t nrows, const int32_t* tok,
                       const int32_t* head, const double* q, double* out) {
   const int G = Hq / Hkv;
   const double scale = 1.0 / sqrt((double)D);
@@ -192,7 +216,8 @@ void oracle_attention(int Hq, int Hkv, int D, const uint16_t* k_cache, const uin
     double* s = malloc(sizeof(double) * (size_t)nkeys);
     const double* qr = q + r * D;
     for (int64_t u = 0; u < nkeys; ++u) {
-      const uint16_t* kr = k_cache + ((slot_base[b] + u) * Hkv + kvh) * D;
+      const uint16_t* kr =
+          k_cache + (slot_of(slot_base, page_table, page_size, pages_per_req, b, u) * Hkv + kvh) * D;
       double acc = 0.0;
       for (int i = 0; i < D; ++i) acc += qr[i] * bf16_bits_to_double(kr[i]);
       s[u] = acc * scale;
@@ -209,7 +234,8 @@ void oracle_attention(int Hq, int Hkv, int D, const uint16_t* k_cache, const uin
     for (int i = 0; i < D; ++i) o[i] = 0.0;
     for (int64_t u = 0; u < nkeys; ++u) {
       double p = s[u] / z;
-      const uint16_t* vr = v_cache + ((slot_base[b] + u) * Hkv + kvh) * D;
+      const uint16_t* vr =
+          v_cache + (slot_of(slot_base, page_table, page_size, pages_per_req, b, u) * Hkv + kvh) * D;
       for (int i = 0; i < D; ++i) o[i] += p * bf16_bits_to_double(vr[i]);
     }
     free(s);

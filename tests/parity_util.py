@@ -19,14 +19,18 @@ def ordered_bits(t: torch.Tensor) -> np.ndarray:
 
 
 def written_slots(host: dict, lo: int = 0, hi: int | None = None) -> np.ndarray:
+    """Slots of the new tokens of requests lo..hi-1 (contiguous or paged layout)."""
     cl = host["cache_lens"].numpy()
     cu = host["cu_seqlens"].numpy()
     sb = host["slot_base"].numpy()
+    pt = host.get("page_table")
+    ps = int(host.get("page_size", 0))
     hi = len(cl) if hi is None else hi
     out = []
     for b in range(lo, hi):
         n = cu[b + 1] - cu[b]
-        out.extend(range(sb[b] + cl[b], sb[b] + cl[b] + n))
+        for pos in range(cl[b], cl[b] + n):
+            out.append(sb[b] + pos if pt is None else int(pt[b, pos // ps]) * ps + pos % ps)
     return np.asarray(out, dtype=np.int64)
 
 

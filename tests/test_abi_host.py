@@ -109,3 +109,27 @@ def test_decode_split_mirror_matches_library(lib, B, max_kv):
     al = lambda x: (x + 255) // 256 * 256
     expect = 256 + al(B * 32 * ms * 128 * 4) + al(B * 32 * ms * 2 * 4)
     assert attn.workspace_size(cfg, 1, B, max_kv) == max(expect, 256 + al(32 * 128 * 2))
+
+
+@pytest.mark.parametrize("page_size,ppr", [(48, 4), (32, 4), (96, 4), (128, 0), (0, 4)])
+def test_bad_page_layout_rejected(lib, page_size, ppr):
+    """A paged cache needs a power-of-two page size >= 64 and a positive page-table
+    row length; the check comes before any pointer is used or anything launched."""
+    from causal_gqa_attention_qkv_gb300 import attn
+    cfg = attn.config(32, 8, 128)
+    fake = 1 << 20
+    kv = attn.AttnKV(fake, fake, 1024, None, fake, fake, fake, page_size, ppr)
+    f = ctypes.c_void_p(fake)
+    rc = lib.attn_kv_append(ctypes.byref(cfg), f, f, f, f, 1, 4, ctypes.byref(kv), f, 1 << 20, None)
+    assert rc == -1
+    rc = lib.attn_decode(ctypes.byref(cfg), f, f, f, 1, 4, ctypes.byref(kv), f, f, 1 << 20, None)
+    assert rc == -1
+
+
+def test_contiguous_layout_needs_slot_base(lib):
+    from causal_gqa_attention_qkv_gb300 import attn
+    cfg = attn.config(32, 8, 128)
+    fake = 1 << 20
+    kv = attn.AttnKV(fake, fake, 1024, None, fake, fake, None, 0, 0)
+    f = ctypes.c_void_p(fake)
+    assert lib.attn_kv_append(ctypes.byref(cfg), f, f, f, f, 1, 4, ctypes.byref(kv), f, 1 << 20, None) == -1

@@ -72,6 +72,32 @@ def test_decode_all_rows(hq, hkv, d, cache):
     run_and_compare(w, gen.make_inputs(w))
 
 
+# Paged KV cache: the cache is pages of page_size slots listed per request in a
+# page table (a seeded random permutation of the pool).  The same logical
+# inputs must give the oracle's result and the same bits as the contiguous
+# layout (the kernels' arithmetic does not depend on where an entry lives).
+PAGED = [
+    # (page size, Hq, Hkv, D, new lens, cached lens, decode_from)
+    (64, 32, 8, 128, [300, 77, 513, 129], [0, 200, 64, 1000], 4),
+    (128, 32, 8, 128, [300, 77, 513, 129], [0, 200, 64, 1000], 4),
+    (256, 16, 2, 64, [130, 1, 65], [3, 0, 700], 3),
+    (64, 32, 8, 128, [1] * 8, [0, 1, 63, 64, 65, 700, 3000, 5000], 0),
+    (128, 8, 8, 64, [1] * 4, [12, 127, 128, 2047], 0),
+    (64, 32, 8, 128, [100, 64, 1, 1, 1], [50, 0, 10, 700, 0], 2),
+]
+
+
+@pytest.mark.parametrize("ps,hq,hkv,d,lens,cache,df", PAGED)
+def test_paged_cache_all_rows_and_same_bits_as_contiguous(ps, hq, hkv, d, lens, cache, df):
+    w = gen.custom(f"paged_{ps}_{hq}_{d}_{df}", hq, hkv, d, lens, cache, seed=ps + sum(lens), decode_from=df)
+    paged = run_and_compare(w, gen.make_inputs(w, page_size=ps))["ds"]
+    from causal_gqa_attention_qkv_gb300 import step
+    contiguous = step.upload(w, gen.make_inputs(w))
+    contiguous.run()
+    torch.cuda.synchronize()
+    assert torch.equal(paged.out.view(torch.int16), contiguous.out.view(torch.int16))
+
+
 def test_mixed_prefill_and_decode_small():
     w = gen.custom("mixed_small", 32, 8, 128, [100, 64, 1, 1, 1], [50, 0, 10, 700, 0], seed=77,
                    decode_from=2)

@@ -318,3 +318,31 @@ def test_region_too_small_writes_nothing():
     assert torch.equal(kc[b1 + 2:b1 + 6].view(torch.int16), inp["k_cache"][b1 + 2:b1 + 6].view(torch.int16))
     b0 = int(inp["slot_base"][0])
     assert not torch.equal(kc[b0:b0 + 4].view(torch.int16), inp["k_cache"][b0:b0 + 4].view(torch.int16))
+
+
+@pytest.mark.parametrize("page_size", [64, 128])
+def test_paged_cache_gives_the_contiguous_result(page_size):
+    """The paged layout only moves where an entry lives: for the same logical
+    inputs the outputs are bit-identical to the contiguous layout, each
+    position's K/V lands in slot page_table[b, p // page_size] * page_size +
+    p % page_size, and no other slot changes."""
+    w = gen.custom("paged_pin", 4, 2, 64, [50, 130, 1, 7], [100, 0, 70, 129], seed=21)
+    cfg = oracle.cfg_of(w)
+    hc = gen.make_inputs(w)
+    hp = gen.make_inputs(w, page_size=page_size)
+    rc, rp = oracle.step(cfg, hc), oracle.step(cfg, hp)
+    assert rc["bad"] == 0 and rp["bad"] == 0
+    assert np.array_equal(rc["out"], rp["out"])
+    kc, vc = rc["k_cache"].view(torch.int16), rc["v_cache"].view(torch.int16)
+    kp, vp = rp["k_cache"].view(torch.int16), rp["v_cache"].view(torch.int16)
+    touched = torch.zeros(kp.shape[0], dtype=torch.bool)
+    pt = hp["page_table"]
+    for b in range(w.batch):
+        end = w.cache_lens[b] + w.new_lens[b]
+        pos = torch.arange(end)
+        sp = pt[b, pos // page_size].long() * page_size + pos % page_size
+        sc = hc["slot_base"][b] + pos
+        assert torch.equal(kp[sp], kc[sc]) and torch.equal(vp[sp], vc[sc])
+        touched[sp] = True
+    k0, v0 = hp["k_cache"].view(torch.int16), hp["v_cache"].view(torch.int16)
+    assert torch.equal(kp[~touched], k0[~touched]) and torch.equal(vp[~touched], v0[~touched])
