@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--workload", default="qwen3_4b_prefill_8seq_U256_2048")
     ap.add_argument("--decode-workload", default="decode_b64_cache_U512_8192")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode measurement")
+    ap.add_argument("--page-size", type=int, default=0,
+                    help="lay the KV caches out in pages of this many slots (0: contiguous regions)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU oracle sample budget")
     return ap.parse_args()
@@ -228,12 +230,12 @@ class Timed:
             ev[4].record()
 
 
-def measure(w, steps, warmup, device, torch, dist_on):
+def measure(w, steps, warmup, device, torch, dist_on, page_size=0):
     """Device-timed steps of workload w.  Returns per-part mean ms and more."""
     from causal_gqa_attention_qkv_gb300 import inputs as gen
     from causal_gqa_attention_qkv_gb300 import step
 
-    host = gen.make_inputs(w)
+    host = gen.make_inputs(w, page_size=page_size)
     ds = step.upload(w, host, device=device)
     B_dec = w.batch - w.decode_from
     ds.decode_cu = torch.arange(B_dec + 1, dtype=torch.int32, device=device)
@@ -372,7 +374,7 @@ def run_ours(args):
     w = gen.ALL[args.workload]
     assert w.decode_from == w.batch, "the headline workload is a prefill workload"
     with ClockSampler(local_rank) as clk:
-        m = measure(w, args.steps, args.warmup, device, torch, dist_on)
+        m = measure(w, args.steps, args.warmup, device, torch, dist_on, args.page_size)
     clocks = clk.summary()
     step_ms, attend_ms = max_over_ranks([m["ms"]["step"], m["ms"]["prefill_attend"]], device)
     flops = prefill_flops(w)
@@ -389,7 +391,8 @@ def run_ours(args):
         "config": {"workload": w.name, "global_batch": w.batch * world, "seq_len": max(w.new_lens),
                    "tokens": w.num_tokens, "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
                    "head_dim": w.head_dim, "attended_pairs": w.attended_pairs(),
-                   "parallelism": f"replicas{world}", "l2": "flushed before every timed step"},
+                   "parallelism": f"replicas{world}", "l2": "flushed before every timed step",
+                   "kv_layout": f"paged{args.page_size}" if args.page_size else "contiguous"},
         "parts_ms": {"prologue": round(m["ms"]["prefill_append"], 4),
                      "prefill_attention": round(attend_ms, 4)},
         "roofline": {"bound": "tensor", "kernel": "prefill attention", "achieved": round(achieved, 3),
@@ -403,7 +406,7 @@ def run_ours(args):
     }
     if not args.no_decode:
         wd = gen.ALL[args.decode_workload]
-        md = measure(wd, args.steps, args.warmup, device, torch, dist_on)
+        md = measure(wd, args.steps, args.warmup, device, torch, dist_on, args.page_size)
         dms, dattend = max_over_ranks([md["ms"]["step"], md["ms"]["decode_attend"]], device)
         nbytes = decode_bytes(wd)
         attend_bytes = nbytes - wd.batch * 2 * wd.num_kv_heads * wd.head_dim * 2  # no append write
