@@ -466,17 +466,29 @@ __device__ void softmax_tile(const TcPar& p, const SeqInfo* seq_tab, const int* 
       float mx[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) mx[e] = kNegInf;
+      // The limits of a warp's rows do not decrease with the lane: lane 0 has
+      // the lowest, lane 31 the highest.  A 32-column chunk past the highest
+      // holds no visible key (skipped, P = 0); one below the lowest needs no
+      // selects.
+      const int lim_lo = __shfl_sync(0xffffffffu, lim_rel, 0);
+      const int lim_hi = __shfl_sync(0xffffffffu, lim_rel, 31);
       if (masked) {
 #pragma unroll 1
-        for (int c0 = 0; c0 < kKeys; c0 += 32) {
+        for (int c0 = 0; c0 < kKeys && c0 <= lim_hi; c0 += 32) {
           uint32_t sr[32];
           tc::ld_32x32b_x32(s_tmem + c0, sr);
           tc::wait_ld();
+          if (c0 + 31 <= lim_lo) {
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const float v0 = c0 + c <= lim_rel ? __uint_as_float(sr[c]) : kNegInf;
-            const float v1 = c0 + c + 1 <= lim_rel ? __uint_as_float(sr[c + 1]) : kNegInf;
-            mx[(c >> 1) & 3] = max3f(mx[(c >> 1) & 3], v0, v1);
+            for (int c = 0; c < 32; c += 2)
+              mx[(c >> 1) & 3] = max3f(mx[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              const float v0 = c0 + c <= lim_rel ? __uint_as_float(sr[c]) : kNegInf;
+              const float v1 = c0 + c + 1 <= lim_rel ? __uint_as_float(sr[c + 1]) : kNegInf;
+              mx[(c >> 1) & 3] = max3f(mx[(c >> 1) & 3], v0, v1);
+            }
           }
         }
       } else {
@@ -527,7 +539,16 @@ __device__ void softmax_tile(const TcPar& p, const SeqInfo* seq_tab, const int* 
       };
       if (masked) {
 #pragma unroll 1
-        for (int q = 0; q < kKeys / 32; ++q) chunk(q, true);
+        for (int q = 0; q < kKeys / 32; ++q) {
+          if (q * 32 > lim_hi) {  // no visible key in this chunk for any row of the warp
+            uint32_t z[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) z[e] = 0u;
+            tc::st_32x32b_x16(s_tmem + q * 16, z);
+          } else {
+            chunk(q, q * 32 + 31 > lim_lo);
+          }
+        }
       } else {
 #pragma unroll 2
         for (int q = 0; q < kKeys / 32; ++q) chunk(q, false);
