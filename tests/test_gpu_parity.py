@@ -98,6 +98,50 @@ def test_paged_cache_all_rows_and_same_bits_as_contiguous(ps, hq, hkv, d, lens, 
     assert torch.equal(paged.out.view(torch.int16), contiguous.out.view(torch.int16))
 
 
+def test_empty_calls_are_no_ops():
+    """N = 0 and B = 0 calls return OK, write nothing and set no status.  The
+    ABI wants valid pointers even then (a torch view with no elements reports
+    address 0), so the library is called with the real buffers and zero sizes."""
+    import ctypes
+    from causal_gqa_attention_qkv_gb300 import attn, step
+    w = gen.custom("empty_base", 8, 2, 128, [5], [3], seed=40)
+    ds = step.upload(w, gen.make_inputs(w))
+    k0, v0, o0 = ds.k_cache.clone(), ds.v_cache.clone(), ds.out.clone()
+    lib, P, st = attn.load(), attn._ptr, attn._stream()
+    cu = torch.zeros(2, dtype=torch.int32, device=ds.out.device)  # one request with no tokens
+    ws, nws = P(ds.workspace), ds.workspace.numel()
+    for kv in (ds.kv_prefill,):
+        s = kv.struct()
+        for B in (0, 1):
+            assert lib.attn_prefill(ctypes.byref(ds.cfg), P(ds.qkv), P(ds.q_norm_w), P(ds.k_norm_w), P(cu), B, 0,
+                                    0, ctypes.byref(s), P(ds.out), ws, nws, st) == 0
+            assert lib.attn_kv_append(ctypes.byref(ds.cfg), P(ds.qkv), None, P(ds.k_norm_w), P(cu), B, 0,
+                                      ctypes.byref(s), ws, nws, st) == 0
+        assert lib.attn_decode(ctypes.byref(ds.cfg), P(ds.qkv), P(ds.q_norm_w), P(ds.k_norm_w), 0, 0,
+                               ctypes.byref(s), P(ds.out), ws, nws, st) == 0
+    torch.cuda.synchronize()
+    assert ds.status() == 0
+    assert torch.equal(k0.view(torch.int16), ds.k_cache.view(torch.int16))
+    assert torch.equal(v0.view(torch.int16), ds.v_cache.view(torch.int16))
+    assert torch.equal(o0.view(torch.int16), ds.out.view(torch.int16))
+
+
+def test_zero_length_sequences_in_a_packed_batch():
+    """Requests with no new tokens (cu_seqlens repeats a value) are skipped;
+    the others are computed as usual."""
+    w = gen.custom("zero_len", 32, 8, 128, [0, 37, 0, 1, 130, 0], [5, 0, 0, 200, 64, 9], seed=41)
+    run_and_compare(w, gen.make_inputs(w))
+
+
+@pytest.mark.parametrize("hq,hkv,d,lens,cache", [
+    (128, 16, 128, [70, 130], [0, 40]),   # the most heads the ABI takes, group 8
+    (128, 128, 64, [33, 65], [7, 0]),     # multi-head (group 1) at the head limit
+])
+def test_largest_head_counts(hq, hkv, d, lens, cache):
+    w = gen.custom(f"heads_{hq}_{hkv}_{d}", hq, hkv, d, lens, cache, seed=hq + hkv + d)
+    run_and_compare(w, gen.make_inputs(w))
+
+
 def test_mixed_prefill_and_decode_small():
     w = gen.custom("mixed_small", 32, 8, 128, [100, 64, 1, 1, 1], [50, 0, 10, 700, 0], seed=77,
                    decode_from=2)
