@@ -23,6 +23,11 @@ Layouts (all row-major, host tensors on the CPU):
   normed and rotated keys); every other slot (the rest of each region and the
   guard slots between regions) holds ``unused_fill`` so that a stray read or
   write is visible.
+* With ``kv_dtype="e4m3"`` the pool is uint8 ``[num_slots, Hkv, D]`` of E4M3
+  codes with one scale per cache (``k_scale``, ``v_scale``): the cached
+  entries are N(0, 1) values divided by the scale and cast with torch's own
+  ``float8_e4m3fn`` conversion; the unused fill is the E4M3 NaN code or a
+  finite sentinel code.
 """
 from __future__ import annotations
 
@@ -36,6 +41,13 @@ BF16_QNAN_BITS = 0x7FC0
 BF16_SENTINEL_BITS = 0x4B3D  # a finite, distinctive value (12.3125 * 2**10)
 
 GUARD_SLOTS = 3  # slots between two requests' regions, never written
+
+# E4M3 codes for the same purpose, and the default scales of a one-byte cache
+# (normed keys and N(0, 1) values stay well inside +-448 * scale).
+E4M3_NAN_BITS = 0x7F
+E4M3_SENTINEL_BITS = 0x5B  # a finite, distinctive code (22.0)
+E4M3_K_SCALE = 0.04
+E4M3_V_SCALE = 0.02
 
 
 @dataclasses.dataclass(frozen=True)
@@ -153,8 +165,14 @@ def _fill_bits(t: torch.Tensor, bits: int) -> None:
     t.view(torch.int16).fill_(bits if bits < 0x8000 else bits - 0x10000)
 
 
+def _e4m3_codes(x: torch.Tensor, scale: float) -> torch.Tensor:
+    """uint8 E4M3 codes of x / scale (torch's conversion; inputs clamped to +-448)."""
+    return (x / scale).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
 def make_inputs(w: Workload, extra_capacity: Sequence[int] | None = None,
-                unused_fill: str = "nan", page_size: int = 0) -> dict:
+                unused_fill: str = "nan", page_size: int = 0, kv_dtype: str = "bf16",
+                k_scale: float = E4M3_K_SCALE, v_scale: float = E4M3_V_SCALE) -> dict:
     """Draw all inputs of one call of workload ``w`` (host tensors).
 
     ``extra_capacity[b]`` is the number of free slots left after request b's
@@ -166,7 +184,10 @@ def make_inputs(w: Workload, extra_capacity: Sequence[int] | None = None,
     ``page_table`` (int32 [B, max pages]; unused entries -1).  The logical
     contents (qkv, weights, prior cache entries by position) are the same as
     with the contiguous layout for the same workload.
+    ``kv_dtype="e4m3"`` makes a one-byte cache (codes, ``k_scale``, ``v_scale``).
     """
+    assert kv_dtype in ("bf16", "e4m3")
+    fp8 = kv_dtype == "e4m3"
     g = _gen(1000 + w.seed)
     B, H, Hkv, D = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
     N = w.num_tokens
@@ -193,15 +214,22 @@ def make_inputs(w: Workload, extra_capacity: Sequence[int] | None = None,
             k += npg[b]
         num_slots = total * page_size
         base = [0] * B
-    k_cache = torch.empty((num_slots, Hkv, D), dtype=torch.bfloat16)
-    v_cache = torch.empty((num_slots, Hkv, D), dtype=torch.bfloat16)
-    bits = BF16_QNAN_BITS if unused_fill == "nan" else BF16_SENTINEL_BITS
-    _fill_bits(k_cache, bits)
-    _fill_bits(v_cache, bits)
+    if fp8:
+        k_cache = torch.full((num_slots, Hkv, D), E4M3_NAN_BITS if unused_fill == "nan" else E4M3_SENTINEL_BITS,
+                             dtype=torch.uint8)
+        v_cache = k_cache.clone()
+    else:
+        k_cache = torch.empty((num_slots, Hkv, D), dtype=torch.bfloat16)
+        v_cache = torch.empty((num_slots, Hkv, D), dtype=torch.bfloat16)
+        bits = BF16_QNAN_BITS if unused_fill == "nan" else BF16_SENTINEL_BITS
+        _fill_bits(k_cache, bits)
+        _fill_bits(v_cache, bits)
     for b in range(B):
         c = w.cache_lens[b]
         if c:
             kp, vp = _bf16_normal(g, (c, Hkv, D)), _bf16_normal(g, (c, Hkv, D))
+            if fp8:
+                kp, vp = _e4m3_codes(kp.float(), k_scale), _e4m3_codes(vp.float(), v_scale)
             if page_table is None:
                 k_cache[base[b]:base[b] + c] = kp
                 v_cache[base[b]:base[b] + c] = vp
@@ -226,6 +254,9 @@ def make_inputs(w: Workload, extra_capacity: Sequence[int] | None = None,
         "num_slots": num_slots,
         "page_table": page_table,
         "page_size": page_size,
+        "kv_dtype": kv_dtype,
+        "k_scale": float(k_scale),
+        "v_scale": float(v_scale),
     }
 
 

@@ -9,9 +9,12 @@ the passages it follows, in that file's header.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (brute force from the teaching snippet, closed forms, torch's ``rms_norm``,
-the complex form of RoPE, invariants).  The RoPE pairing convention itself
-(rotate-half) is a reading the pages leave open: parity unpinned for that
-choice, pinned for everything given it.
+the complex form of RoPE, invariants; the E4M3 codec against torch's
+``float8_e4m3fn`` for every code and for ties).  The RoPE pairing convention
+itself (rotate-half) is a reading the pages leave open: parity unpinned for
+that choice, pinned for everything given it.  So is the one-byte cache
+format (E4M3, one scale per cache, code of fp32(x) * fp32(1/scale)): the
+pages name no format; pinned given that reading.
 """
 from __future__ import annotations
 
@@ -31,6 +34,7 @@ _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
 _I64 = ctypes.c_int64
 _D = ctypes.c_double
+_F = ctypes.c_float
 
 
 def build(force: bool = False) -> str:
@@ -52,6 +56,10 @@ def _load():
         lib = ctypes.CDLL(_LIB)
         lib.oracle_bf16_round.restype = ctypes.c_uint16
         lib.oracle_bf16_round.argtypes = [_D]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_e4m3_encode.argtypes = [_D]
+        lib.oracle_e4m3_decode.restype = _D
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
         lib.oracle_rmsnorm.restype = None
         lib.oracle_rmsnorm.argtypes = [_P, _P, ctypes.c_int, _D, _P]
         lib.oracle_rope.restype = None
@@ -60,11 +68,11 @@ def _load():
         lib.oracle_prologue.argtypes = [
             ctypes.c_int, ctypes.c_int, ctypes.c_int, _D, _D,
             _P, _I64, _P, _P, ctypes.c_int, _P, _P, _P, _P, _P, ctypes.c_int, ctypes.c_int,
-            _I64, _P, _P, _I64, _P, _P, _P]
+            _I64, _P, _P, ctypes.c_int, _F, _F, _I64, _P, _P, _P]
         lib.oracle_attention.restype = None
         lib.oracle_attention.argtypes = [
-            ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P, _P,
-            _P, ctypes.c_int, ctypes.c_int, _I64, _P, _P, _P, _P]
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, ctypes.c_int, _F, _F, ctypes.c_int, _P,
+            _P, _P, _P, ctypes.c_int, ctypes.c_int, _I64, _P, _P, _P, _P]
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -92,6 +100,41 @@ def _bits_view(t: torch.Tensor) -> np.ndarray:
 
 def bits_to_bf16(a: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+
+def _cache_copy(t: torch.Tensor) -> np.ndarray:
+    """A cache tensor's entries as a new array: uint16 bf16 bits, or the
+    uint8 E4M3 bytes of a one-byte cache."""
+    if t.dtype == torch.uint8:
+        return np.array(t.detach().cpu().contiguous().numpy(), copy=True)
+    return _bits(t)
+
+
+def _cache_view(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.uint8:
+        return t.detach().cpu().contiguous().numpy()
+    return _bits_view(t)
+
+
+def _cache_tensor(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(a) if a.dtype == np.uint8 else bits_to_bf16(a)
+
+
+def _kv_format(inputs: dict):
+    """(kv_fp8, k_scale, v_scale) of the inputs' cache."""
+    if inputs.get("kv_dtype", "bf16") == "e4m3":
+        return 1, float(inputs["k_scale"]), float(inputs["v_scale"])
+    return 0, 1.0, 1.0
+
+
+def e4m3_encode(x: float) -> int:
+    """The E4M3 code nearest to ``x`` (ties to even, magnitudes beyond 448
+    clamped to 448)."""
+    return int(_load().oracle_e4m3_encode(float(x)))
+
+
+def e4m3_decode(b: int) -> float:
+    return float(_load().oracle_e4m3_decode(int(b)))
 
 
 def bf16_round(x: float) -> int:
@@ -125,7 +168,8 @@ def _pages(inputs: dict):
 
 def prologue(cfg: dict, inputs: dict, q_rows=None):
     """Steps 1-4.  Returns (k_cache, v_cache, q, bad) where the caches are new
-    bf16 tensors (the inputs are not modified), q is fp64 ``[N, Hq, D]`` (or
+    tensors of the input caches' type (bf16, or uint8 E4M3 codes; the inputs
+    are not modified), q is fp64 ``[N, Hq, D]`` (or
     ``[R, D]`` for the (token, head) pairs in ``q_rows``), and ``bad`` counts
     requests whose cache region is too small (they write nothing)."""
     lib = _load()
@@ -133,8 +177,9 @@ def prologue(cfg: dict, inputs: dict, q_rows=None):
     assert D <= 256 and D % 2 == 0 and Hq % Hkv == 0
     qkv = _bits_view(inputs["qkv"])
     N = qkv.shape[0]
-    kc = _bits(inputs["k_cache"])
-    vc = _bits(inputs["v_cache"])
+    kc = _cache_copy(inputs["k_cache"])
+    vc = _cache_copy(inputs["v_cache"])
+    fp8, ks, vs = _kv_format(inputs)
     qw, kw = _bits(inputs["q_norm_w"]), _bits(inputs["k_norm_w"])
     cu = np.ascontiguousarray(inputs["cu_seqlens"].numpy().astype(np.int32))
     cl = np.ascontiguousarray(inputs["cache_lens"].numpy().astype(np.int32))
@@ -154,9 +199,9 @@ def prologue(cfg: dict, inputs: dict, q_rows=None):
         q = np.zeros((nq, D), dtype=np.float64)
     bad = lib.oracle_prologue(Hq, Hkv, D, float(cfg["rms_eps"]), float(cfg["rope_theta"]),
                               _ptr(qkv), N, _ptr(qw), _ptr(kw), B, _ptr(cu), _ptr(cl), _ptr(sb),
-                              _ptr(cap), _ptr(pt), ps, ppr, kc.shape[0], _ptr(kc), _ptr(vc), nq,
-                              _ptr(qt), _ptr(qh), _ptr(q))
-    return bits_to_bf16(kc), bits_to_bf16(vc), q, bad
+                              _ptr(cap), _ptr(pt), ps, ppr, kc.shape[0], _ptr(kc), _ptr(vc), fp8, ks,
+                              vs, nq, _ptr(qt), _ptr(qh), _ptr(q))
+    return _cache_tensor(kc), _cache_tensor(vc), q, bad
 
 
 def attention(cfg: dict, k_cache: torch.Tensor, v_cache: torch.Tensor, inputs: dict,
@@ -170,13 +215,15 @@ def attention(cfg: dict, k_cache: torch.Tensor, v_cache: torch.Tensor, inputs: d
     tok = np.ascontiguousarray(rows[:, 0])
     head = np.ascontiguousarray(rows[:, 1])
     q = np.ascontiguousarray(q, dtype=np.float64).reshape(R, D)
-    kc, vc = _bits_view(k_cache), _bits_view(v_cache)
+    kc, vc = _cache_view(k_cache), _cache_view(v_cache)
+    fp8, ks, vs = _kv_format(inputs)
     cu = np.ascontiguousarray(inputs["cu_seqlens"].numpy().astype(np.int32))
     cl = np.ascontiguousarray(inputs["cache_lens"].numpy().astype(np.int32))
     sb = np.ascontiguousarray(inputs["slot_base"].numpy().astype(np.int64))
     pt, ps, ppr = _pages(inputs)
     out = np.zeros((R, D), dtype=np.float64)
-    lib.oracle_attention(Hq, Hkv, D, _ptr(kc), _ptr(vc), cl.shape[0], _ptr(cu), _ptr(cl), _ptr(sb),
+    lib.oracle_attention(Hq, Hkv, D, _ptr(kc), _ptr(vc), fp8, ks, vs, cl.shape[0], _ptr(cu), _ptr(cl),
+                         _ptr(sb),
                          _ptr(pt), ps, ppr, R, _ptr(tok), _ptr(head), _ptr(q), _ptr(out))
     return out
 

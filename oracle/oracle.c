@@ -30,6 +30,15 @@
  *   - norm before RoPE; position of new token j of request b is c_b + j;
  *   - Q stays in fp64; K is rounded to bf16 (round to nearest even) once,
  *     when it is written to the cache; softmax and P.V in fp64.
+ *
+ * One-byte cache entries (kv_fp8 != 0): the concept chapter's section 4.3
+ * (decode is bound by memory bandwidth) and its section 2.6 (KV-cache
+ * reduction among the modern variants) motivate them; the pages fix no
+ * format, so the reading is OCP FP8 E4M3 with one scale per cache: the
+ * stored byte of x is e4m3(fp32(x) * fp32(1 / scale)), the product taken in
+ * fp32 because that is the precision the stored code is decided in, rounded
+ * to nearest even with magnitudes beyond 448 clamped to 448; an entry reads
+ * as byte * scale.  Attention then runs in fp64 on those values.
  */
 #include <math.h>
 #include <stdint.h>
@@ -68,6 +77,52 @@ uint16_t oracle_bf16_round(double x) {
   uint32_t u;
   memcpy(&u, &f, sizeof u);
   return sign | (uint16_t)(u >> 16);
+}
+
+/*
+ * OCP FP8 E4M3: sign bit, 4 exponent bits (bias 7), 3 mantissa bits.  Code
+ * (E, M) with E >= 1 is (8 + M) * 2^(E - 10); E = 0 is M * 2^-9 (subnormal);
+ * E = 15, M = 7 is NaN; there is no infinity, so 448 (E = 15, M = 6) is the
+ * largest finite value.
+ */
+double oracle_e4m3_decode(uint8_t b) {
+  int E = (b >> 3) & 15, M = b & 7;
+  if (E == 15 && M == 7) return NAN;
+  double v = E == 0 ? ldexp((double)M, -9) : ldexp((double)(8 + M), E - 10);
+  return (b & 0x80) ? -v : v;
+}
+
+/* Nearest E4M3 code to x, ties to even; finite magnitudes at or beyond 448
+ * give 448 (the saturating conversion).  The quantum of the binade
+ * [2^e, 2^(e+1)) is 2^(e-3), and 2^-9 below 2^-6 (subnormals); dividing by
+ * it is exact, nearbyint rounds to nearest even, and the rounded value is
+ * then exactly one code (it may be the bottom of the next binade). */
+uint8_t oracle_e4m3_encode(double x) {
+  if (isnan(x)) return 0x7F;
+  uint8_t sign = signbit(x) ? 0x80 : 0;
+  double a = fabs(x);
+  if (a >= 448.0) return sign | 0x7E;
+  if (a == 0.0) return sign;
+  int e;
+  frexp(a, &e); /* a in [2^(e-1), 2^e) */
+  int lo = e - 1 < -6 ? -6 : e - 1;
+  double quantum = ldexp(1.0, lo - 3);
+  double r = nearbyint(a / quantum) * quantum; /* <= 448 since a < 448 = 14 * 32 */
+  if (r < ldexp(1.0, -6)) return sign | (uint8_t)(r / ldexp(1.0, -9));
+  int er;
+  double f = frexp(r, &er); /* r = f * 2^er, f in [0.5, 1) */
+  int E = er - 1 + 7;
+  int M = (int)((2.0 * f - 1.0) * 8.0);
+  return sign | (uint8_t)(E << 3) | (uint8_t)M;
+}
+
+/* Code stored for value x under a cache scale: e4m3(fp32(x) * fp32(1/scale)),
+ * both roundings to fp32 and the product in fp32 (C evaluates float * float
+ * in float on the targets this builds for). */
+static uint8_t e4m3_store(double x, float scale) {
+  const float r = 1.0f / scale;
+  const float t = (float)x * r;
+  return oracle_e4m3_encode((double)t);
 }
 
 /* Weighted RMSNorm of one head vector (step 2). */
@@ -118,9 +173,9 @@ static void load_head(const uint16_t* row, int64_t col0, int D, double* out) {
 }
 
 /*
- * Steps 1-4 for all N tokens.  The cache (k_cache, v_cache: bf16 bits
- * [num_slots, Hkv, D]) is updated in place: token j of request b goes to the
- * slot of position cache_lens[b] + j (slot_of).  Q rows (normed, rotated, fp64) are written
+ * Steps 1-4 for all N tokens.  The cache (k_cache, v_cache: bf16 bits, or
+ * E4M3 bytes when kv_fp8, [num_slots, Hkv, D]) is updated in place: token j
+ * of request b goes to the slot of position cache_lens[b] + j (slot_of).  Q rows (normed, rotated, fp64) are written
  * to q_out: all N*Hq rows as [N, Hq, D] when nq < 0, otherwise the nq rows
  * (q_tok[r], q_head[r]) as [nq, D].  Returns the number of requests whose
  * region cannot hold cache_lens + new tokens (those write nothing).
@@ -130,9 +185,9 @@ int oracle_prologue(int Hq, int Hkv, int D, double eps, double theta,
                     const uint16_t* k_norm_w, int B, const int32_t* cu_seqlens,
                     const int32_t* cache_lens, const int64_t* slot_base,
                     const int32_t* slot_capacity, const int32_t* page_table, int page_size,
-                    int pages_per_req, int64_t num_slots, uint16_t* k_cache,
-                    uint16_t* v_cache, int64_t nq, const int32_t* q_tok,
-                    const int32_t* q_head, double* q_out) {
+                    int pages_per_req, int64_t num_slots, void* k_cache,
+                    void* v_cache, int kv_fp8, float k_scale, float v_scale, int64_t nq,
+                    const int32_t* q_tok, const int32_t* q_head, double* q_out) {
   const int64_t W = (int64_t)(Hq + 2 * Hkv) * D;
   double* qw = malloc(sizeof(double) * D);
   double* kw = malloc(sizeof(double) * D);
@@ -166,12 +221,22 @@ int oracle_prologue(int Hq, int Hkv, int D, double eps, double theta,
         load_head(row, (int64_t)(Hq + kh) * D, D, x);
         oracle_rmsnorm(x, kw, D, eps, y);
         oracle_rope(y, D, pos, theta);
-        uint16_t* kd = k_cache + (slot * Hkv + kh) * D;
-        uint16_t* vd = v_cache + (slot * Hkv + kh) * D;
+        const int64_t e0 = (slot * Hkv + kh) * D;
         const uint16_t* vs = row + (int64_t)(Hq + Hkv + kh) * D;
-        for (int i = 0; i < D; ++i) {
-          kd[i] = oracle_bf16_round(y[i]);
-          vd[i] = vs[i];
+        if (kv_fp8) {
+          uint8_t* kd = (uint8_t*)k_cache + e0;
+          uint8_t* vd = (uint8_t*)v_cache + e0;
+          for (int i = 0; i < D; ++i) {
+            kd[i] = e4m3_store(y[i], k_scale);
+            vd[i] = e4m3_store(bf16_bits_to_double(vs[i]), v_scale);
+          }
+        } else {
+          uint16_t* kd = (uint16_t*)k_cache + e0;
+          uint16_t* vd = (uint16_t*)v_cache + e0;
+          for (int i = 0; i < D; ++i) {
+            kd[i] = oracle_bf16_round(y[i]);
+            vd[i] = vs[i];
+          }
         }
       }
     }
@@ -196,9 +261,16 @@ int oracle_prologue(int Hq, int Hkv, int D, double eps, double theta,
 /*
  * Step 5 for nrows (token, head) rows: out[r] = softmax(q_r . K^T / sqrt(D)) V
  * over the keys at positions 0 .. c_b + j of the row's request (the query's
- * own key included; later keys excluded), read from the cache.
+ * own key included; later keys excluded), read from the cache (E4M3 entries
+ * when kv_fp8: byte * scale).
  */
-void oracle_attention(int Hq, int Hkv, int D, const uint16_t* k_cache, const uint16_t* v_cache,
+static double cache_entry(const void* cache, int kv_fp8, float scale, int64_t idx) {
+  if (kv_fp8) return oracle_e4m3_decode(((const uint8_t*)cache)[idx]) * (double)scale;
+  return bf16_bits_to_double(((const uint16_t*)cache)[idx]);
+}
+
+void oracle_attention(int Hq, int Hkv, int D, const void* k_cache, const void* v_cache,
+                      int kv_fp8, float k_scale, float v_scale,
                       int B, const int32_t* cu_seqlens, const int32_t* cache_lens,
                       const int64_t* slot_base, const int32_t* page_table, int page_size,
                       int pages_per_req, int64_t nrows, const int32_t* tok,
@@ -216,10 +288,9 @@ void oracle_attention(int Hq, int Hkv, int D, const uint16_t* k_cache, const uin
     double* s = malloc(sizeof(double) * (size_t)nkeys);
     const double* qr = q + r * D;
     for (int64_t u = 0; u < nkeys; ++u) {
-      const uint16_t* kr =
-          k_cache + (slot_of(slot_base, page_table, page_size, pages_per_req, b, u) * Hkv + kvh) * D;
+      const int64_t k0 = (slot_of(slot_base, page_table, page_size, pages_per_req, b, u) * Hkv + kvh) * D;
       double acc = 0.0;
-      for (int i = 0; i < D; ++i) acc += qr[i] * bf16_bits_to_double(kr[i]);
+      for (int i = 0; i < D; ++i) acc += qr[i] * cache_entry(k_cache, kv_fp8, k_scale, k0 + i);
       s[u] = acc * scale;
     }
     /* softmax(s) = exp(s - max) / sum exp(s - max): the shift leaves it unchanged */
@@ -234,9 +305,8 @@ void oracle_attention(int Hq, int Hkv, int D, const uint16_t* k_cache, const uin
     for (int i = 0; i < D; ++i) o[i] = 0.0;
     for (int64_t u = 0; u < nkeys; ++u) {
       double p = s[u] / z;
-      const uint16_t* vr =
-          v_cache + (slot_of(slot_base, page_table, page_size, pages_per_req, b, u) * Hkv + kvh) * D;
-      for (int i = 0; i < D; ++i) o[i] += p * bf16_bits_to_double(vr[i]);
+      const int64_t v0 = (slot_of(slot_base, page_table, page_size, pages_per_req, b, u) * Hkv + kvh) * D;
+      for (int i = 0; i < D; ++i) o[i] += p * cache_entry(v_cache, kv_fp8, v_scale, v0 + i);
     }
     free(s);
   }

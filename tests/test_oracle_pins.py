@@ -346,3 +346,81 @@ def test_paged_cache_gives_the_contiguous_result(page_size):
         touched[sp] = True
     k0, v0 = hp["k_cache"].view(torch.int16), hp["v_cache"].view(torch.int16)
     assert torch.equal(kp[~touched], k0[~touched]) and torch.equal(vp[~touched], v0[~touched])
+
+
+# ---------------------------------------------------------------- E4M3 cache entries
+def _torch_e4m3_values(codes):
+    return torch.as_tensor(codes, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+
+
+def test_e4m3_decode_matches_torch_for_every_code():
+    """Every one of the 256 codes decodes as torch's float8_e4m3fn reads it;
+    0x7F and 0xFF are the only NaNs and 448 is the largest finite value."""
+    got = np.array([oracle.e4m3_decode(b) for b in range(256)])
+    ref = _torch_e4m3_values(np.arange(256))
+    nan = np.isnan(ref)
+    assert np.flatnonzero(nan).tolist() == [0x7F, 0xFF] and np.isnan(got[nan]).all()
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert got[~nan].max() == 448.0 and got[0x01] == 2.0 ** -9 and got[0x08] == 2.0 ** -6
+
+
+def test_e4m3_encode_matches_torch_in_range_and_rounds_ties_to_even():
+    g = np.random.default_rng(5)
+    x = np.concatenate([g.normal(size=20000) * 40, g.normal(size=20000) * 1e-2,
+                        g.uniform(-447.9, 447.9, 20000), [0.0, -0.0, 2.0 ** -10, -(2.0 ** -10)]])
+    x = x.astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(float(v)) for v in x], dtype=np.uint8)
+    assert np.array_equal(got, ref)
+    # every midpoint between neighbouring positive codes goes to the even code
+    vals = [(oracle.e4m3_decode(b), b) for b in range(0x7F)]
+    for (va, a), (vb, b) in zip(vals, vals[1:]):
+        mid = (va + vb) / 2
+        assert oracle.e4m3_encode(mid) == (a if a % 2 == 0 else b)
+        assert oracle.e4m3_encode(np.nextafter(mid, 0.0)) == a
+        assert oracle.e4m3_encode(np.nextafter(mid, 1e9)) == b
+
+
+def test_e4m3_encode_saturates_beyond_448():
+    for x in (448.0, 448.1, 463.9, 464.0, 500.0, 1e30, math.inf):
+        assert oracle.e4m3_encode(x) == 0x7E
+        assert oracle.e4m3_encode(-x) == 0xFE
+
+
+def test_e4m3_cache_store_rule_and_reads():
+    """A one-byte cache holds e4m3(fp32(x) * fp32(1 / scale)) per entry:
+    V codes equal torch's own cast of that fp32 product; K codes read back
+    within half a code step (plus half a bf16 step) of the bf16 cache's K;
+    and attention over the codes equals attention over a bf16 cache holding
+    the decoded values when those are exact in bf16 (scale a power of two)."""
+    w = gen.custom("e4m3_pin", 8, 2, 64, [11, 5], [6, 0], seed=31)
+    cfg = oracle.cfg_of(w)
+    for ks, vs in ((0.04, 0.02), (2.0 ** -4, 2.0 ** -5)):
+        h8 = gen.make_inputs(w, kv_dtype="e4m3", k_scale=ks, v_scale=vs)
+        r8 = oracle.step(cfg, h8)
+        hb = gen.make_inputs(w)
+        rb = oracle.step(cfg, hb)
+        k8, v8 = r8["k_cache"].numpy(), r8["v_cache"].numpy()
+        kb = rb["k_cache"].double().numpy()
+        Hq, Hkv, D = w.num_q_heads, w.num_kv_heads, w.head_dim
+        for b in range(w.batch):
+            for j in range(w.new_lens[b]):
+                t = int(h8["cu_seqlens"][b]) + j
+                slot = int(h8["slot_base"][b]) + w.cache_lens[b] + j
+                v_in = h8["qkv"][t, (Hq + Hkv) * D:].float().reshape(Hkv, D)
+                want = (v_in * torch.tensor(1.0 / np.float32(vs), dtype=torch.float32)) \
+                    .to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+                assert np.array_equal(v8[slot], want)
+                kr = _torch_e4m3_values(k8[slot]) * np.float32(ks)
+                # code step at |x| / scale, in units of x
+                step = ks * 2.0 ** (np.floor(np.log2(np.maximum(np.abs(kb[slot]) / ks, 2.0 ** -6))) - 3)
+                assert (np.abs(kr - kb[slot]) <= 0.5 * step + 2.0 ** -8 * np.abs(kb[slot]) + 1e-12).all()
+        if ks == 2.0 ** -4:
+            # the same codes, decoded into a bf16 cache: identical attention in fp64
+            hbf = dict(h8, kv_dtype="bf16",
+                       k_cache=(torch.from_numpy(k8).view(torch.float8_e4m3fn).double() * ks).to(torch.bfloat16),
+                       v_cache=(torch.from_numpy(v8).view(torch.float8_e4m3fn).double() * vs).to(torch.bfloat16))
+            rows = oracle.all_rows(w.num_tokens, Hq)
+            a8 = oracle.attention(cfg, r8["k_cache"], r8["v_cache"], h8, rows, r8["q"])
+            ab = oracle.attention(cfg, hbf["k_cache"], hbf["v_cache"], hbf, rows, r8["q"])
+            assert np.array_equal(a8, ab)
