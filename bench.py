@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--workload", default="qwen3_4b_prefill_8seq_U256_2048")
     ap.add_argument("--decode-workload", default="decode_b64_cache_U512_8192")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode measurement")
+    ap.add_argument("--mixed-workload", default="mixed_4x1024chunks_256decode")
+    ap.add_argument("--no-mixed", action="store_true", help="skip the mixed-step measurement")
     ap.add_argument("--page-size", type=int, default=0,
                     help="lay the KV caches out in pages of this many slots (0: contiguous regions)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
@@ -353,6 +355,34 @@ def cpu_oracle_decode_rate(w, budget_s: float):
     return decode_bytes(w, 0, nb), dt, f"all heads of the first {nb} requests of {w.name}", oracle.num_threads()
 
 
+def measure_mixed(wm, args, device, torch, dist_on, peaks, peak_kind) -> dict:
+    """One serving step that mixes prefill chunks (on top of cached prefixes)
+    with decode rows, issued back to back on one stream: the chunks'
+    prepare + attention, then the decode rows' append + attention.  The
+    step's roofline fraction adds the tensor-bound and the HBM-bound parts:
+    (chunk FLOPs / bf16 peak + decode bytes / HBM peak) / step time."""
+    mm = measure(wm, args.steps, args.warmup, device, torch, dist_on, args.page_size)
+    ms = mm["ms"]
+    step_ms, pp, pa, da, dd = max_over_ranks([ms["step"], ms["prefill_append"], ms["prefill_attend"],
+                                              ms["decode_append"], ms["decode_attend"]], device)
+    fl = prefill_flops(wm, 0, wm.decode_from)
+    nb = decode_bytes(wm, wm.decode_from, wm.batch)
+    peak_t, hbm = float(peaks["bf16_tflops"]) * 1e12, float(peaks["hbm_gbs"]) * 1e9
+    ideal_s = fl / peak_t + nb / hbm
+    attend_bytes = nb - (wm.batch - wm.decode_from) * 2 * wm.num_kv_heads * wm.head_dim * 2
+    return {
+        "workload": wm.name, "ms_per_step": round(step_ms, 4),
+        "chunk_flops": fl, "decode_bytes": nb,
+        "roofline_frac": round(ideal_s / (step_ms * 1e-3), 4),
+        "roofline_peaks": f"bf16_tflops and hbm_gbs ({peak_kind})",
+        "parts_ms": {"chunk_prepare": round(pp, 4), "chunk_attention": round(pa, 4),
+                     "decode_append": round(da, 4), "decode_attention": round(dd, 4)},
+        "chunk_attention_tflops": round(fl / (pa * 1e-3) / 1e12, 2),
+        "decode_attention_gbs": round(attend_bytes / (dd * 1e-3) / 1e9, 1),
+        "gpu_launches": mm["launches"],
+    }
+
+
 def run_ours(args):
     import torch
 
@@ -425,6 +455,10 @@ def run_ours(args):
             "gpu_launches": md["launches"],
         }
         line["gpu_launches"] += md["launches"]
+    if not args.no_mixed:
+        line["mixed"] = measure_mixed(gen.ALL[args.mixed_workload], args, device, torch, dist_on, peaks,
+                                      peak_kind)
+        line["gpu_launches"] += line["mixed"]["gpu_launches"]
     if rank == 0 and world == 1 and not args.no_cpu:
         flops_s, dt, desc, cores, _ = cpu_oracle_rate(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(flops_s / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,

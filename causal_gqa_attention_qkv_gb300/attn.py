@@ -33,7 +33,12 @@ class AttnKV(ctypes.Structure):
                 ("num_slots", ctypes.c_int64), ("slot_base", ctypes.c_void_p),
                 ("cache_lens", ctypes.c_void_p), ("slot_capacity", ctypes.c_void_p),
                 ("page_table", ctypes.c_void_p), ("page_size", ctypes.c_int32),
-                ("pages_per_req", ctypes.c_int32)]
+                ("pages_per_req", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
+                ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
+
+
+ATTN_KV_BF16 = 0
+ATTN_KV_E4M3 = 1
 
 
 class AttnError(RuntimeError):
@@ -103,18 +108,22 @@ def config(num_q_heads: int, num_kv_heads: int, head_dim: int, rms_eps: float = 
 class KVCache:
     """Device tensors of one layer's KV cache (see attn_kv_t)."""
 
-    k_cache: torch.Tensor       # bf16 [num_slots, Hkv, D]
-    v_cache: torch.Tensor       # bf16 [num_slots, Hkv, D]
+    k_cache: torch.Tensor       # bf16, or uint8 E4M3 codes, [num_slots, Hkv, D]
+    v_cache: torch.Tensor       # same type and shape as k_cache
     slot_base: torch.Tensor     # int64 [B] (contiguous layout)
     cache_lens: torch.Tensor    # int32 [B]
     slot_capacity: torch.Tensor  # int32 [B]
     page_table: torch.Tensor | None = None  # int32 [B, pages_per_req] (paged layout)
     page_size: int = 0
+    k_scale: float = 1.0        # E4M3 caches: entry = code * scale
+    v_scale: float = 1.0
 
     def struct(self) -> AttnKV:
+        fp8 = self.k_cache.dtype == torch.uint8
         for name in ("k_cache", "v_cache"):
             t = getattr(self, name)
-            assert t.dtype == torch.bfloat16 and t.is_contiguous() and t.is_cuda, name
+            assert t.dtype == (torch.uint8 if fp8 else torch.bfloat16), name
+            assert t.is_contiguous() and t.is_cuda, name
         assert self.slot_base.dtype == torch.int64 and self.slot_base.is_contiguous()
         assert self.cache_lens.dtype == torch.int32 and self.cache_lens.is_contiguous()
         assert self.slot_capacity.dtype == torch.int32 and self.slot_capacity.is_contiguous()
@@ -125,7 +134,8 @@ class KVCache:
             pt, ps, ppr = self.page_table.data_ptr(), int(self.page_size), int(self.page_table.shape[1])
         return AttnKV(self.k_cache.data_ptr(), self.v_cache.data_ptr(), self.k_cache.shape[0],
                       self.slot_base.data_ptr(), self.cache_lens.data_ptr(),
-                      self.slot_capacity.data_ptr(), pt, ps, ppr)
+                      self.slot_capacity.data_ptr(), pt, ps, ppr,
+                      ATTN_KV_E4M3 if fp8 else ATTN_KV_BF16, float(self.k_scale), float(self.v_scale))
 
 
 def decode_max_splits(B: int, num_kv_heads: int, max_kv_len: int) -> int:

@@ -27,15 +27,22 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return g_encode;
 }
 
-int encode_cache_map(void* base, int64_t num_slots, int Hkv, int D, int box_rows, CUtensorMap* m) {
+// bf16 cache: boxes of 64 (d) x 1 (head) x box_rows, 128-byte swizzled.
+// E4M3 cache (one byte per entry): boxes of D x 1 x box_rows, 128-byte
+// swizzled for D = 128, unswizzled 64-byte rows for D = 64.
+int encode_cache_map(void* base, int64_t num_slots, int Hkv, int D, int box_rows, bool f8,
+                     CUtensorMap* m) {
   auto enc = encoder();
   if (!enc) return -1;
+  const cuuint64_t es = f8 ? 1 : 2;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)num_slots};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
-  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+  cuuint64_t strides[2] = {(cuuint64_t)D * es, (cuuint64_t)Hkv * D * es};
+  cuuint32_t box[3] = {f8 ? (cuuint32_t)D : 64u, 1, (cuuint32_t)box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  const CUtensorMapSwizzle sw =
+      (!f8 || D == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+  CUresult r = enc(m, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base,
+                   dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : -1;
 }
@@ -63,6 +70,13 @@ int check_kv(const attn_kv_t* kv) {
     return ATTN_EINVAL;
   }
   if (kv->num_slots <= 0 || kv->num_slots >= (int64_t(1) << 31)) return ATTN_EINVAL;
+  if (kv->kv_dtype == ATTN_KV_E4M3) {
+    if (!(kv->k_scale > 0.f) || !(kv->v_scale > 0.f) || std::isinf(kv->k_scale) ||
+        std::isinf(kv->v_scale))
+      return ATTN_EINVAL;
+  } else if (kv->kv_dtype != ATTN_KV_BF16) {
+    return ATTN_EINVAL;
+  }
   if ((reinterpret_cast<uintptr_t>(kv->k_cache) | reinterpret_cast<uintptr_t>(kv->v_cache)) & 15)
     return ATTN_EINVAL;
   return ATTN_OK;
@@ -122,8 +136,9 @@ int make_qkv_map(const void* qkv, int N, int Htot, int D, int G, int BT, CUtenso
 }
 
 int make_cache_maps(const attn_kv_t& kv, int Hkv, int D, int box_rows, CacheMaps* maps) {
-  if (encode_cache_map(kv.k_cache, kv.num_slots, Hkv, D, box_rows, &maps->k) != 0) return -1;
-  if (encode_cache_map(kv.v_cache, kv.num_slots, Hkv, D, box_rows, &maps->v) != 0) return -1;
+  const bool f8 = kv.kv_dtype == ATTN_KV_E4M3;
+  if (encode_cache_map(kv.k_cache, kv.num_slots, Hkv, D, box_rows, f8, &maps->k) != 0) return -1;
+  if (encode_cache_map(kv.v_cache, kv.num_slots, Hkv, D, box_rows, f8, &maps->v) != 0) return -1;
   return 0;
 }
 
@@ -256,6 +271,7 @@ int attn_prefill_prepare(const attn_config_t* cfg, const void* qkv, const void* 
                          void* stream) {
   int rc = check_common(cfg, kv, qkv, q_norm_w, q_out);
   if (rc) return rc;
+  if (kv->kv_dtype != ATTN_KV_BF16) return ATTN_EINVAL;  // prefill reads bf16 caches only
   if (!k_norm_w || !aligned16(k_norm_w)) return ATTN_EINVAL;
   if (!cu_seqlens || B < 0 || N < 0) return ATTN_EINVAL;
   if (!ws_ok(workspace, ws_bytes, kWsHeader)) return ATTN_EWORKSPACE;
@@ -270,6 +286,7 @@ int attn_prefill_attend(const attn_config_t* cfg, const void* q, const int32_t* 
                         void* workspace, size_t ws_bytes, void* stream) {
   int rc = check_common(cfg, kv, q, q, out);
   if (rc) return rc;
+  if (kv->kv_dtype != ATTN_KV_BF16) return ATTN_EINVAL;  // prefill reads bf16 caches only
   if (!cu_seqlens || B < 0 || N < 0 || max_seqlen < 0) return ATTN_EINVAL;
   if (!ws_ok(workspace, ws_bytes, kWsHeader)) return ATTN_EWORKSPACE;
   if ((rc = check_device())) return rc;
@@ -284,6 +301,7 @@ int attn_prefill(const attn_config_t* cfg, const void* qkv, const void* q_norm_w
                  size_t ws_bytes, void* stream) {
   int rc = check_common(cfg, kv, qkv, q_norm_w, out);
   if (rc) return rc;
+  if (kv->kv_dtype != ATTN_KV_BF16) return ATTN_EINVAL;  // prefill reads bf16 caches only
   if (!k_norm_w || !aligned16(k_norm_w)) return ATTN_EINVAL;
   if (!cu_seqlens || B < 0 || N < 0 || max_seqlen < 0) return ATTN_EINVAL;
   if (!ws_ok(workspace, ws_bytes, kWsHeader + q_stage_bytes(cfg, N))) return ATTN_EWORKSPACE;

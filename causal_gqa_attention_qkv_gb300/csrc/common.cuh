@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -28,6 +29,37 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---------------------------------------------------------------- f16 and E4M3
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Four E4M3 codes (byte i = element i) -> two f16 pairs: lo = elements 0, 1,
+// hi = elements 2, 3 (first element in the low half).  Exact: every E4M3
+// value is an f16 value.
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+// E4M3 codes of two fp32 values, first in the low byte: round to nearest
+// even, magnitudes beyond 448 clamped to 448.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Byte permute: result byte i = byte sel_i of the pair (a = bytes 0-3, b = 4-7).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
 }
 
 // ---------------------------------------------------------------- status
@@ -181,6 +213,30 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// D = A * B + D, m16n8k16, f16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_f16_16816(float* d, const uint32_t* a, uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+      " {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -267,6 +323,65 @@ __device__ __forceinline__ void q_row_frags(const uint16_t* row, bool valid, con
   for (int ks = 0; ks < D / 16; ++ks) {
     frag[ks][0] = pack_bf16(x[ks][0], x[ks][1]);
     frag[ks][1] = pack_bf16(x[ks][2], x[ks][3]);
+  }
+}
+
+// One query row normalised and rotated, as f16 A fragments in the layout
+// the E4M3 decode kernel reads keys in: quad member c = lane & 3 holds the
+// columns [c D/4, (c+1) D/4), frag[ks][0] = columns c D/4 + 4ks + {0,1} and
+// frag[ks][1] = c D/4 + 4ks + {2,3} (the dot product does not depend on
+// which k slot a column occupies, as long as query and key agree).  The
+// RMSNorm sum is a quad reduction; the RoPE partner column (D/2 away) sits
+// in quad member c ^ 2.  All 32 lanes must call this; rows with
+// valid == false yield zeros.
+template <int D>
+__device__ __forceinline__ void q_row_frags_quarters(const uint16_t* row, bool valid,
+                                                     const uint16_t* w, float eps, float pos,
+                                                     const RopeFreqs& fr,
+                                                     uint32_t (&frag)[D / 16][2]) {
+  constexpr int Q = D / 4;  // columns per quad member
+  const int c = threadIdx.x & 3;
+  float x[Q];
+  float ss = 0.f;
+#pragma unroll
+  for (int v = 0; v < Q / 8; ++v) {
+    const uint4 u = valid ? __ldg(reinterpret_cast<const uint4*>(row + c * Q + 8 * v)) : make_uint4(0, 0, 0, 0);
+    const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[8 * v + 2 * j] = bf16_lo(uw[j]);
+      x[8 * v + 2 * j + 1] = bf16_hi(uw[j]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < Q; ++i) ss = fmaf(x[i], x[i], ss);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+  const float inv = rsqrtf(ss * (1.0f / D) + eps);
+#pragma unroll
+  for (int v = 0; v < Q / 8; ++v) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(w + c * Q + 8 * v));
+    const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[8 * v + 2 * j] = bf16_lo(uw[j]) * (x[8 * v + 2 * j] * inv);
+      x[8 * v + 2 * j + 1] = bf16_hi(uw[j]) * (x[8 * v + 2 * j + 1] * inv);
+    }
+  }
+  const bool first_half = c < 2;
+#pragma unroll
+  for (int e = 0; e < Q; ++e) {
+    const int i = (c & 1) * Q + e;  // rotation pair index < D/2
+    float cs, sn;
+    rope_angle(pos, fr.hi[i], fr.lo[i], fr, &cs, &sn);
+    const float other = __shfl_xor_sync(0xffffffffu, x[e], 2);
+    // first half: x_i c - x_{i+D/2} s; second half: x_{i+D/2} c + x_i s
+    x[e] = first_half ? x[e] * cs - other * sn : x[e] * cs + other * sn;
+  }
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    frag[ks][0] = pack_f16(x[4 * ks], x[4 * ks + 1]);
+    frag[ks][1] = pack_f16(x[4 * ks + 2], x[4 * ks + 3]);
   }
 }
 

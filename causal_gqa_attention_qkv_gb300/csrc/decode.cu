@@ -33,28 +33,45 @@ struct DecodePar {
   KvIndex kv;
   int32_t* status;
   int32_t Hq, G, split_len, max_splits;
-  float scale_log2;  // log2(e) / sqrt(D)
+  float scale_log2;  // log2(e) / sqrt(D), times k_scale for an E4M3 cache
+  float v_scale;     // 1, or v_scale for an E4M3 cache
 };
 
-template <int D>
+// One K or V tile: 64 keys.  bf16: D / 64 boxes of 64 rows x 128 bytes
+// (128-byte swizzled).  E4M3: one box of 64 rows x D bytes, 128-byte
+// swizzled when D = 128, plain rows of 64 bytes when D = 64.
+template <int D, bool F8>
 struct DecodeLayout {
-  static constexpr int kRegions = D / 64;                        // 128-byte column blocks
-  static constexpr int kRegionBytes = kKeysPerTile * 128;        // 64 rows x 128 B
-  static constexpr int kTileBytes = kRegions * kRegionBytes;     // 64 keys x D
+  static constexpr int kRegions = F8 ? 1 : D / 64;
+  static constexpr int kRegionBytes = kKeysPerTile * (F8 ? D : 128);
+  static constexpr int kTileBytes = kRegions * kRegionBytes;     // 64 keys x D entries
   static constexpr int kStageBytes = 2 * kTileBytes;             // K + V
   static constexpr int kBarOffset = kStages * kStageBytes;
   static constexpr int kSmemBytes = kBarOffset + 2 * kStages * 8 + 1024;  // + alignment slack
 };
 
+// Byte offset of 16-byte chunk `chunk` of key row `key` in an E4M3 tile.
+template <int D>
+__device__ __forceinline__ uint32_t f8_off(uint32_t key, uint32_t chunk) {
+  return D == 128 ? sw128(key, chunk) : key * (uint32_t)D + (chunk << 4);
+}
+
 __device__ __forceinline__ void named_sync_consumers() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
-template <int D>
+// F8: the cache holds E4M3 codes.  The tiles are converted to f16 in
+// registers (exact) and the products run as f16 mma.sync.  Each lane then
+// reads contiguous bytes: for Q.K^T, quad member c takes the columns
+// [c D/4, (c+1) D/4) of its key row (the query fragments use the same column
+// order); for P.V, lane (g, c) takes columns [g D/8, (g+1) D/8) of its four
+// keys 2c, 2c+1, 2c+8, 2c+9, byte-interleaved in pairs of keys, so n-tile t
+// of the output holds column g D/8 + t.
+template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads)
     decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const DecodePar p) {
-  using Lay = DecodeLayout<D>;
+  using Lay = DecodeLayout<D, F8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::kBarOffset);
@@ -109,7 +126,7 @@ __global__ void __launch_bounds__(kThreads)
           slot = 0;
         }
 #pragma unroll
-        for (int rg = 0; rg < Lay::kRegions; ++rg) {
+        for (int rg = 0; rg < Lay::kRegions; ++rg) {  // x: 64 bf16 (128 B) per box, or 0
           tma_load_3d(kt + rg * Lay::kRegionBytes, &kmap, &full[st], rg * 64, kh, (int)slot);
           tma_load_3d(vt + rg * Lay::kRegionBytes, &vmap, &full[st], rg * 64, kh, (int)slot);
         }
@@ -131,8 +148,13 @@ __global__ void __launch_bounds__(kThreads)
   const int h0 = kh * G;
   const int qrow = lane >> 2;  // A/C fragment row of this thread (rows >= G are padding)
   uint32_t qa[D / 16][2];  // rows 0-7 of the A fragment; rows 8-15 are zero
-  q_row_frags<D>(p.qkv + (int64_t)b * p.W + (int64_t)(h0 + min(qrow, G - 1)) * D, qrow < G,
-                 p.q_norm_w, p.eps, (float)r.cached, p.freqs, qa);
+  if constexpr (F8)
+    q_row_frags_quarters<D>(p.qkv + (int64_t)b * p.W + (int64_t)(h0 + min(qrow, G - 1)) * D, qrow < G,
+                            p.q_norm_w, p.eps, (float)r.cached, p.freqs, qa);
+  else
+    q_row_frags<D>(p.qkv + (int64_t)b * p.W + (int64_t)(h0 + min(qrow, G - 1)) * D, qrow < G,
+                   p.q_norm_w, p.eps, (float)r.cached, p.freqs, qa);
+  const int qc = lane & 3;  // quad member
   float o[D / 8][4];
 #pragma unroll
   for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
@@ -148,16 +170,36 @@ __global__ void __launch_bounds__(kThreads)
     const uint32_t kb = smem_u32(smem + st * Lay::kStageBytes);
     const uint32_t vb = kb + Lay::kTileBytes;
     float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    if constexpr (F8) {
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      const int mi = lane >> 3;
-      const int key = warp * 16 + (mi >> 1) * 8 + (lane & 7);
-      const int chunk = 2 * ks + (mi & 1);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(kb + (chunk >> 3) * Lay::kRegionBytes + sw128(key, chunk & 7), b0, b1, b2, b3);
-      const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
-      mma_bf16_16816(s[0], a, b0, b1);
-      mma_bf16_16816(s[1], a, b2, b3);
+      for (int nt = 0; nt < 2; ++nt) {
+        const int key = warp * 16 + nt * 8 + qrow;
+#pragma unroll
+        for (int hc = 0; hc < D / 64; ++hc) {
+          const uint4 raw = lds128(kb + f8_off<D>(key, qc * (D / 64) + hc));
+          const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t b0, b1;
+            e4m3x4_to_f16(wv[j], b0, b1);
+            const int ks = 4 * hc + j;
+            const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
+            mma_f16_16816(s[nt], a, b0, b1);
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const int mi = lane >> 3;
+        const int key = warp * 16 + (mi >> 1) * 8 + (lane & 7);
+        const int chunk = 2 * ks + (mi & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kb + (chunk >> 3) * Lay::kRegionBytes + sw128(key, chunk & 7), b0, b1, b2, b3);
+        const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
+        mma_bf16_16816(s[0], a, b0, b1);
+        mma_bf16_16816(s[1], a, b2, b3);
+      }
     }
     const int kfirst = k0 + i * kKeysPerTile + warp * 16;  // first key of this warp's slice
     const int kA = kfirst + 2 * (lane & 3);
@@ -185,11 +227,45 @@ __global__ void __launch_bounds__(kThreads)
       o[dt][0] *= alpha;
       o[dt][1] *= alpha;
     }
-    const uint32_t pa[4] = {pack_bf16(pr[0], pr[1]), 0u, pack_bf16(pr[2], pr[3]), 0u};
     // keys past the end hold arbitrary bits: zero their V entries so 0 * NaN cannot occur
     const bool partial = kfirst + 16 > k1;
     const uint32_t mA = (kA < k1 ? 0x0000FFFFu : 0u) | (kA + 1 < k1 ? 0xFFFF0000u : 0u);
     const uint32_t mB = (kA + 8 < k1 ? 0x0000FFFFu : 0u) | (kA + 9 < k1 ? 0xFFFF0000u : 0u);
+    if constexpr (F8) {
+      const uint32_t pa[4] = {pack_f16(pr[0], pr[1]), 0u, pack_f16(pr[2], pr[3]), 0u};
+      // keys 2c, 2c+1 (b0) and 2c+8, 2c+9 (b1) of this warp's 16, columns [g D/8, (g+1) D/8)
+      constexpr int W = D / 32;  // 32-bit words per key and lane
+      uint32_t kv4[4][W];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int key = warp * 16 + 2 * qc + (q4 & 1) + (q4 >> 1) * 8;
+        if constexpr (D == 128) {
+          const uint4 v = lds128(vb + f8_off<D>(key, qrow));
+          kv4[q4][0] = v.x; kv4[q4][1] = v.y; kv4[q4][2] = v.z; kv4[q4][3] = v.w;
+        } else {
+          const uint2 v = lds64(vb + key * (uint32_t)D + qrow * 8);
+          kv4[q4][0] = v.x; kv4[q4][1] = v.y;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < W; ++j) {
+        // byte pairs (key a, key b) per column: columns 4j + 0..3 of this lane
+        uint32_t b0[4], b1[4];
+        e4m3x4_to_f16(prmt(kv4[0][j], kv4[1][j], 0x5140u), b0[0], b0[1]);
+        e4m3x4_to_f16(prmt(kv4[0][j], kv4[1][j], 0x7362u), b0[2], b0[3]);
+        e4m3x4_to_f16(prmt(kv4[2][j], kv4[3][j], 0x5140u), b1[0], b1[1]);
+        e4m3x4_to_f16(prmt(kv4[2][j], kv4[3][j], 0x7362u), b1[2], b1[3]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (partial) {
+            b0[e] &= mA;
+            b1[e] &= mB;
+          }
+          mma_f16_16816(o[4 * j + e], pa, b0[e], b1[e]);
+        }
+      }
+    } else {
+    const uint32_t pa[4] = {pack_bf16(pr[0], pr[1]), 0u, pack_bf16(pr[2], pr[3]), 0u};
 #pragma unroll
     for (int dp = 0; dp < D / 16; ++dp) {
       const int mi = lane >> 3;
@@ -203,6 +279,7 @@ __global__ void __launch_bounds__(kThreads)
       }
       mma_bf16_16816(o[2 * dp], pa, b0, b1);
       mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
+    }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
@@ -221,11 +298,16 @@ __global__ void __launch_bounds__(kThreads)
   float* mm = mo + kConsumerWarps * G * D;                      // [warps][G]
   float* ml = mm + kConsumerWarps * G;                          // [warps][G]
   if (qrow < G) {
-    float* dst = mo + (warp * G + qrow) * D + 2 * (lane & 3);
+    float* dst = mo + (warp * G + qrow) * D;
 #pragma unroll
     for (int dt = 0; dt < D / 8; ++dt) {
-      dst[dt * 8] = o[dt][0];
-      dst[dt * 8 + 1] = o[dt][1];
+      if constexpr (F8) {  // n-tile dt, column n: output column n D/8 + dt
+        dst[(2 * qc) * (D / 8) + dt] = o[dt][0] * p.v_scale;
+        dst[(2 * qc + 1) * (D / 8) + dt] = o[dt][1] * p.v_scale;
+      } else {
+        dst[dt * 8 + 2 * qc] = o[dt][0];
+        dst[dt * 8 + 2 * qc + 1] = o[dt][1];
+      }
     }
     if ((lane & 3) == 0) {
       mm[warp * G + qrow] = m;
@@ -282,9 +364,9 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodePar p) {
   p.out[row * D + d] = *reinterpret_cast<const uint16_t*>(&v);
 }
 
-template <int D>
+template <int D, bool F8>
 int launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
-  using Lay = DecodeLayout<D>;
+  using Lay = DecodeLayout<D, F8>;
   CacheMaps maps;
   if (make_cache_maps(a.kv, a.cfg.num_kv_heads, D, kKeysPerTile, &maps) != 0) return ATTN_ELAUNCH;
   DecodePar p;
@@ -302,12 +384,13 @@ int launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
   p.G = a.cfg.num_q_heads / a.cfg.num_kv_heads;
   p.split_len = a.split_len;
   p.max_splits = a.max_splits;
-  p.scale_log2 = 1.4426950408889634f / sqrtf((float)D);
-  if (cudaFuncSetAttribute(decode_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  p.scale_log2 = 1.4426950408889634f / sqrtf((float)D) * (F8 ? a.kv.k_scale : 1.0f);
+  p.v_scale = F8 ? a.kv.v_scale : 1.0f;
+  if (cudaFuncSetAttribute(decode_split_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Lay::kSmemBytes) != cudaSuccess)
     return ATTN_ELAUNCH;
   dim3 grid(a.max_splits, a.cfg.num_kv_heads, a.B);
-  decode_split_kernel<D><<<grid, kThreads, Lay::kSmemBytes, stream>>>(maps.k, maps.v, p);
+  decode_split_kernel<D, F8><<<grid, kThreads, Lay::kSmemBytes, stream>>>(maps.k, maps.v, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
   if (a.max_splits > 1) {
     decode_combine_kernel<D><<<dim3(a.cfg.num_q_heads, a.B), D, 0, stream>>>(p);
@@ -332,7 +415,9 @@ int decode_split_len(int B, int Hkv, int max_kv_len, int* max_splits) {
 
 int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (a.B <= 0) return ATTN_OK;
-  return a.cfg.head_dim == 128 ? launch_decode_t<128>(a, stream) : launch_decode_t<64>(a, stream);
+  const bool f8 = a.kv.kv_dtype == ATTN_KV_E4M3;
+  if (a.cfg.head_dim == 128) return f8 ? launch_decode_t<128, true>(a, stream) : launch_decode_t<128, false>(a, stream);
+  return f8 ? launch_decode_t<64, true>(a, stream) : launch_decode_t<64, false>(a, stream);
 }
 
 }  // namespace gb300

@@ -31,8 +31,9 @@ struct ProloguePar {
   const uint16_t* __restrict__ k_norm_w;   // [D] bf16
   uint16_t* __restrict__ q_out;            // [N, Hq, D] bf16 or NULL
   const int32_t* cu_seqlens;  // [B+1] or NULL: token b is request b (decode)
-  uint16_t* __restrict__ k_cache;
-  uint16_t* __restrict__ v_cache;
+  void* __restrict__ k_cache;  // bf16, or E4M3 codes (one byte per entry)
+  void* __restrict__ v_cache;
+  float inv_k, inv_v;          // E4M3: fp32(1 / scale), rounded on the host
   KvIndex kv;
   int32_t* status;
   int32_t B, N, Hq, Hkv;
@@ -40,13 +41,31 @@ struct ProloguePar {
   RopeFreqs freqs;
 };
 
+// E4M3 codes of eight fp32 values times an fp32 factor (the product rounded
+// to fp32 first, as the cache format states), element i in byte i.
+__device__ __forceinline__ uint2 e4m3x8(const float (&y)[8], float r) {
+  uint2 v;
+  v.x = e4m3x2(__fmul_rn(y[0], r), __fmul_rn(y[1], r)) | (e4m3x2(__fmul_rn(y[2], r), __fmul_rn(y[3], r)) << 16);
+  v.y = e4m3x2(__fmul_rn(y[4], r), __fmul_rn(y[5], r)) | (e4m3x2(__fmul_rn(y[6], r), __fmul_rn(y[7], r)) << 16);
+  return v;
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4& raw, float (&y)[8]) {
+  const uint32_t* rw = reinterpret_cast<const uint32_t*>(&raw);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    y[2 * e] = bf16_lo(rw[e]);
+    y[2 * e + 1] = bf16_hi(rw[e]);
+  }
+}
+
 // One warp per token.  The token's head vectors (D bf16 = D/8 lanes x 16 bytes)
 // are taken HPI = 32 / (D/8) at a time, lane l holding 8 values of head
 // hd0 + j*HPI + l / (D/8): each load instruction reads 512 contiguous bytes of
 // the qkv row and each store writes whole head vectors.  cos/sin of the
 // token's D/2 rotation angles are computed once (D/64 per lane) and handed to
-// the lanes that need them with shuffles.
-template <int D>
+// the lanes that need them with shuffles.  F8: the cache holds E4M3 codes.
+template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) kv_append_kernel(const ProloguePar p) {
   constexpr int L = D / 8;      // lanes per head vector
   constexpr int HPI = 32 / L;   // head vectors per warp-wide step
@@ -164,8 +183,16 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) kv_append_kernel(const P
       // steps made only of V heads: bit copies into the cache
       const bool step_all_v = hd0 + (base + k) * HPI >= p.Hq + p.Hkv;
       if (step_all_v) {
-        if (live && ok == 2)
-          *reinterpret_cast<uint4*>(p.v_cache + cache_row + (int64_t)(hd - p.Hq - p.Hkv) * D) = raw[k];
+        if (live && ok == 2) {
+          const int64_t e0 = cache_row + (int64_t)(hd - p.Hq - p.Hkv) * D;
+          if constexpr (F8) {
+            float y[8];
+            unpack_bf16x8(raw[k], y);
+            *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.v_cache) + e0) = e4m3x8(y, p.inv_v);
+          } else {
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.v_cache) + e0) = raw[k];
+          }
+        }
         continue;
       }
       float x[8];
@@ -183,21 +210,30 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) kv_append_kernel(const P
       const float inv = rsqrtf(ss * (1.0f / D) + p.eps);
 #pragma unroll
       for (int e = 0; e < 8; ++e) x[e] = (is_q ? qw[e] : kw[e]) * (x[e] * inv);
-      uint32_t o[4];
+      float rot[8];
 #pragma unroll
-      for (int e = 0; e < 8; e += 2) {
-        const float q0 = __shfl_xor_sync(0xffffffffu, x[e], L / 2);
-        const float q1 = __shfl_xor_sync(0xffffffffu, x[e + 1], L / 2);
-        o[e / 2] = pack_bf16(fmaf(q0, sn[e], x[e] * cs[e]), fmaf(q1, sn[e + 1], x[e + 1] * cs[e + 1]));
+      for (int e = 0; e < 8; ++e) {
+        const float other = __shfl_xor_sync(0xffffffffu, x[e], L / 2);
+        rot[e] = fmaf(other, sn[e], x[e] * cs[e]);
       }
-      const uint4 v4 = is_v ? raw[k] : make_uint4(o[0], o[1], o[2], o[3]);
       if (!live) continue;
+      const int64_t e0 = cache_row + (int64_t)(hd - (is_v ? p.Hq + p.Hkv : p.Hq)) * D;
+      if (F8 && !is_q) {
+        if (ok == 2) {
+          float y[8];
+          if (is_v) unpack_bf16x8(raw[k], y);
+          uint8_t* dst = static_cast<uint8_t*>(is_v ? p.v_cache : p.k_cache) + e0;
+          *reinterpret_cast<uint2*>(dst) = e4m3x8(is_v ? y : rot, is_v ? p.inv_v : p.inv_k);
+        }
+        continue;
+      }
+      const uint4 v4 = is_v ? raw[k]
+                            : make_uint4(pack_bf16(rot[0], rot[1]), pack_bf16(rot[2], rot[3]),
+                                         pack_bf16(rot[4], rot[5]), pack_bf16(rot[6], rot[7]));
       if (is_q) {
         *reinterpret_cast<uint4*>(q_row + (int64_t)hd * D) = v4;
       } else if (ok == 2) {
-        uint16_t* dst = is_v ? p.v_cache + cache_row + (int64_t)(hd - p.Hq - p.Hkv) * D
-                             : p.k_cache + cache_row + (int64_t)(hd - p.Hq) * D;
-        *reinterpret_cast<uint4*>(dst) = v4;
+        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(is_v ? p.v_cache : p.k_cache) + e0) = v4;
       }
     }
   }
@@ -213,8 +249,11 @@ cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t stream) {
   p.k_norm_w = static_cast<const uint16_t*>(a.k_norm_w);
   p.q_out = static_cast<uint16_t*>(a.q_out);
   p.cu_seqlens = a.cu_seqlens;
-  p.k_cache = static_cast<uint16_t*>(a.kv.k_cache);
-  p.v_cache = static_cast<uint16_t*>(a.kv.v_cache);
+  p.k_cache = a.kv.k_cache;
+  p.v_cache = a.kv.v_cache;
+  const bool f8 = a.kv.kv_dtype == ATTN_KV_E4M3;
+  p.inv_k = f8 ? 1.0f / a.kv.k_scale : 1.0f;
+  p.inv_v = f8 ? 1.0f / a.kv.v_scale : 1.0f;
   p.kv = kv_index(a.kv);
   p.status = a.status;
   p.B = a.B;
@@ -224,10 +263,13 @@ cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t stream) {
   p.eps = a.cfg.rms_eps;
   p.freqs = a.freqs;
   const dim3 grid((a.N + kWarpsPerBlock - 1) / kWarpsPerBlock);
-  if (a.cfg.head_dim == 128)
-    kv_append_kernel<128><<<grid, kThreads, 0, stream>>>(p);
-  else
-    kv_append_kernel<64><<<grid, kThreads, 0, stream>>>(p);
+  if (a.cfg.head_dim == 128) {
+    if (f8) kv_append_kernel<128, true><<<grid, kThreads, 0, stream>>>(p);
+    else kv_append_kernel<128, false><<<grid, kThreads, 0, stream>>>(p);
+  } else {
+    if (f8) kv_append_kernel<64, true><<<grid, kThreads, 0, stream>>>(p);
+    else kv_append_kernel<64, false><<<grid, kThreads, 0, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 

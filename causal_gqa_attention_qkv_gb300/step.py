@@ -71,15 +71,16 @@ def upload(w, host: dict, device="cuda") -> DeviceStep:
     slot_base, cache_lens, cap = dev(host["slot_base"]), dev(host["cache_lens"]), dev(host["slot_capacity"])
     pt = dev(host["page_table"]) if host.get("page_table") is not None else None
     ps = int(host.get("page_size", 0))
+    scales = (float(host.get("k_scale", 1.0)), float(host.get("v_scale", 1.0)))
     part = lambda t, lo, hi: None if t is None else t[lo:hi].contiguous()
     kv_p = kv_d = None
     if df > 0:
         kv_p = attn.KVCache(k_cache, v_cache, slot_base[:df], cache_lens[:df], cap[:df],
-                            part(pt, 0, df), ps)
+                            part(pt, 0, df), ps, *scales)
     if df < w.batch:
         assert all(n == 1 for n in w.new_lens[df:]), "decode requests take one token each"
         kv_d = attn.KVCache(k_cache, v_cache, slot_base[df:], cache_lens[df:], cap[df:],
-                            part(pt, df, w.batch), ps)
+                            part(pt, df, w.batch), ps, *scales)
     N = w.num_tokens
     out = torch.zeros((N, w.num_q_heads * w.head_dim), dtype=torch.bfloat16, device=device)
     max_kv = max([c + n for c, n in zip(w.cache_lens, w.new_lens)] + [1])

@@ -88,7 +88,22 @@ typedef struct attn_config {
  * <= pages_per_req * page_size), else the request is skipped
  * (ATTN_STATUS_CAPACITY).  cache_lens[b] is read, never written: the caller
  * advances it after the call (the transformer-basics "Prefill vs Decode"
- * cache goes 0 -> 12 -> 13). */
+ * cache goes 0 -> 12 -> 13).
+ *
+ * Element type (kv_dtype):
+ *   ATTN_KV_BF16 (0): bf16 entries; k_scale and v_scale are ignored.
+ *   ATTN_KV_E4M3 (1): one byte per entry, OCP FP8 E4M3 (bias 7, largest
+ *     finite 448, no infinity), each cache 1-byte [num_slots, Hkv, D].  The
+ *     stored byte of a value x is e4m3(x * r) with r = 1 / scale rounded to
+ *     fp32 on the host and x * r an fp32 product: round to nearest even,
+ *     magnitudes above 448 clamped to 448.  x is the fp32 normed and rotated K
+ *     (the value the bf16 cache rounds to bf16) or the bf16 V input.  Readers
+ *     take byte * scale.  k_scale and v_scale are finite and > 0.  This
+ *     element type halves the bytes a decode step reads (concept chapter
+ *     section 4.3: decode is bound by memory bandwidth; its section 2.6 lists
+ *     KV-cache reduction among the modern variants); attn_decode,
+ *     attn_decode_attend, attn_decode_static_scratch and attn_kv_append take
+ *     it, the prefill calls answer ATTN_EINVAL. */
 typedef struct attn_kv {
   void* k_cache;
   void* v_cache;
@@ -99,7 +114,12 @@ typedef struct attn_kv {
   const int32_t* page_table;    /* NULL, or [B, pages_per_req] page numbers (paged layout) */
   int32_t page_size;            /* slots per page (paged layout) */
   int32_t pages_per_req;        /* row length of page_table (paged layout) */
+  int32_t kv_dtype;             /* ATTN_KV_BF16 or ATTN_KV_E4M3 */
+  float k_scale;                /* E4M3: K entry = byte * k_scale */
+  float v_scale;                /* E4M3: V entry = byte * v_scale */
 } attn_kv_t;
+
+enum { ATTN_KV_BF16 = 0, ATTN_KV_E4M3 = 1 };
 
 enum {
   ATTN_OK = 0,

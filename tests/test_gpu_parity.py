@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from causal_gqa_attention_qkv_gb300 import inputs as gen
-from parity_util import check_caches, check_out, gather_rows, run_and_compare
+from parity_util import check_caches, check_out, gather_rows, run_and_compare, written_slots
 
 pytestmark = pytest.mark.gpu
 
@@ -96,6 +96,50 @@ def test_paged_cache_all_rows_and_same_bits_as_contiguous(ps, hq, hkv, d, lens, 
     contiguous.run()
     torch.cuda.synchronize()
     assert torch.equal(paged.out.view(torch.int16), contiguous.out.view(torch.int16))
+
+
+# One-byte (E4M3) caches: the append codes K and V, decode reads the codes.
+# Scales: the generator's defaults, a power of two, and one small enough that
+# some K and V products pass 448 and are clamped.
+E4M3_DECODE = [
+    # (Hq, Hkv, D, cached lens, page size, k_scale, v_scale)
+    (32, 8, 128, [0, 1, 63, 64, 65, 255, 256, 257, 1000, 3000], 0, 0.04, 0.02),
+    (4, 2, 64, [0, 5, 511, 2047], 0, 0.04, 0.02),
+    (16, 2, 128, [7, 129, 4000], 64, 2.0 ** -5, 2.0 ** -6),
+    (8, 8, 64, [12, 300, 64], 128, 0.04, 0.02),
+    (32, 8, 128, [33, 900], 0, 0.003, 0.004),
+]
+
+
+@pytest.mark.parametrize("hq,hkv,d,cache,ps,ks,vs", E4M3_DECODE)
+def test_e4m3_cache_decode_all_rows(hq, hkv, d, cache, ps, ks, vs):
+    w = gen.custom(f"e4m3_{hq}_{hkv}_{d}_{ps}", hq, hkv, d, [1] * len(cache), cache, seed=len(cache) + d + ps,
+                   decode_from=0)
+    host = gen.make_inputs(w, page_size=ps, kv_dtype="e4m3", k_scale=ks, v_scale=vs)
+    res = run_and_compare(w, host)
+    if ks == 0.003:  # some products passed 448 and were clamped (on both sides: the caches match)
+        slots = written_slots(host)
+        for name in ("k_cache", "v_cache"):
+            assert ((res["ref"][name].numpy()[slots] & 0x7F) == 0x7E).any(), name
+
+
+def test_e4m3_decode_static_scratch_matches_workspace_decode():
+    from causal_gqa_attention_qkv_gb300 import attn, step
+    w = gen.custom("e4m3_static", 32, 8, 128, [1] * 6, [5, 70, 700, 2000, 64, 4095], seed=91, decode_from=0)
+    host = gen.make_inputs(w, kv_dtype="e4m3")
+    a = step.upload(w, host)
+    a.run()
+    b = step.upload(w, host)
+    attn.decode_static_scratch(b.cfg, b.qkv, b.q_norm_w, b.k_norm_w, b.max_cache_len, b.kv_decode, b.out)
+    torch.cuda.synchronize()
+    assert a.status() == 0 and b.status() == 0
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+    assert torch.equal(a.k_cache, b.k_cache) and torch.equal(a.v_cache, b.v_cache)
+
+
+def test_e4m3_full_decode_batch_all_rows():
+    w = gen.decode_batch()
+    run_and_compare(w, gen.make_inputs(w, kv_dtype="e4m3"))
 
 
 def test_empty_calls_are_no_ops():
