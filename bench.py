@@ -70,15 +70,15 @@ def prefill_flops(w, lo=0, hi=None) -> float:
     return 4.0 * w.head_dim * w.num_q_heads * w.attended_pairs(lo, hi)
 
 
-def decode_bytes(w, lo=0, hi=None) -> float:
+def decode_bytes(w, lo=0, hi=None, entry_bytes=2) -> float:
     """Algorithmic HBM bytes of the decode requests [lo, hi): cache read
-    (K and V of the c_b cached entries), the new token's qkv row, the K/V
-    append and the output row."""
+    (K and V of the c_b cached entries, entry_bytes each: 2 for bf16, 1 for
+    E4M3), the new token's qkv row, the K/V append and the output row."""
     hi = w.batch if hi is None else hi
-    D, Hq, Hkv = w.head_dim, w.num_q_heads, w.num_kv_heads
+    D, Hq, Hkv, e = w.head_dim, w.num_q_heads, w.num_kv_heads, entry_bytes
     total = 0
     for c in w.cache_lens[lo:hi]:
-        total += 2 * c * Hkv * D * 2 + w.qkv_width * 2 + 2 * Hkv * D * 2 + Hq * D * 2
+        total += 2 * c * Hkv * D * e + w.qkv_width * 2 + 2 * Hkv * D * e + Hq * D * 2
     return float(total)
 
 
@@ -232,12 +232,12 @@ class Timed:
             ev[4].record()
 
 
-def measure(w, steps, warmup, device, torch, dist_on, page_size=0):
+def measure(w, steps, warmup, device, torch, dist_on, page_size=0, kv_dtype="bf16"):
     """Device-timed steps of workload w.  Returns per-part mean ms and more."""
     from causal_gqa_attention_qkv_gb300 import inputs as gen
     from causal_gqa_attention_qkv_gb300 import step
 
-    host = gen.make_inputs(w, page_size=page_size)
+    host = gen.make_inputs(w, page_size=page_size, kv_dtype=kv_dtype)
     ds = step.upload(w, host, device=device)
     B_dec = w.batch - w.decode_from
     ds.decode_cu = torch.arange(B_dec + 1, dtype=torch.int32, device=device)
@@ -355,6 +355,31 @@ def cpu_oracle_decode_rate(w, budget_s: float):
     return decode_bytes(w, 0, nb), dt, f"all heads of the first {nb} requests of {w.name}", oracle.num_threads()
 
 
+def measure_decode(wd, args, device, torch, dist_on, peaks, peak_kind, kv_dtype, entry_bytes,
+                   traffic_kernel) -> dict:
+    """The decode step (append + split-KV attention + combine) of workload wd
+    over a cache of bf16 or E4M3 entries.  Bytes count the entries as stored."""
+    md = measure(wd, args.steps, args.warmup, device, torch, dist_on, args.page_size, kv_dtype)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    dms, dattend = max_over_ranks([md["ms"]["step"], md["ms"]["decode_attend"]], device)
+    nbytes = decode_bytes(wd, entry_bytes=entry_bytes)
+    attend_bytes = nbytes - wd.batch * 2 * wd.num_kv_heads * wd.head_dim * entry_bytes  # no append write
+    hbm = float(peaks["hbm_gbs"])
+    return {
+        "value": round(whole_job_rate(nbytes, world, dms) / 1e9, 1), "unit": "GB/s",
+        "ms_per_step": round(dms, 4), "workload": wd.name, "kv_dtype": kv_dtype, "bytes_per_step": nbytes,
+        "parts_ms": {"kv_append": round(md["ms"]["decode_append"], 4),
+                     "decode_attention": round(dattend, 4)},
+        "roofline": {"bound": "hbm", "kernel": "decode split-KV + combine",
+                     "achieved": round(attend_bytes / (dattend * 1e-3) / 1e9, 1), "peak": hbm,
+                     "peak_kind": f"hbm_gbs ({peak_kind})", "unit": "GB/s",
+                     "frac": round(attend_bytes / (dattend * 1e-3) / 1e9 / hbm, 4),
+                     "frac_of_8tbs_nominal": round(attend_bytes / (dattend * 1e-3) / 8e12, 4),
+                     "traffic": recorded_traffic(traffic_kernel, source_sha("decode.cu", "common.cuh"))},
+        "gpu_launches": md["launches"],
+    }
+
+
 def measure_mixed(wm, args, device, torch, dist_on, peaks, peak_kind) -> dict:
     """One serving step that mixes prefill chunks (on top of cached prefixes)
     with decode rows, issued back to back on one stream: the chunks'
@@ -436,25 +461,10 @@ def run_ours(args):
     }
     if not args.no_decode:
         wd = gen.ALL[args.decode_workload]
-        md = measure(wd, args.steps, args.warmup, device, torch, dist_on, args.page_size)
-        dms, dattend = max_over_ranks([md["ms"]["step"], md["ms"]["decode_attend"]], device)
-        nbytes = decode_bytes(wd)
-        attend_bytes = nbytes - wd.batch * 2 * wd.num_kv_heads * wd.head_dim * 2  # no append write
-        hbm = float(peaks["hbm_gbs"])
-        line["decode"] = {
-            "value": round(whole_job_rate(nbytes, world, dms) / 1e9, 1), "unit": "GB/s",
-            "ms_per_step": round(dms, 4), "workload": wd.name, "bytes_per_step": nbytes,
-            "parts_ms": {"kv_append": round(md["ms"]["decode_append"], 4),
-                         "decode_attention": round(dattend, 4)},
-            "roofline": {"bound": "hbm", "kernel": "decode split-KV + combine",
-                         "achieved": round(attend_bytes / (dattend * 1e-3) / 1e9, 1), "peak": hbm,
-                         "peak_kind": f"hbm_gbs ({peak_kind})", "unit": "GB/s",
-                         "frac": round(attend_bytes / (dattend * 1e-3) / 1e9 / hbm, 4),
-                         "frac_of_8tbs_nominal": round(attend_bytes / (dattend * 1e-3) / 8e12, 4),
-                         "traffic": recorded_traffic("decode_split", source_sha("decode.cu", "common.cuh"))},
-            "gpu_launches": md["launches"],
-        }
-        line["gpu_launches"] += md["launches"]
+        for key, kvd, eb, kname in (("decode", "bf16", 2, "decode_split"),
+                                    ("decode_e4m3", "e4m3", 1, "decode_split_e4m3")):
+            line[key] = measure_decode(wd, args, device, torch, dist_on, peaks, peak_kind, kvd, eb, kname)
+            line["gpu_launches"] += line[key]["gpu_launches"]
     if not args.no_mixed:
         line["mixed"] = measure_mixed(gen.ALL[args.mixed_workload], args, device, torch, dist_on, peaks,
                                       peak_kind)

@@ -16,7 +16,12 @@ namespace gb300 {
 namespace {
 
 constexpr int kKeysPerTile = 64;
-constexpr int kStages = 3;
+#ifndef DECODE_F8_STAGES
+#define DECODE_F8_STAGES 6
+#endif
+#ifndef DECODE_F8_MIN_BLOCKS
+#define DECODE_F8_MIN_BLOCKS 2  // resident CTAs per SM the registers must allow
+#endif
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 
@@ -45,6 +50,9 @@ struct DecodeLayout {
   static constexpr int kRegions = F8 ? 1 : D / 64;
   static constexpr int kRegionBytes = kKeysPerTile * (F8 ? D : 128);
   static constexpr int kTileBytes = kRegions * kRegionBytes;     // 64 keys x D entries
+  // bytes in flight per CTA: 3 x 32 KB (bf16, D = 128) or 6 x 16 KB (E4M3),
+  // two CTAs per SM either way
+  static constexpr int kStages = F8 ? DECODE_F8_STAGES : 3;
   static constexpr int kStageBytes = 2 * kTileBytes;             // K + V
   static constexpr int kBarOffset = kStages * kStageBytes;
   static constexpr int kSmemBytes = kBarOffset + 2 * kStages * 8 + 1024;  // + alignment slack
@@ -68,14 +76,14 @@ __device__ __forceinline__ void named_sync_consumers() {
 // keys 2c, 2c+1, 2c+8, 2c+9, byte-interleaved in pairs of keys, so n-tile t
 // of the output holds column g D/8 + t.
 template <int D, bool F8>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, F8 ? DECODE_F8_MIN_BLOCKS : 0)
     decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const DecodePar p) {
   using Lay = DecodeLayout<D, F8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::kBarOffset);
-  uint64_t* empty = full + kStages;
+  uint64_t* empty = full + Lay::kStages;
   __shared__ int s_abort;       // written by the producer only
   __shared__ int s_cons_abort;  // written by consumers only, read after their barrier
 
@@ -95,7 +103,7 @@ __global__ void __launch_bounds__(kThreads)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < Lay::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
@@ -111,8 +119,8 @@ __global__ void __launch_bounds__(kThreads)
       prefetch_tmap(&vmap);
       int issued = 0;
       for (int i = 0; i < ntiles; ++i) {
-        const int st = i % kStages;
-        if (i >= kStages && !mbar_wait(&empty[st], ((i / kStages) - 1) & 1)) {
+        const int st = i % Lay::kStages;
+        if (i >= Lay::kStages && !mbar_wait(&empty[st], ((i / Lay::kStages) - 1) & 1)) {
           s_abort = 1;
           break;
         }
@@ -135,8 +143,8 @@ __global__ void __launch_bounds__(kThreads)
       __syncwarp(1);
       // After a failed wait, let the copies still in flight land before exit.
       if (s_abort) {
-        for (int i = max(0, issued - kStages); i < issued; ++i)
-          (void)mbar_wait(&full[i % kStages], (i / kStages) & 1);
+        for (int i = max(0, issued - Lay::kStages); i < issued; ++i)
+          (void)mbar_wait(&full[i % Lay::kStages], (i / Lay::kStages) & 1);
         set_status(p.status, ATTN_STATUS_TIMEOUT);
       }
     }
@@ -161,34 +169,139 @@ __global__ void __launch_bounds__(kThreads)
   float m = kNegInf, l = 0.f;
   bool ok = true;
 
+  if constexpr (F8) {
+    // Two 64-key tiles per pass: twice the independent work between two
+    // waits, and one softmax reduction and one O rescale per 128 keys.
+    constexpr int S = Lay::kStages;
+    for (int i = 0; i < ntiles; i += 2) {
+      const bool two = i + 1 < ntiles;
+      const int st0 = i % S, st1 = (i + 1) % S;
+      if (!mbar_wait(&full[st0], (i / S) & 1) || (two && !mbar_wait(&full[st1], ((i + 1) / S) & 1))) {
+        ok = false;
+        break;
+      }
+      // Without a second tile, stage st1 holds an older tile or nothing and no
+      // copy is in flight into it; all of its keys lie past k1 and are masked.
+      const uint32_t kb[2] = {smem_u32(smem + st0 * Lay::kStageBytes), smem_u32(smem + st1 * Lay::kStageBytes)};
+      uint32_t kw[2][2][D / 16];  // [tile][key octet][word]
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int hc = 0; hc < D / 64; ++hc) {
+            const uint4 raw = lds128(kb[t] + f8_off<D>(warp * 16 + nt * 8 + qrow, qc * (D / 64) + hc));
+            kw[t][nt][4 * hc] = raw.x;
+            kw[t][nt][4 * hc + 1] = raw.y;
+            kw[t][nt][4 * hc + 2] = raw.z;
+            kw[t][nt][4 * hc + 3] = raw.w;
+          }
+      float s[2][2][4];
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) s[t][nt][0] = s[t][nt][1] = s[t][nt][2] = s[t][nt][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            uint32_t b0, b1;
+            e4m3x4_to_f16(kw[t][nt][ks], b0, b1);
+            mma_f16_16816(s[t][nt], a, b0, b1);
+          }
+      }
+      float sc[2][4];
+      int kA[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        kA[t] = k0 + (i + t) * kKeysPerTile + warp * 16 + 2 * qc;
+        sc[t][0] = kA[t] < k1 ? s[t][0][0] * p.scale_log2 : kNegInf;
+        sc[t][1] = kA[t] + 1 < k1 ? s[t][0][1] * p.scale_log2 : kNegInf;
+        sc[t][2] = kA[t] + 8 < k1 ? s[t][1][0] * p.scale_log2 : kNegInf;
+        sc[t][3] = kA[t] + 9 < k1 ? s[t][1][1] * p.scale_log2 : kNegInf;
+      }
+      float mx = fmaxf(fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[0][2], sc[0][3])),
+                       fmaxf(fmaxf(sc[1][0], sc[1][1]), fmaxf(sc[1][2], sc[1][3])));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m, mx);
+      const float m_use = m_new == kNegInf ? 0.f : m_new;
+      const float alpha = fast_exp2(m - m_use);
+      float pr[2][4], rs = 0.f;
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          pr[t][e] = fast_exp2(sc[t][e] - m_use);
+          rs += pr[t][e];
+        }
+      l = l * alpha + rs;
+      m = m_new;
+#pragma unroll
+      for (int dt = 0; dt < D / 8; ++dt) {
+        o[dt][0] *= alpha;
+        o[dt][1] *= alpha;
+      }
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const uint32_t pa[4] = {pack_f16(pr[t][0], pr[t][1]), 0u, pack_f16(pr[t][2], pr[t][3]), 0u};
+        // keys past the end hold arbitrary bits: zero their V entries so 0 * NaN cannot occur
+        const bool partial = kA[t] - 2 * qc + 16 > k1;
+        const uint32_t mA = (kA[t] < k1 ? 0x0000FFFFu : 0u) | (kA[t] + 1 < k1 ? 0xFFFF0000u : 0u);
+        const uint32_t mB = (kA[t] + 8 < k1 ? 0x0000FFFFu : 0u) | (kA[t] + 9 < k1 ? 0xFFFF0000u : 0u);
+        const uint32_t vb = kb[t] + Lay::kTileBytes;
+        // keys 2c, 2c+1 (b0) and 2c+8, 2c+9 (b1) of this warp's 16, columns [g D/8, (g+1) D/8)
+        constexpr int W = D / 32;  // 32-bit words per key and lane
+        uint32_t kv4[4][W];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int key = warp * 16 + 2 * qc + (q4 & 1) + (q4 >> 1) * 8;
+          if constexpr (D == 128) {
+            const uint4 v = lds128(vb + f8_off<D>(key, qrow));
+            kv4[q4][0] = v.x; kv4[q4][1] = v.y; kv4[q4][2] = v.z; kv4[q4][3] = v.w;
+          } else {
+            const uint2 v = lds64(vb + key * (uint32_t)D + qrow * 8);
+            kv4[q4][0] = v.x; kv4[q4][1] = v.y;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < W; ++j) {
+          // byte pairs (key a, key b) per column: columns 4j + 0..3 of this lane
+          uint32_t b0[4], b1[4];
+          e4m3x4_to_f16(prmt(kv4[0][j], kv4[1][j], 0x5140u), b0[0], b0[1]);
+          e4m3x4_to_f16(prmt(kv4[0][j], kv4[1][j], 0x7362u), b0[2], b0[3]);
+          e4m3x4_to_f16(prmt(kv4[2][j], kv4[3][j], 0x5140u), b1[0], b1[1]);
+          e4m3x4_to_f16(prmt(kv4[2][j], kv4[3][j], 0x7362u), b1[2], b1[3]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (partial) {
+              b0[e] &= mA;
+              b1[e] &= mB;
+            }
+            mma_f16_16816(o[4 * j + e], pa, b0[e], b1[e]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&empty[st0]);
+        if (two) mbar_arrive(&empty[st1]);
+      }
+    }
+  } else
   for (int i = 0; i < ntiles; ++i) {
-    const int st = i % kStages;
-    if (!mbar_wait(&full[st], (i / kStages) & 1)) {
+    const int st = i % Lay::kStages;
+    if (!mbar_wait(&full[st], (i / Lay::kStages) & 1)) {
       ok = false;
       break;
     }
     const uint32_t kb = smem_u32(smem + st * Lay::kStageBytes);
     const uint32_t vb = kb + Lay::kTileBytes;
     float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    if constexpr (F8) {
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int key = warp * 16 + nt * 8 + qrow;
-#pragma unroll
-        for (int hc = 0; hc < D / 64; ++hc) {
-          const uint4 raw = lds128(kb + f8_off<D>(key, qc * (D / 64) + hc));
-          const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t b0, b1;
-            e4m3x4_to_f16(wv[j], b0, b1);
-            const int ks = 4 * hc + j;
-            const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
-            mma_f16_16816(s[nt], a, b0, b1);
-          }
-        }
-      }
-    } else {
+    {
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         const int mi = lane >> 3;
@@ -231,40 +344,7 @@ __global__ void __launch_bounds__(kThreads)
     const bool partial = kfirst + 16 > k1;
     const uint32_t mA = (kA < k1 ? 0x0000FFFFu : 0u) | (kA + 1 < k1 ? 0xFFFF0000u : 0u);
     const uint32_t mB = (kA + 8 < k1 ? 0x0000FFFFu : 0u) | (kA + 9 < k1 ? 0xFFFF0000u : 0u);
-    if constexpr (F8) {
-      const uint32_t pa[4] = {pack_f16(pr[0], pr[1]), 0u, pack_f16(pr[2], pr[3]), 0u};
-      // keys 2c, 2c+1 (b0) and 2c+8, 2c+9 (b1) of this warp's 16, columns [g D/8, (g+1) D/8)
-      constexpr int W = D / 32;  // 32-bit words per key and lane
-      uint32_t kv4[4][W];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int key = warp * 16 + 2 * qc + (q4 & 1) + (q4 >> 1) * 8;
-        if constexpr (D == 128) {
-          const uint4 v = lds128(vb + f8_off<D>(key, qrow));
-          kv4[q4][0] = v.x; kv4[q4][1] = v.y; kv4[q4][2] = v.z; kv4[q4][3] = v.w;
-        } else {
-          const uint2 v = lds64(vb + key * (uint32_t)D + qrow * 8);
-          kv4[q4][0] = v.x; kv4[q4][1] = v.y;
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < W; ++j) {
-        // byte pairs (key a, key b) per column: columns 4j + 0..3 of this lane
-        uint32_t b0[4], b1[4];
-        e4m3x4_to_f16(prmt(kv4[0][j], kv4[1][j], 0x5140u), b0[0], b0[1]);
-        e4m3x4_to_f16(prmt(kv4[0][j], kv4[1][j], 0x7362u), b0[2], b0[3]);
-        e4m3x4_to_f16(prmt(kv4[2][j], kv4[3][j], 0x5140u), b1[0], b1[1]);
-        e4m3x4_to_f16(prmt(kv4[2][j], kv4[3][j], 0x7362u), b1[2], b1[3]);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (partial) {
-            b0[e] &= mA;
-            b1[e] &= mB;
-          }
-          mma_f16_16816(o[4 * j + e], pa, b0[e], b1[e]);
-        }
-      }
-    } else {
+    {
     const uint32_t pa[4] = {pack_bf16(pr[0], pr[1]), 0u, pack_bf16(pr[2], pr[3]), 0u};
 #pragma unroll
     for (int dp = 0; dp < D / 16; ++dp) {
