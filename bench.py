@@ -459,6 +459,20 @@ def run_ours(args):
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clocks,
     }
+    # the same prefill over a one-byte (E4M3) cache: tiles converted to f16 on chip
+    me = measure(w, args.steps, args.warmup, device, torch, dist_on, args.page_size, "e4m3")
+    e_step, e_attend = max_over_ranks([me["ms"]["step"], me["ms"]["prefill_attend"]], device)
+    line["prefill_e4m3"] = {
+        "value": round(whole_job_rate(flops, world, e_step) / 1e12, 3), "unit": "TFLOP/s",
+        "ms_per_step": round(e_step, 4), "kv_dtype": "e4m3",
+        "parts_ms": {"prologue": round(me["ms"]["prefill_append"], 4), "prefill_attention": round(e_attend, 4)},
+        "roofline": {"bound": "tensor", "kernel": "prefill attention (E4M3 cache)",
+                     "achieved": round(flops / (e_attend * 1e-3) / 1e12, 3), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(flops / (e_attend * 1e-3) / 1e12 / peak, 4)},
+        "gpu_launches": me["launches"],
+    }
+    line["gpu_launches"] += me["launches"]
+    del me
     if not args.no_decode:
         wd = gen.ALL[args.decode_workload]
         for key, kvd, eb, kname in (("decode", "bf16", 2, "decode_split"),

@@ -271,7 +271,6 @@ int attn_prefill_prepare(const attn_config_t* cfg, const void* qkv, const void* 
                          void* stream) {
   int rc = check_common(cfg, kv, qkv, q_norm_w, q_out);
   if (rc) return rc;
-  if (kv->kv_dtype != ATTN_KV_BF16) return ATTN_EINVAL;  // prefill reads bf16 caches only
   if (!k_norm_w || !aligned16(k_norm_w)) return ATTN_EINVAL;
   if (!cu_seqlens || B < 0 || N < 0) return ATTN_EINVAL;
   if (!ws_ok(workspace, ws_bytes, kWsHeader)) return ATTN_EWORKSPACE;
@@ -286,7 +285,6 @@ int attn_prefill_attend(const attn_config_t* cfg, const void* q, const int32_t* 
                         void* workspace, size_t ws_bytes, void* stream) {
   int rc = check_common(cfg, kv, q, q, out);
   if (rc) return rc;
-  if (kv->kv_dtype != ATTN_KV_BF16) return ATTN_EINVAL;  // prefill reads bf16 caches only
   if (!cu_seqlens || B < 0 || N < 0 || max_seqlen < 0) return ATTN_EINVAL;
   if (!ws_ok(workspace, ws_bytes, kWsHeader)) return ATTN_EWORKSPACE;
   if ((rc = check_device())) return rc;
@@ -301,7 +299,6 @@ int attn_prefill(const attn_config_t* cfg, const void* qkv, const void* q_norm_w
                  size_t ws_bytes, void* stream) {
   int rc = check_common(cfg, kv, qkv, q_norm_w, out);
   if (rc) return rc;
-  if (kv->kv_dtype != ATTN_KV_BF16) return ATTN_EINVAL;  // prefill reads bf16 caches only
   if (!k_norm_w || !aligned16(k_norm_w)) return ATTN_EINVAL;
   if (!cu_seqlens || B < 0 || N < 0 || max_seqlen < 0) return ATTN_EINVAL;
   if (!ws_ok(workspace, ws_bytes, kWsHeader + q_stage_bytes(cfg, N))) return ATTN_EWORKSPACE;

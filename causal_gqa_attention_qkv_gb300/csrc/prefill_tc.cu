@@ -21,11 +21,12 @@
 //   warps 0-3   softmax of Q tile A, warps 4-7 softmax of Q tile B: thread r
 //               of a warpgroup owns row r = TMEM lane r of its tile.  Per KV
 //               tile: read S from TMEM, mask, online softmax in fp32 (exp2
-//               domain), P (bf16) written over S in TMEM, O rescaled in TMEM
+//               domain), P (bf16; f16 with F8) written over S in TMEM, O rescaled in TMEM
 //               when the reference max moves; per item: O / l -> out.
-//   warp 8      TMA: K tiles (2-stage ring of 128 keys, across items).
+//   warp 8      TMA: K tiles (2-stage ring of 128 keys, across items); with
+//               F8 the whole warp also converts each tile to f16.
 //   warp 9      MMA issuer (one thread) and TMEM owner.
-//   warp 10     TMA: V tiles (2-stage ring).
+//   warp 10     TMA: V tiles (2-stage ring; converted the same way with F8).
 //   warp 11     claims items; TMA: the item's two Q tiles (one buffer each).
 // Each producer runs in a warp of its own: a thread waiting for a free stage
 // may be suspended, and diverged lanes of one warp do not run independently.
@@ -37,6 +38,13 @@
 // runs and the other way round.  Because the tensor-core operations of one
 // thread complete in issue order, S_X(j+1) being complete means P.V_X(j) is
 // complete: the softmax may rescale O_X as soon as it sees S_X(j+1).
+//
+// E4M3 caches (F8): the K and V warps copy each 128-key tile of codes into
+// the last 128 x D bytes of its stage and convert it there, all 32 lanes, to
+// the f16 tile layout the bf16 path gets from TMA (every E4M3 value is an
+// f16 value); Q arrives in f16, P is packed to f16, the products run as
+// kind::f16 with f16 operands, and the cache scales multiply the scores
+// (k_scale) and the output (v_scale).
 #include "kernels.cuh"
 #include "tcgen05.cuh"
 
@@ -70,7 +78,8 @@ struct TcPar {
   int32_t* status;
   int32_t* work;  // [0]: next item to claim, [1]: CTAs finished
   uint16_t* out;
-  float scale_log2;  // log2(e) / sqrt(D)
+  float scale_log2;  // log2(e) / sqrt(D), times k_scale for an E4M3 cache
+  float v_scale;     // 1, or v_scale for an E4M3 cache
   int32_t Hq, Hkv, log2G, log2BT, N, B, max_seqlen;
   int32_t num_vitems;  // rounds x B x Hkv, rounds = ceil(max_seqlen / (2 x 128/G))
 };
@@ -107,7 +116,9 @@ enum Bar {
   kODoneA, kODoneB,                           // the item's last P.V_X complete
   kMmaDone,
   kItemFull0, kItemFree0 = kItemFull0 + kRing,  // item ring: slot written / read by every role
-  kBarCount = kItemFree0 + kRing
+  kKLand0 = kItemFree0 + kRing,               // E4M3: a stage's codes have landed
+  kVLand0 = kKLand0 + kKStages,
+  kBarCount = kVLand0 + kVStages
 };
 static_assert(kBarCount <= TcLayout<64>::kNumBars, "barriers");
 
@@ -309,6 +320,82 @@ __device__ void produce_kv(const TcPar& p, const SeqInfo* seq_tab, const int* ri
   for (int t = max(0, g - stages); t < g; ++t) (void)mbar_wait(&bars[full0 + t % stages], (t / stages) & 1);
 }
 
+// The same ring for an E4M3 cache, run by the whole warp: lane 0 copies each
+// tile of codes (128 keys x D bytes) into the last 128 x D bytes of its stage;
+// then every lane converts key rows to the f16 tile layout and lane 0
+// releases the stage to the tensor cores.
+template <int D>
+__device__ void produce_kv_f8(const TcPar& p, const SeqInfo* seq_tab, const int* ring,
+                              const CUtensorMap* map, uint8_t* smem, uint64_t* bars, int base,
+                              int full0, int empty0, int land0, int stages, bool& ok) {
+  using Lay = TcLayout<D>;
+  const int lane = threadIdx.x & 31;
+  constexpr int kCodeBytes = kKeys * D;
+  if (lane == 0) prefetch_tmap(map);
+  ItemWalk w;
+  w.start(p, seq_tab, ring, bars, true, ok);
+  int g = 0, issued = 0;
+  while (w.valid && ok) {
+    for (int j = 0; j < w.it.nk; ++j, ++g) {
+      const int st = g % stages;
+      if (!__all_sync(0xffffffffu, g < stages || mbar_wait(&bars[empty0 + st], (g / stages - 1) & 1))) {
+        ok = false;
+        break;
+      }
+      uint8_t* dst = smem + base + st * Lay::kTile;
+      uint8_t* land = dst + Lay::kTile - kCodeBytes;  // 1024-aligned
+      uint64_t* bar = &bars[land0 + st];
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar, kCodeBytes);
+        if (!p.half_boxes) {
+          tma_load_3d(land, map, bar, 0, w.it.kh, kv_row(p, w.it, j * kKeys));
+        } else {
+          const int pos1 = min(j * kKeys + 64, ((w.it.kv_total - 1) >> 6) << 6);
+          tma_load_3d(land, map, bar, 0, w.it.kh, kv_row(p, w.it, j * kKeys));
+          tma_load_3d(land + kCodeBytes / 2, map, bar, 0, w.it.kh, kv_row(p, w.it, pos1));
+        }
+      }
+      ++issued;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar, (g / stages) & 1))) { ok = false; break; }
+      // Lane l converts key rows l, l + 32, l + 64, l + 96: codes of row r
+      // (D bytes, 128-byte swizzled when D = 128) -> f16 row r of each
+      // 64-column region.  Each row is read whole before any lane writes:
+      // for D = 64 later f16 rows cover other lanes' code rows.
+      const uint32_t tile = smem_u32(dst), codes = smem_u32(land);
+#pragma unroll 1
+      for (int i = 0; i < kKeys / 32; ++i) {
+        const uint32_t r = (uint32_t)(lane + 32 * i);
+        uint4 c[D / 16];
+#pragma unroll
+        for (int ch = 0; ch < D / 16; ++ch)
+          c[ch] = lds128(codes + (D == 128 ? sw128(r, ch) : r * (uint32_t)D + ch * 16));
+        __syncwarp();
+#pragma unroll
+        for (int ch = 0; ch < D / 16; ++ch) {
+          uint4 lo, hi;  // codes 16ch .. 16ch + 7 and 16ch + 8 .. 16ch + 15 as f16
+          e4m3x4_to_f16(c[ch].x, lo.x, lo.y);
+          e4m3x4_to_f16(c[ch].y, lo.z, lo.w);
+          e4m3x4_to_f16(c[ch].z, hi.x, hi.y);
+          e4m3x4_to_f16(c[ch].w, hi.z, hi.w);
+          const uint32_t region = tile + (uint32_t)((2 * ch) >> 3) * kRegionBytes;
+          sts128(region + sw128(r, (2 * ch) & 7), lo);
+          sts128(region + sw128(r, (2 * ch + 1) & 7), hi);
+        }
+        __syncwarp();
+      }
+      tc::fence_proxy_async();  // the f16 tile is visible to the tensor cores
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[full0 + st]);
+    }
+    if (!ok) break;
+    w.next(p, ok);
+  }
+  // Every copy issued has landed before the CTA may exit.
+  if (lane == 0)
+    for (int t = max(0, issued - stages); t < issued; ++t)
+      (void)mbar_wait(&bars[land0 + t % stages], (t / stages) & 1);
+}
+
 // Claims items from the counter in the workspace, publishes each to the
 // ring and loads its two Q tiles.  The last slot written holds -1.
 template <int D>
@@ -346,12 +433,14 @@ __device__ void produce_q(const TcPar& p, const SeqInfo* seq_tab, int* ring,
     for (int x = 0; x < 2; ++x) (void)mbar_wait(&bars[kQFullA + x], (k - 1) & 1);
 }
 
-template <int D>
+template <int D, bool F8>
 __device__ void issue_mma(const TcPar& p, const SeqInfo* seq_tab, const int* ring, uint32_t sbase,
                           uint32_t tmem, uint64_t* bars, bool& ok) {
   using Lay = TcLayout<D>;
-  constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kTileRows, kKeys, false);
-  constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kTileRows, D, true);
+  constexpr uint32_t idesc_s = F8 ? tc::idesc_f16_f32(kTileRows, kKeys, false)
+                                  : tc::idesc_bf16_f32(kTileRows, kKeys, false);
+  constexpr uint32_t idesc_o = F8 ? tc::idesc_f16_f32(kTileRows, D, true)
+                                  : tc::idesc_bf16_f32(kTileRows, D, true);
   // S_X = Q_X K(st)^T into TMEM columns 128 x
   auto qk = [&](int x, int st) {
     const uint64_t qd = tc::sdesc_sw128(sbase + Lay::kQ + x * Lay::kTile, 16, 1024);
@@ -431,7 +520,7 @@ __device__ void issue_mma(const TcPar& p, const SeqInfo* seq_tab, const int* rin
 }
 
 // Softmax and epilogue of Q tile x (0: A, 1: B) of every item.
-template <int D>
+template <int D, bool F8>
 __device__ void softmax_tile(const TcPar& p, const SeqInfo* seq_tab, const int* ring, uint32_t sbase,
                              uint32_t tmem, uint64_t* bars, const CUtensorMap* omap, int x, bool& ok) {
   using Lay = TcLayout<D>;
@@ -533,7 +622,7 @@ __device__ void softmax_tile(const TcPar& p, const SeqInfo* seq_tab, const int* 
           const float p0 = fast_exp2(f2_lo(t));  // exp2(-inf) = 0
           const float p1 = fast_exp2(f2_hi(t));
           acc2[e & 3] = f2_add(acc2[e & 3], f2_pack(p0, p1));
-          pk[e] = pack_bf16(p0, p1);
+          pk[e] = F8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);  // P <= 256: exact range in f16
         }
         tc::st_32x32b_x16(s_tmem + q * 16, pk);
       };
@@ -591,7 +680,7 @@ __device__ void softmax_tile(const TcPar& p, const SeqInfo* seq_tab, const int* 
     if (!wait_warp(&bars[kODoneA + x], k & 1)) { ok = false; break; }
     tc::fence_after();
     {
-      const float inv_l = 1.f / l;
+      const float inv_l = F8 ? p.v_scale / l : 1.f / l;
       // This warp's 32 rows are 32/G whole tokens.  When all of them belong to
       // the sequence they leave through this warp's staging slot (128-byte
       // swizzled, the layout of a 64 d x G heads x 32/G tokens box) by TMA
@@ -649,7 +738,7 @@ __device__ void softmax_tile(const TcPar& p, const SeqInfo* seq_tab, const int* 
   if ((threadIdx.x & 31) == 0) bulk_wait_all();  // every output store has completed
 }
 
-template <int D>
+template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                       const __grid_constant__ CUtensorMap kmap,
@@ -679,10 +768,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&bars[kKFull0 + s], 1);
       mbar_init(&bars[kKEmpty0 + s], 1);
+      mbar_init(&bars[kKLand0 + s], 1);
     }
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(&bars[kVFull0 + s], 1);
       mbar_init(&bars[kVEmpty0 + s], 1);
+      mbar_init(&bars[kVLand0 + s], 1);
     }
     mbar_init(&bars[kMmaDone], 1);
     for (int s = 0; s < kRing; ++s) {
@@ -706,7 +797,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool ok = true;
 
   if (warp < 8) {
-    softmax_tile<D>(p, seq_tab, ring, sbase, tmem, bars, &omap, warp >> 2, ok);
+    softmax_tile<D, F8>(p, seq_tab, ring, sbase, tmem, bars, &omap, warp >> 2, ok);
+  } else if (F8 && warp == kKWarp) {  // the whole warp converts the tiles
+    produce_kv_f8<D>(p, seq_tab, ring, &kmap, smem, bars, Lay::kK, kKFull0, kKEmpty0, kKLand0, kKStages, ok);
+  } else if (F8 && warp == kVWarp) {
+    produce_kv_f8<D>(p, seq_tab, ring, &vmap, smem, bars, Lay::kV, kVFull0, kVEmpty0, kVLand0, kVStages, ok);
   } else {
     if (lane == 0) {
       if (warp == kKWarp)
@@ -716,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       else if (warp == kQWarp)
         produce_q<D>(p, seq_tab, ring, &qmap, smem, bars, ok);
       else
-        issue_mma<D>(p, seq_tab, ring, sbase, tmem, bars, ok);
+        issue_mma<D, F8>(p, seq_tab, ring, sbase, tmem, bars, ok);
     }
   }
   if (!ok) set_status(p.status, ATTN_STATUS_TIMEOUT);
@@ -736,7 +831,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool F8>
 int launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream) {
   using Lay = TcLayout<D>;
   const int Hq = a.cfg.num_q_heads, Hkv = a.cfg.num_kv_heads;
@@ -758,7 +853,8 @@ int launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream) {
   p.status = a.status;
   p.work = a.work;
   p.out = static_cast<uint16_t*>(a.out);
-  p.scale_log2 = 1.4426950408889634f / sqrtf((float)D);
+  p.scale_log2 = 1.4426950408889634f / sqrtf((float)D) * (F8 ? a.kv.k_scale : 1.0f);
+  p.v_scale = F8 ? a.kv.v_scale : 1.0f;
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.log2G = log2G;
@@ -774,11 +870,11 @@ int launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream) {
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return ATTN_ELAUNCH;
-  if (cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(prefill_tc_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Lay::kSmemBytes) != cudaSuccess)
     return ATTN_ELAUNCH;
   const int grid = (int)std::min<int64_t>(sms, nv);
-  prefill_tc_kernel<D><<<grid, kThreads, Lay::kSmemBytes, stream>>>(qmap, maps.k, maps.v, omap, p);
+  prefill_tc_kernel<D, F8><<<grid, kThreads, Lay::kSmemBytes, stream>>>(qmap, maps.k, maps.v, omap, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
 }
 
@@ -786,8 +882,10 @@ int launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream) {
 
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   if (a.B <= 0 || a.N <= 0 || a.max_seqlen <= 0) return ATTN_OK;
-  return a.cfg.head_dim == 128 ? launch_prefill_tc_t<128>(a, stream)
-                               : launch_prefill_tc_t<64>(a, stream);
+  const bool f8 = a.kv.kv_dtype == ATTN_KV_E4M3;
+  if (a.cfg.head_dim == 128)
+    return f8 ? launch_prefill_tc_t<128, true>(a, stream) : launch_prefill_tc_t<128, false>(a, stream);
+  return f8 ? launch_prefill_tc_t<64, true>(a, stream) : launch_prefill_tc_t<64, false>(a, stream);
 }
 
 }  // namespace gb300

@@ -227,7 +227,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) kv_append_kernel(const P
         }
         continue;
       }
+      // the prepared Q is f16 next to an E4M3 cache (the prefill kernel's operand type), else bf16
       const uint4 v4 = is_v ? raw[k]
+                       : F8 ? make_uint4(pack_f16(rot[0], rot[1]), pack_f16(rot[2], rot[3]),
+                                         pack_f16(rot[4], rot[5]), pack_f16(rot[6], rot[7]))
                             : make_uint4(pack_bf16(rot[0], rot[1]), pack_bf16(rot[2], rot[3]),
                                          pack_bf16(rot[4], rot[5]), pack_bf16(rot[6], rot[7]));
       if (is_q) {

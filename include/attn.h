@@ -101,9 +101,9 @@ typedef struct attn_config {
  *     take byte * scale.  k_scale and v_scale are finite and > 0.  This
  *     element type halves the bytes a decode step reads (concept chapter
  *     section 4.3: decode is bound by memory bandwidth; its section 2.6 lists
- *     KV-cache reduction among the modern variants); attn_decode,
- *     attn_decode_attend, attn_decode_static_scratch and attn_kv_append take
- *     it, the prefill calls answer ATTN_EINVAL. */
+ *     KV-cache reduction among the modern variants).  Every call takes it;
+ *     next to an E4M3 cache the prepared Q of attn_prefill_prepare /
+ *     attn_prefill_attend is f16 instead of bf16. */
 typedef struct attn_kv {
   void* k_cache;
   void* v_cache;
@@ -165,8 +165,9 @@ ATTN_API int attn_kv_append(const attn_config_t* cfg, const void* qkv, const voi
                    const attn_kv_t* kv, void* workspace, size_t ws_bytes, void* stream);
 
 /* First half of attn_prefill: split qkv, RMSNorm + RoPE on Q and K, append
- * K and V to the cache, and write the prepared (normed, rotated, bf16) Q to
- * q_out [N, Hq, D] (device, caller-owned, 16-byte aligned).  cu_seqlens,
+ * K and V to the cache, and write the prepared (normed, rotated) Q to q_out
+ * [N, Hq, D] (device, caller-owned, 16-byte aligned): bf16, or f16 next to
+ * an E4M3 cache.  cu_seqlens,
  * B, N and kv as for attn_prefill.  Code walkthrough section 3.3; basics
  * "Attention calculation: part 1" (q_norm / k_norm after .view) and "Prefill
  * vs Decode" (past_key_values.update). */

@@ -139,11 +139,9 @@ def test_contiguous_layout_needs_slot_base(lib):
     (1, 0.04, 0.02, True), (1, 0.0, 0.02, False), (1, 0.04, -1.0, False), (1, float("inf"), 0.02, False),
     (1, 0.04, float("nan"), False), (2, 1.0, 1.0, False), (-1, 1.0, 1.0, False), (0, 0.0, 0.0, True)])
 def test_cache_element_type_checked(lib, dtype, ks, vs, ok):
-    """kv_dtype is bf16 (scales ignored) or E4M3 with finite positive scales;
-    E4M3 caches pass the argument checks of the append and decode calls and
-    are refused by the prefill calls.  Everything here fails before any
-    pointer is used: without a GPU the calls that pass the checks stop at the
-    device query (-4 or -5)."""
+    """kv_dtype is bf16 (scales ignored) or E4M3 with finite positive scales,
+    checked by every call before any pointer is used: without a GPU the calls
+    that pass the checks stop at the device query (-4 or -5)."""
     from causal_gqa_attention_qkv_gb300 import attn
     cfg = attn.config(32, 8, 128)
     fake = 1 << 20
@@ -156,8 +154,8 @@ def test_cache_element_type_checked(lib, dtype, ks, vs, ok):
     rc = lib.attn_kv_append(ctypes.byref(cfg), f, f, f, f, 1, 4, k, f, 1 << 20, None)
     assert (rc in past_checks) if ok else rc == -1
     rc = lib.attn_prefill(ctypes.byref(cfg), f, f, f, f, 1, 4, 4, k, f, f, 1 << 20, None)
-    assert (rc in past_checks) if (ok and dtype == 0) else rc == -1
+    assert (rc in past_checks) if ok else rc == -1
     rc = lib.attn_prefill_prepare(ctypes.byref(cfg), f, f, f, f, 1, 4, k, f, f, 1 << 20, None)
-    assert (rc in past_checks) if (ok and dtype == 0) else rc == -1
+    assert (rc in past_checks) if ok else rc == -1
     rc = lib.attn_prefill_attend(ctypes.byref(cfg), f, f, 1, 4, 4, k, f, f, 1 << 20, None)
-    assert (rc in past_checks) if (ok and dtype == 0) else rc == -1
+    assert (rc in past_checks) if ok else rc == -1

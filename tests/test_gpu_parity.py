@@ -123,6 +123,31 @@ def test_e4m3_cache_decode_all_rows(hq, hkv, d, cache, ps, ks, vs):
             assert ((res["ref"][name].numpy()[slots] & 0x7F) == 0x7E).any(), name
 
 
+E4M3_PREFILL = [
+    # (Hq, Hkv, D, new lens, cached lens, page size, decode_from)
+    (32, 8, 128, [300, 77, 513, 129, 1], [0, 200, 64, 1000, 5], 0, 5),
+    (16, 2, 64, [130, 1, 65, 257], [3, 0, 700, 128], 0, 4),
+    (32, 8, 128, [300, 77, 513, 129], [0, 200, 64, 1000], 64, 4),
+    (8, 8, 64, [200, 31], [64, 0], 128, 2),
+    (32, 8, 128, [100, 64, 1, 1, 1], [50, 0, 10, 700, 0], 0, 2),
+]
+
+
+@pytest.mark.parametrize("hq,hkv,d,lens,cache,ps,df", E4M3_PREFILL)
+def test_e4m3_cache_prefill_and_mixed_all_rows(hq, hkv, d, lens, cache, ps, df):
+    """Prefill (and the decode rows of a mixed step) over a one-byte cache:
+    the tiles are converted to f16 in shared memory; every row and both
+    caches against the oracle."""
+    w = gen.custom(f"e4m3p_{hq}_{hkv}_{d}_{ps}_{df}", hq, hkv, d, lens, cache, seed=sum(lens) + d + ps,
+                   decode_from=df)
+    run_and_compare(w, gen.make_inputs(w, page_size=ps, kv_dtype="e4m3"))
+
+
+def test_e4m3_full_qwen3_4b_prefill_sampled():
+    w = gen.qwen3_4b_prefill()
+    run_and_compare(w, gen.make_inputs(w, kv_dtype="e4m3"), rows=_sampled(w, tail=64, count=4096, seed=5))
+
+
 def test_e4m3_decode_static_scratch_matches_workspace_decode():
     from causal_gqa_attention_qkv_gb300 import attn, step
     w = gen.custom("e4m3_static", 32, 8, 128, [1] * 6, [5, 70, 700, 2000, 64, 4095], seed=91, decode_from=0)
