@@ -10,7 +10,8 @@ the passages it follows, in that file's header.
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (brute force from the teaching snippet, closed forms, torch's ``rms_norm``,
 the complex form of RoPE, invariants; the E4M3 codec against torch's
-``float8_e4m3fn`` for every code and for ties).  The RoPE pairing convention
+``float8_e4m3fn`` for every code and for ties; sampling against closed-form
+distributions, scipy's softmax and its limits).  The RoPE pairing convention
 itself (rotate-half) is a reading the pages leave open: parity unpinned for
 that choice, pinned for everything given it.  So is the one-byte cache
 format (E4M3, one scale per cache, code of fp32(x) * fp32(1/scale)): the
@@ -73,6 +74,8 @@ def _load():
         lib.oracle_attention.argtypes = [
             ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, ctypes.c_int, _F, _F, ctypes.c_int, _P,
             _P, _P, _P, ctypes.c_int, ctypes.c_int, _I64, _P, _P, _P, _P]
+        lib.oracle_sample.restype = _I64
+        lib.oracle_sample.argtypes = [_I64, _P, _D, _I64, _D, _D, ctypes.POINTER(_D)]
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -226,6 +229,25 @@ def attention(cfg: dict, k_cache: torch.Tensor, v_cache: torch.Tensor, inputs: d
                          _ptr(sb),
                          _ptr(pt), ps, ppr, R, _ptr(tok), _ptr(head), _ptr(q), _ptr(out))
     return out
+
+
+def sample(logits, temperature, top_k, top_p, uniform):
+    """Tokens chosen from rows of fp32 logits ``[B, V]`` (greedy for
+    temperature <= 0; else temperature, top-k, top-p, inverse-CDF sampling in
+    vocabulary order with ``uniform``).  Returns (tokens int64 [B], margins
+    float64 [B]): a margin is the relative distance of the row's real-valued
+    decisions from a boundary (inf for greedy rows)."""
+    lib = _load()
+    x = np.ascontiguousarray(np.asarray(logits, dtype=np.float32))
+    B, V = x.shape
+    toks = np.zeros(B, dtype=np.int64)
+    margins = np.zeros(B, dtype=np.float64)
+    m = _D()
+    for b in range(B):
+        toks[b] = lib.oracle_sample(V, x[b].ctypes.data_as(_P), float(temperature[b]), int(top_k[b]),
+                                    float(top_p[b]), float(uniform[b]), ctypes.byref(m))
+        margins[b] = m.value
+    return toks, margins
 
 
 def all_rows(num_tokens: int, num_q_heads: int) -> np.ndarray:

@@ -312,6 +312,100 @@ void oracle_attention(int Hq, int Hkv, int D, const void* k_cache, const void* v
   }
 }
 
+/*
+ * Token sampling from one row of logits (concept chapter section 3.2: greedy
+ * decoding, temperature, top-k and top-p; the walkthrough's section 4.3:
+ * greedy batches take the argmax, the others temperature + top-k/top-p).
+ *
+ *   temperature <= 0: greedy, the smallest index holding the largest logit.
+ *   Otherwise the distribution is softmax(logits / temperature) (section
+ *   3.2.2's formula), truncated (section 3.2.3) to the tokens whose logit is
+ *   at least lambda = max(lambda_k, lambda_p):
+ *     top-k (0 < top_k < V): lambda_k = the top_k-th largest logit (ties
+ *       with it are kept);
+ *     top-p (top_p < 1): walking the tokens from the most probable down,
+ *       lambda_p = the logit at which the cumulative probability first
+ *       reaches top_p (tokens of equal logit enter together);
+ *   then renormalised and sampled by the inverse distribution function in
+ *   vocabulary order with the given uniform u in [0, 1): the token is the
+ *   smallest kept index whose cumulative kept probability exceeds u.
+ *
+ * Returns the token.  *margin (not for greedy rows: +inf) is the smallest
+ * relative distance of the row's two real-valued decisions from a boundary:
+ * the top-p crossing (cumulative mass against top_p, as a fraction of the
+ * total) and the sampled position (u against the cumulative kept fractions).
+ * A result whose margin is below the device's rounding error may validly
+ * differ on the device.
+ */
+/* qsort order: larger logit first, then smaller index (one row at a time). */
+static const float* g_sort_logits;
+static int cmp_desc_logit(const void* a, const void* b) {
+  const float* l = g_sort_logits;
+  int64_t i = *(const int64_t*)a, j = *(const int64_t*)b;
+  if (l[i] != l[j]) return l[i] > l[j] ? -1 : 1;
+  return i < j ? -1 : (i > j);
+}
+
+int64_t oracle_sample(int64_t V, const float* logits, double temperature, int64_t top_k,
+                      double top_p, double u, double* margin) {
+  *margin = INFINITY;
+  int64_t arg = 0;
+  for (int64_t i = 1; i < V; ++i)
+    if (logits[i] > logits[arg]) arg = i;
+  if (!(temperature > 0.0)) return arg;
+  double m = (double)logits[arg] / temperature;
+  double* w = malloc(sizeof(double) * (size_t)V);
+  double W = 0.0;
+  for (int64_t i = 0; i < V; ++i) {
+    w[i] = exp((double)logits[i] / temperature - m);
+    W += w[i];
+  }
+  int64_t* order = malloc(sizeof(int64_t) * (size_t)V);
+  for (int64_t i = 0; i < V; ++i) order[i] = i;
+  g_sort_logits = logits;
+  qsort(order, (size_t)V, sizeof(int64_t), cmp_desc_logit);
+  double lambda = -INFINITY;
+  if (top_k > 0 && top_k < V) lambda = logits[order[top_k - 1]];
+  if (top_p < 1.0) {
+    double cum = 0.0, target = top_p * W;
+    for (int64_t n = 0; n < V;) {
+      int64_t e = n;
+      double group = 0.0;
+      while (e < V && logits[order[e]] == logits[order[n]]) group += w[order[e++]];
+      double before = cum;
+      cum += group;
+      if (cum >= target || e == V) {
+        double lp = logits[order[n]];
+        if (lp > lambda) lambda = lp;
+        double d = fmin(cum - target, target - before) / W;
+        if (d < *margin) *margin = d;
+        break;
+      }
+      n = e;
+    }
+  }
+  double S = 0.0;
+  for (int64_t i = 0; i < V; ++i)
+    if (logits[i] >= lambda) S += w[i];
+  double t = u * S, cum = 0.0;
+  int64_t token = -1, last = -1;
+  for (int64_t i = 0; i < V; ++i) {
+    if (!(logits[i] >= lambda)) continue;
+    last = i;
+    double before = cum;
+    cum += w[i];
+    if (w[i] > 0.0) {
+      double d = fmin(fabs(cum - t), fabs(before - t)) / S;
+      if (d < *margin) *margin = d;
+    }
+    if (token < 0 && cum > t) token = i;
+  }
+  if (token < 0) token = last;
+  free(w);
+  free(order);
+  return token;
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

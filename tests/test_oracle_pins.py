@@ -424,3 +424,73 @@ def test_e4m3_cache_store_rule_and_reads():
             a8 = oracle.attention(cfg, r8["k_cache"], r8["v_cache"], h8, rows, r8["q"])
             ab = oracle.attention(cfg, hbf["k_cache"], hbf["v_cache"], hbf, rows, r8["q"])
             assert np.array_equal(a8, ab)
+
+
+# ---------------------------------------------------------------- sampling
+def _grid(n):
+    return (np.arange(n) + 0.5) / n
+
+
+def _freq(logits, T, k, p, n=20000):
+    """Token frequencies of the oracle over a uniform grid of n values of u."""
+    L = np.repeat(np.asarray(logits, dtype=np.float32)[None], n, 0)
+    toks, _ = oracle.sample(L, [T] * n, [k] * n, [p] * n, _grid(n))
+    return np.bincount(toks, minlength=L.shape[1]) / n, toks
+
+
+def test_sample_greedy_is_the_first_maximum():
+    g = np.random.default_rng(1)
+    x = g.integers(-5, 5, size=(50, 40)).astype(np.float32)  # many ties
+    toks, margins = oracle.sample(x, [0.0] * 50, [0] * 50, [1.0] * 50, g.random(50))
+    assert np.array_equal(toks, np.argmax(x, axis=1)) and np.isinf(margins).all()
+
+
+def test_sample_closed_form_top_p_and_top_k_ties():
+    """probabilities 0.5, 0.3, 0.15, 0.05 (the logits are their logs):
+    top-p 0.8 keeps the first two (0.5 + 0.3 reaches 0.8), 0.81 the first
+    three; top-k 2 with three tied leaders keeps all three (ties enter
+    together)."""
+    lp = np.log([0.5, 0.3, 0.15, 0.05])
+    f, _ = _freq(lp + 0.0, 1.0, 0, 0.79)
+    np.testing.assert_allclose(f, [0.625, 0.375, 0, 0], atol=1e-3)
+    f, _ = _freq(lp, 1.0, 0, 0.81)
+    np.testing.assert_allclose(f, np.array([0.5, 0.3, 0.15, 0]) / 0.95, atol=1e-3)
+    f, _ = _freq(lp, 1.0, 0, 1.0)
+    np.testing.assert_allclose(f, [0.5, 0.3, 0.15, 0.05], atol=1e-3)
+    f, _ = _freq([1.0, 1.0, 0.0, 1.0], 1.0, 2, 1.0)
+    np.testing.assert_allclose(f, [1 / 3, 1 / 3, 0, 1 / 3], atol=1e-3)
+
+
+@pytest.mark.parametrize("T,k,p", [(1.0, 0, 1.0), (0.7, 10, 1.0), (1.3, 0, 0.9), (0.5, 25, 0.6), (2.0, 5, 0.99)])
+def test_sample_frequencies_match_truncated_softmax(T, k, p):
+    """Over a fine grid of u the oracle's frequencies equal the truncated,
+    renormalised softmax(logits / T): scipy's softmax, numpy's sort for the
+    k most probable and for the smallest prefix reaching p."""
+    from scipy.special import softmax
+    g = np.random.default_rng(int(T * 10) + k)
+    x = (g.normal(size=60) * 2).astype(np.float32)
+    P = softmax(x.astype(np.float64) / T)
+    order = np.argsort(-P, kind="stable")
+    keep = np.ones(60, dtype=bool)
+    if 0 < k < 60:
+        keep &= P >= P[order[k - 1]]
+    if p < 1:
+        c = np.cumsum(P[order])
+        n = int(np.searchsorted(c, p * c[-1] * (1 - 1e-12)))
+        keep &= P >= P[order[n]]
+    want = np.where(keep, P, 0.0)
+    want /= want.sum()
+    f, _ = _freq(x, T, k, p, n=40000)
+    np.testing.assert_allclose(f, want, atol=2e-4)
+
+
+def test_sample_inverse_cdf_in_vocabulary_order_and_limits():
+    g = np.random.default_rng(9)
+    x = (g.normal(size=30) * 3).astype(np.float32)
+    _, toks = _freq(x, 1.0, 0, 1.0, n=5000)
+    assert np.all(np.diff(toks) >= 0)  # u increasing -> token index nondecreasing
+    f, _ = _freq(x, 1e4, 0, 1.0, n=30000)  # very high temperature: nearly uniform
+    np.testing.assert_allclose(f, np.full(30, 1 / 30), atol=2e-3)
+    for T, k, p in ((1e-3, 0, 1.0), (1.0, 1, 1.0), (1.0, 0, 1e-9)):  # limits that reach greedy
+        f, _ = _freq(x, T, k, p, n=200)
+        assert f[np.argmax(x)] == 1.0
