@@ -49,6 +49,7 @@ def parse_args():
     ap.add_argument("--no-decode", action="store_true", help="skip the decode measurement")
     ap.add_argument("--mixed-workload", default="mixed_4x1024chunks_256decode")
     ap.add_argument("--no-mixed", action="store_true", help="skip the mixed-step measurement")
+    ap.add_argument("--no-sampling", action="store_true", help="skip the sampling measurement")
     ap.add_argument("--page-size", type=int, default=0,
                     help="lay the KV caches out in pages of this many slots (0: contiguous regions)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
@@ -380,6 +381,43 @@ def measure_decode(wd, args, device, torch, dist_on, peaks, peak_kind, kv_dtype,
     }
 
 
+def measure_sampling(args, device, torch, dist_on, peaks, peak_kind, B=64) -> dict:
+    """Token sampling (temperature + top-k + top-p, no greedy rows) from fp32
+    logits of B rows over the Qwen3 vocabulary: one kernel launch per step.
+    Bytes: the logits and the per-row parameters read, the tokens written."""
+    from causal_gqa_attention_qkv_gb300 import attn
+    from causal_gqa_attention_qkv_gb300 import inputs as gen
+    h = gen.make_sampling_inputs(B, gen.QWEN3_VOCAB, seed=6, greedy_share=0.0)
+    d = {k: v.to(device) for k, v in h.items()}
+    tokens = torch.empty(B, dtype=torch.int32, device=device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    run = lambda: attn.sample_tokens(d["logits"], d["temperature"], d["top_k"], d["top_p"], d["uniform"], tokens)
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        run()
+    torch.cuda.synchronize()
+    if dist_on:
+        torch.distributed.barrier()
+    times = []
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        run()
+        e1.record()
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    (ms,) = max_over_ranks([sum(times) / len(times)], device)
+    nbytes = B * gen.QWEN3_VOCAB * 4 + B * 4 * 4 + B * 4
+    hbm = float(peaks["hbm_gbs"])
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"sample_b{B}_v{gen.QWEN3_VOCAB}_topk_topp_temperature", "ms_per_step": round(ms, 4),
+            "rows_per_s": round(B / (ms * 1e-3), 1), "bytes_per_step": nbytes,
+            "roofline": {"bound": "hbm", "kernel": "sample_kernel", "achieved": round(gbs, 1), "peak": hbm,
+                         "peak_kind": f"hbm_gbs ({peak_kind})", "unit": "GB/s", "frac": round(gbs / hbm, 4)},
+            "gpu_launches": args.steps}
+
+
 def measure_mixed(wm, args, device, torch, dist_on, peaks, peak_kind) -> dict:
     """One serving step that mixes prefill chunks (on top of cached prefixes)
     with decode rows, issued back to back on one stream: the chunks'
@@ -483,6 +521,9 @@ def run_ours(args):
         line["mixed"] = measure_mixed(gen.ALL[args.mixed_workload], args, device, torch, dist_on, peaks,
                                       peak_kind)
         line["gpu_launches"] += line["mixed"]["gpu_launches"]
+    if not args.no_sampling:
+        line["sampling"] = measure_sampling(args, device, torch, dist_on, peaks, peak_kind)
+        line["gpu_launches"] += line["sampling"]["gpu_launches"]
     if rank == 0 and world == 1 and not args.no_cpu:
         flops_s, dt, desc, cores, _ = cpu_oracle_rate(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(flops_s / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,

@@ -67,6 +67,7 @@ EXPORTS = {
     "attn_decode_static_scratch": (ctypes.c_int, [_CFG, _P, _P, _P, _I32, _I32, _KV, _P, _P, _P]),
     "attn_get_status": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "attn_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    "attn_sample_tokens": (ctypes.c_int, [_P, _I32, _I32, ctypes.c_int64, _P, _P, _P, _P, _P, _P]),
 }
 
 
@@ -244,3 +245,19 @@ def get_status(workspace, stream=None) -> int:
     st = ctypes.c_int32(0)
     _check(load().attn_get_status(_ptr(workspace), _stream(stream), ctypes.byref(st)))
     return int(st.value)
+
+
+def sample_tokens(logits, temperature, top_k, top_p, uniform, tokens=None, stream=None):
+    """One token per row of fp32 logits [B, V] (include/sample.h): greedy where
+    temperature <= 0, else temperature + top-k + top-p, sampled with the row's
+    uniform number.  Returns the int32 [B] device tensor of tokens."""
+    assert logits.dtype == torch.float32 and logits.is_cuda and logits.dim() == 2 and logits.stride(1) == 1
+    B, V = logits.shape
+    for t, dt in ((temperature, torch.float32), (top_k, torch.int32), (top_p, torch.float32),
+                  (uniform, torch.float32)):
+        assert t.dtype == dt and t.is_cuda and t.is_contiguous() and t.numel() == B
+    if tokens is None:
+        tokens = torch.empty(B, dtype=torch.int32, device=logits.device)
+    _check(load().attn_sample_tokens(_ptr(logits), B, V, logits.stride(0), _ptr(temperature), _ptr(top_k),
+                                     _ptr(top_p), _ptr(uniform), _ptr(tokens), _stream(stream)))
+    return tokens

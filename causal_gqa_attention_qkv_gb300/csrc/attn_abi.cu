@@ -6,6 +6,7 @@
 #include <cmath>
 #include <mutex>
 
+#include "../../include/sample.h"
 #include "kernels.cuh"
 
 namespace gb300 {
@@ -352,6 +353,17 @@ int attn_get_status(void* workspace, void* stream, int32_t* status) {
   if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), s) != cudaSuccess) return ATTN_ELAUNCH;
   if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ELAUNCH;
   return ATTN_OK;
+}
+
+int attn_sample_tokens(const float* logits, int32_t B, int32_t V, int64_t ld, const float* temperature,
+                       const int32_t* top_k, const float* top_p, const float* uniform, int32_t* tokens,
+                       void* stream) {
+  if (!logits || !temperature || !top_k || !top_p || !uniform || !tokens) return ATTN_EINVAL;
+  if (B < 0 || V < 1 || V > (1 << 30) || ld < V) return ATTN_EINVAL;
+  int rc = check_device();
+  if (rc) return rc;
+  return launch_sample(logits, B, V, ld, temperature, top_k, top_p, uniform, tokens,
+                       static_cast<cudaStream_t>(stream));
 }
 
 const char* attn_strerror(int code) {

@@ -88,4 +88,9 @@ struct PrefillArgs {
 };
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 
+// One token per row of logits (include/sample.h); arguments checked by the caller.
+int launch_sample(const float* logits, int32_t B, int32_t V, int64_t ld, const float* temperature,
+                  const int32_t* top_k, const float* top_p, const float* uniform, int32_t* tokens,
+                  cudaStream_t stream);
+
 }  // namespace gb300

@@ -283,3 +283,34 @@ def sample_rows(w: Workload, count: int, tail: int, seed: int) -> torch.Tensor:
         heads = torch.randint(0, w.num_q_heads, (count,), generator=g).tolist()
         rows.update(zip(toks, heads))
     return torch.tensor(sorted(rows), dtype=torch.int32).reshape(-1, 2)
+
+
+QWEN3_VOCAB = 151936
+
+
+def make_sampling_inputs(B: int, V: int = QWEN3_VOCAB, seed: int = 0, greedy_share: float = 0.1) -> dict:
+    """Seeded logits and per-row sampling parameters (host tensors).
+
+    Logits are fp32 ``[B, V]``: N(0, 1) * 2 for every token plus, per row, 1-8
+    candidate tokens raised by U[4, 12] (the peaked shape of a language-model
+    head's output; no trained weights).  Per row: temperature from {0.3, 0.7,
+    1.0, 1.5} (0 = greedy for about ``greedy_share`` of the rows), top_k from
+    {0 (none), 1, 20, 50, 2000}, top_p from {1.0 (none), 0.95, 0.9, 0.5},
+    uniform in [0, 1).
+    """
+    g = _gen(7000 + seed)
+    logits = torch.randn((B, V), generator=g, dtype=torch.float32) * 2.0
+    for b in range(B):
+        n = int(torch.randint(1, 9, (1,), generator=g))
+        idx = torch.randint(0, V, (n,), generator=g)
+        logits[b, idx] += 4.0 + 8.0 * torch.rand(n, generator=g)
+    pick = lambda vals: torch.tensor(vals)[torch.randint(0, len(vals), (B,), generator=g)]
+    temperature = pick([0.3, 0.7, 1.0, 1.5]).float()
+    temperature[torch.rand(B, generator=g) < greedy_share] = 0.0
+    return {
+        "logits": logits,
+        "temperature": temperature,
+        "top_k": pick([0, 1, 20, 50, 2000]).to(torch.int32),
+        "top_p": pick([1.0, 0.95, 0.9, 0.5]).float(),
+        "uniform": torch.rand(B, generator=g, dtype=torch.float32),
+    }

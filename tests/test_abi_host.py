@@ -1,5 +1,5 @@
 """Host-side checks of the C ABI (no GPU needed): the library loads, exports
-every entry point include/attn.h declares, and rejects bad arguments before
+every entry point the headers under include/ declare, and rejects bad arguments before
 touching a pointer or the device."""
 import ctypes
 import os
@@ -19,15 +19,20 @@ def lib():
 
 
 def declared_functions():
-    text = open(os.path.join(ROOT, "include", "attn.h")).read()
-    return sorted(set(re.findall(r"ATTN_API\s+[\w\s\*]*?\b(attn_\w+)\s*\(", text)))
+    """Every ATTN_API function of every header under include/."""
+    names = set()
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names.update(re.findall(r"ATTN_API\s+[\w\s\*]*?\b(attn_\w+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_calls():
     names = declared_functions()
     for n in ("attn_prefill", "attn_decode", "attn_kv_append", "attn_workspace_size",
               "attn_prefill_prepare", "attn_prefill_attend", "attn_decode_attend",
-              "attn_get_status", "attn_strerror", "attn_workspace_init"):
+              "attn_get_status", "attn_strerror", "attn_workspace_init", "attn_sample_tokens"):
         assert n in names
 
 
@@ -159,3 +164,14 @@ def test_cache_element_type_checked(lib, dtype, ks, vs, ok):
     assert (rc in past_checks) if ok else rc == -1
     rc = lib.attn_prefill_attend(ctypes.byref(cfg), f, f, 1, 4, 4, k, f, f, 1 << 20, None)
     assert (rc in past_checks) if ok else rc == -1
+
+
+def test_sample_arguments_checked(lib):
+    f = ctypes.c_void_p(1 << 20)
+    call = lambda lg=f, B=4, V=100, ld=100, tok=f: lib.attn_sample_tokens(lg, B, V, ld, f, f, f, f, tok, None)
+    assert call(lg=None) == -1
+    assert call(tok=None) == -1
+    assert call(B=-1) == -1
+    assert call(V=0) == -1
+    assert call(ld=99) == -1
+    assert call() in (-4, -5)  # past the checks: no GPU here
