@@ -33,7 +33,6 @@ constexpr int kBins = 4096;   // second and third digits: 12 bits
 // masses), later reused for the block histograms of the other two
 constexpr int kSmemBytes = kWarps * kBins0 * (4 + 8);
 static_assert(kBins * (4 + 8) <= kSmemBytes, "histograms");
-constexpr float kFix = 1099511627776.f;  // 2^40
 constexpr int kMaxChunks = 2 * kThreads;  // chunks of the final scan (kept masses in shared memory)
 static_assert(kMaxChunks * 8 <= kSmemBytes, "chunk sums");
 using u64 = unsigned long long;
@@ -56,8 +55,15 @@ struct SamplePar {
 };
 
 // exp((v - mx) / T) in units of 2^-40, computed the same way in every pass.
+// The weight w <= 1 becomes round(w x 2^40) from two 32-bit conversions:
+// w x 2^20 = hi + f exactly (hi its integer part), then lo = round(f x 2^20).
+// (A direct float -> 64-bit integer conversion runs on the fp64 pipe, which
+// this part has little of.)
 __device__ __forceinline__ u64 fixed_weight(float v, float mx, float log2e_over_t) {
-  return __float2ull_rn(__fmul_rn(exp2f(__fmul_rn(__fsub_rn(v, mx), log2e_over_t)), kFix));
+  const float s = __fmul_rn(exp2f(__fmul_rn(__fsub_rn(v, mx), log2e_over_t)), 1048576.f);
+  const uint32_t hi = __float2uint_rd(s);
+  const uint32_t lo = __float2uint_rn(__fmul_rn(__fsub_rn(s, __uint2float_rn(hi)), 1048576.f));
+  return ((u64)hi << 20) + lo;
 }
 
 // Calls f(index, value) for this thread's share of the row: float4 loads two
