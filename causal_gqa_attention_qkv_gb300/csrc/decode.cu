@@ -5,9 +5,9 @@
 // Decode": attention of the new token to the cache is one more row of the
 // lower-triangular attention matrix.  The grid is (split, KV head, request):
 // each CTA streams one contiguous slice of one KV head's cache through shared
-// memory exactly once (TMA, 3-stage mbarrier pipeline) and applies it to all
-// Hq/Hkv query heads of the group at the same time, so every cached byte is
-// read from HBM once per step.  Partial results (running max, sum, unscaled
+// memory exactly once (TMA, mbarrier pipeline of 3 bf16 or 6 E4M3 stages) and
+// applies it to all Hq/Hkv query heads of the group at the same time, so
+// every cached byte is read from HBM once per step.  Partial results (running max, sum, unscaled
 // output) of the splits are merged by log-sum-exp in a second kernel.
 #include "kernels.cuh"
 

@@ -73,7 +73,8 @@ typedef struct attn_config {
 } attn_config_t;
 
 /* The KV cache of one layer (host struct holding device pointers).
- * k_cache, v_cache: bf16 [num_slots, Hkv, D], contiguous, row = one slot.
+ * k_cache, v_cache: [num_slots, Hkv, D] entries (bf16, or E4M3 codes: see
+ * kv_dtype below), contiguous, row = one slot.
  * The entry at position p of request b lives in one slot:
  *   contiguous (page_table == NULL): slot slot_base[b] + p; request b owns
  *     slots [slot_base[b], slot_base[b] + slot_capacity[b]);

@@ -76,6 +76,9 @@ def _load():
             _P, _P, _P, ctypes.c_int, ctypes.c_int, _I64, _P, _P, _P, _P]
         lib.oracle_sample.restype = _I64
         lib.oracle_sample.argtypes = [_I64, _P, _D, _I64, _D, _D, ctypes.POINTER(_D)]
+        lib.oracle_sample_bracket.restype = ctypes.c_int
+        lib.oracle_sample_bracket.argtypes = [_I64, _P, _D, _I64, _D, _I64, ctypes.POINTER(_D),
+                                              ctypes.POINTER(_D)]
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -248,6 +251,16 @@ def sample(logits, temperature, top_k, top_p, uniform):
                                     float(top_p[b]), float(uniform[b]), ctypes.byref(m))
         margins[b] = m.value
     return toks, margins
+
+
+def sample_bracket(logits_row, temperature, top_k, top_p, token):
+    """(kept, lo, hi) for a non-greedy row: whether ``token`` survives the
+    truncation and the range [lo, hi) of u that selects it."""
+    x = np.ascontiguousarray(np.asarray(logits_row, dtype=np.float32))
+    lo, hi = _D(), _D()
+    kept = _load().oracle_sample_bracket(x.shape[0], x.ctypes.data_as(_P), float(temperature), int(top_k),
+                                         float(top_p), int(token), ctypes.byref(lo), ctypes.byref(hi))
+    return bool(kept), lo.value, hi.value
 
 
 def all_rows(num_tokens: int, num_q_heads: int) -> np.ndarray:

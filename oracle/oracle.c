@@ -346,28 +346,31 @@ static int cmp_desc_logit(const void* a, const void* b) {
   return i < j ? -1 : (i > j);
 }
 
-int64_t oracle_sample(int64_t V, const float* logits, double temperature, int64_t top_k,
-                      double top_p, double u, double* margin) {
-  *margin = INFINITY;
+/* The truncation step for one row: weights w_i = exp(l_i / T - max / T),
+ * their total *W, the kept threshold *lambda (logits >= *lambda are kept)
+ * and the relative distance *margin_p of top_p from the crossing (inf when
+ * top-p does not truncate).  Returns w (malloc'd). */
+static double* truncate_row(int64_t V, const float* logits, double temperature, int64_t top_k,
+                            double top_p, double* lambda, double* W, double* margin_p) {
   int64_t arg = 0;
   for (int64_t i = 1; i < V; ++i)
     if (logits[i] > logits[arg]) arg = i;
-  if (!(temperature > 0.0)) return arg;
   double m = (double)logits[arg] / temperature;
   double* w = malloc(sizeof(double) * (size_t)V);
-  double W = 0.0;
+  *W = 0.0;
   for (int64_t i = 0; i < V; ++i) {
     w[i] = exp((double)logits[i] / temperature - m);
-    W += w[i];
+    *W += w[i];
   }
   int64_t* order = malloc(sizeof(int64_t) * (size_t)V);
   for (int64_t i = 0; i < V; ++i) order[i] = i;
   g_sort_logits = logits;
   qsort(order, (size_t)V, sizeof(int64_t), cmp_desc_logit);
-  double lambda = -INFINITY;
-  if (top_k > 0 && top_k < V) lambda = logits[order[top_k - 1]];
+  *lambda = -INFINITY;
+  *margin_p = INFINITY;
+  if (top_k > 0 && top_k < V) *lambda = logits[order[top_k - 1]];
   if (top_p < 1.0) {
-    double cum = 0.0, target = top_p * W;
+    double cum = 0.0, target = top_p * *W;
     for (int64_t n = 0; n < V;) {
       int64_t e = n;
       double group = 0.0;
@@ -376,14 +379,29 @@ int64_t oracle_sample(int64_t V, const float* logits, double temperature, int64_
       cum += group;
       if (cum >= target || e == V) {
         double lp = logits[order[n]];
-        if (lp > lambda) lambda = lp;
-        double d = fmin(cum - target, target - before) / W;
-        if (d < *margin) *margin = d;
+        if (lp > *lambda) *lambda = lp;
+        *margin_p = fmin(cum - target, target - before) / *W;
         break;
       }
       n = e;
     }
   }
+  free(order);
+  return w;
+}
+
+int64_t oracle_sample(int64_t V, const float* logits, double temperature, int64_t top_k,
+                      double top_p, double u, double* margin) {
+  *margin = INFINITY;
+  if (!(temperature > 0.0)) {
+    int64_t arg = 0;
+    for (int64_t i = 1; i < V; ++i)
+      if (logits[i] > logits[arg]) arg = i;
+    return arg;
+  }
+  double lambda, W, margin_p;
+  double* w = truncate_row(V, logits, temperature, top_k, top_p, &lambda, &W, &margin_p);
+  *margin = margin_p;
   double S = 0.0;
   for (int64_t i = 0; i < V; ++i)
     if (logits[i] >= lambda) S += w[i];
@@ -402,8 +420,27 @@ int64_t oracle_sample(int64_t V, const float* logits, double temperature, int64_
   }
   if (token < 0) token = last;
   free(w);
-  free(order);
   return token;
+}
+
+/* For a non-greedy row: whether `token` is kept, and the kept cumulative
+ * fractions just before (*lo) and after (*hi) it in vocabulary order (the
+ * range of u that selects it). */
+int oracle_sample_bracket(int64_t V, const float* logits, double temperature, int64_t top_k,
+                          double top_p, int64_t token, double* lo, double* hi) {
+  double lambda, W, margin_p;
+  double* w = truncate_row(V, logits, temperature, top_k, top_p, &lambda, &W, &margin_p);
+  double S = 0.0, before = 0.0;
+  for (int64_t i = 0; i < V; ++i)
+    if (logits[i] >= lambda) {
+      if (i < token) before += w[i];
+      S += w[i];
+    }
+  int kept = token >= 0 && token < V && logits[token] >= lambda;
+  *lo = before / S;
+  *hi = (before + (kept ? w[token] : 0.0)) / S;
+  free(w);
+  return kept;
 }
 
 int oracle_num_threads(void) {
