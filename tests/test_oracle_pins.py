@@ -494,3 +494,19 @@ def test_sample_inverse_cdf_in_vocabulary_order_and_limits():
     for T, k, p in ((1e-3, 0, 1.0), (1.0, 1, 1.0), (1.0, 0, 1e-9)):  # limits that reach greedy
         f, _ = _freq(x, T, k, p, n=200)
         assert f[np.argmax(x)] == 1.0
+
+
+def test_sample_bracket_contains_u_of_the_sampled_token():
+    """The bracket helper used to accept near-boundary device tokens agrees with
+    the sampler: the sampled token is kept and its range of u contains u, and a
+    token below the kept threshold is reported as not kept."""
+    g = np.random.default_rng(17)
+    for r in range(40):
+        x = (g.normal(size=200) * 2).astype(np.float32)
+        T, k, p, u = float(g.choice([0.5, 1.0, 2.0])), int(g.choice([0, 5, 50])), float(g.choice([1.0, 0.9, 0.5])), float(g.random())
+        tok, _ = oracle.sample(x[None], [T], [k], [p], [u])
+        kept, lo, hi = oracle.sample_bracket(x, T, k, p, int(tok[0]))
+        assert kept and lo - 1e-12 <= u < hi + 1e-12
+        if k == 5:
+            low = int(np.argmin(x))
+            assert not oracle.sample_bracket(x, T, k, p, low)[0]
