@@ -359,7 +359,7 @@ int attn_sample_tokens(const float* logits, int32_t B, int32_t V, int64_t ld, co
                        const int32_t* top_k, const float* top_p, const float* uniform, int32_t* tokens,
                        void* stream) {
   if (!logits || !temperature || !top_k || !top_p || !uniform || !tokens) return ATTN_EINVAL;
-  if (B < 0 || V < 1 || V > (1 << 30) || ld < V) return ATTN_EINVAL;
+  if (B < 0 || V < 1 || V > (1 << 23) || ld < V) return ATTN_EINVAL;  // sums of 2^-40 units fit 64 bits
   int rc = check_device();
   if (rc) return rc;
   return launch_sample(logits, B, V, ld, temperature, top_k, top_p, uniform, tokens,

@@ -38,8 +38,9 @@ extern "C" {
  *   uniform:     fp32 [B], each in [0, 1): the row's random number.
  *   tokens:      int32 [B] on the device (output).
  * All device pointers, caller-owned; asynchronous on `stream`.  Returns
- * ATTN_OK, ATTN_EINVAL (NULL pointer, B < 0, V < 1, V > 2^30, ld < V),
- * ATTN_EDEVICE or ATTN_ELAUNCH. */
+ * ATTN_OK, ATTN_EINVAL (NULL pointer, B < 0, V < 1, V > 2^23, ld < V),
+ * ATTN_EDEVICE or ATTN_ELAUNCH.  (Weights are summed exactly as 64-bit
+ * integers in units of 2^-40, which bounds V by 2^23.) */
 ATTN_API int attn_sample_tokens(const float* logits, int32_t B, int32_t V, int64_t ld,
                                 const float* temperature, const int32_t* top_k, const float* top_p,
                                 const float* uniform, int32_t* tokens, void* stream);

@@ -173,5 +173,6 @@ def test_sample_arguments_checked(lib):
     assert call(tok=None) == -1
     assert call(B=-1) == -1
     assert call(V=0) == -1
+    assert call(V=(1 << 23) + 1, ld=(1 << 23) + 1) == -1
     assert call(ld=99) == -1
     assert call() in (-4, -5)  # past the checks: no GPU here
