@@ -510,3 +510,23 @@ def test_sample_bracket_contains_u_of_the_sampled_token():
         if k == 5:
             low = int(np.argmin(x))
             assert not oracle.sample_bracket(x, T, k, p, low)[0]
+
+
+@pytest.mark.parametrize("page_size", [64, 128])
+def test_paged_e4m3_cache_gives_the_contiguous_result(page_size):
+    """With one-byte entries as with bf16 ones, the page table only moves where
+    an entry lives: identical outputs, and each position's codes in its page
+    slot."""
+    w = gen.custom("paged_e4m3_pin", 4, 2, 64, [50, 130, 1], [100, 0, 129], seed=23)
+    cfg = oracle.cfg_of(w)
+    hc = gen.make_inputs(w, kv_dtype="e4m3")
+    hp = gen.make_inputs(w, page_size=page_size, kv_dtype="e4m3")
+    rc, rp = oracle.step(cfg, hc), oracle.step(cfg, hp)
+    assert rc["bad"] == 0 and rp["bad"] == 0
+    assert np.array_equal(rc["out"], rp["out"])
+    pt = hp["page_table"]
+    for b in range(w.batch):
+        pos = torch.arange(w.cache_lens[b] + w.new_lens[b])
+        sp = pt[b, pos // page_size].long() * page_size + pos % page_size
+        sc = hc["slot_base"][b] + pos
+        assert torch.equal(rp["k_cache"][sp], rc["k_cache"][sc]) and torch.equal(rp["v_cache"][sp], rc["v_cache"][sc])
