@@ -129,6 +129,7 @@ E4M3_PREFILL = [
     (16, 2, 64, [130, 1, 65, 257], [3, 0, 700, 128], 0, 4),
     (32, 8, 128, [300, 77, 513, 129], [0, 200, 64, 1000], 64, 4),
     (8, 8, 64, [200, 31], [64, 0], 128, 2),
+    (16, 2, 64, [130, 1, 65], [3, 0, 700], 64, 3),    # D 64 over 64-slot pages: two 64-row boxes
     (32, 8, 128, [100, 64, 1, 1, 1], [50, 0, 10, 700, 0], 0, 2),
 ]
 
