@@ -314,3 +314,20 @@ def make_sampling_inputs(B: int, V: int = QWEN3_VOCAB, seed: int = 0, greedy_sha
         "top_p": pick([1.0, 0.95, 0.9, 0.5]).float(),
         "uniform": torch.rand(B, generator=g, dtype=torch.float32),
     }
+
+
+QWEN3_4B_HIDDEN = 2560
+
+
+def make_projection_inputs(w: Workload, hidden: int = QWEN3_4B_HIDDEN, seed: int = 0) -> dict:
+    """Seeded hidden states and random projection weights around the step
+    (host bf16 tensors; no trained weights): ``hidden`` ``[N, C]`` N(0, 1),
+    ``w_qkv`` ``[(Hq+2Hkv)*D, C]`` and ``w_o`` ``[C, Hq*D]`` N(0, 1/fan_in), so
+    that the projected qkv has about unit variance like the step's own qkv."""
+    g = _gen(8000 + seed)
+    N, C = w.num_tokens, hidden
+    return {
+        "hidden": _bf16_normal(g, (N, C)),
+        "w_qkv": _bf16_normal(g, (w.qkv_width, C), C ** -0.5),
+        "w_o": _bf16_normal(g, (C, w.num_q_heads * w.head_dim), (w.num_q_heads * w.head_dim) ** -0.5),
+    }

@@ -70,6 +70,10 @@ def _load():
             ctypes.c_int, ctypes.c_int, ctypes.c_int, _D, _D,
             _P, _I64, _P, _P, ctypes.c_int, _P, _P, _P, _P, _P, ctypes.c_int, ctypes.c_int,
             _I64, _P, _P, ctypes.c_int, _F, _F, _I64, _P, _P, _P]
+        lib.oracle_prologue_projected.restype = ctypes.c_int
+        lib.oracle_prologue_projected.argtypes = lib.oracle_prologue.argtypes
+        lib.oracle_linear.restype = None
+        lib.oracle_linear.argtypes = [_I64, _I64, _I64, _P, _P, _P]
         lib.oracle_attention.restype = None
         lib.oracle_attention.argtypes = [
             ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, ctypes.c_int, _F, _F, ctypes.c_int, _P,
@@ -172,16 +176,40 @@ def _pages(inputs: dict):
     return pt.reshape(-1), int(inputs["page_size"]), int(pt.shape[1])
 
 
-def prologue(cfg: dict, inputs: dict, q_rows=None):
+def linear(x, w) -> np.ndarray:
+    """y = x w^T in fp64: x ``[N, C]`` (bf16 tensor or float array), w bf16
+    ``[O, C]`` (the linear layer's weight layout).  Returns fp64 ``[N, O]``."""
+    if isinstance(x, torch.Tensor):
+        x = x.detach().cpu().double().numpy()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    wb = _bits(w)
+    N, C = x.shape
+    O = wb.shape[0]
+    assert wb.shape[1] == C
+    y = np.zeros((N, O), dtype=np.float64)
+    _load().oracle_linear(N, C, O, _ptr(x), _ptr(wb), _ptr(y))
+    return y
+
+
+def prologue(cfg: dict, inputs: dict, q_rows=None, qkv64=None):
     """Steps 1-4.  Returns (k_cache, v_cache, q, bad) where the caches are new
     tensors of the input caches' type (bf16, or uint8 E4M3 codes; the inputs
     are not modified), q is fp64 ``[N, Hq, D]`` (or
     ``[R, D]`` for the (token, head) pairs in ``q_rows``), and ``bad`` counts
-    requests whose cache region is too small (they write nothing)."""
+    requests whose cache region is too small (they write nothing).
+
+    ``qkv64`` (fp64 ``[N, (Hq+2Hkv)*D]``, e.g. from ``linear``) replaces the
+    bf16 qkv: the projection's output enters the norm, the rotation and the
+    cache without a bf16 rounding of its own."""
     lib = _load()
     Hq, Hkv, D = cfg["num_q_heads"], cfg["num_kv_heads"], cfg["head_dim"]
     assert D <= 256 and D % 2 == 0 and Hq % Hkv == 0
-    qkv = _bits_view(inputs["qkv"])
+    if qkv64 is not None:
+        qkv = np.ascontiguousarray(qkv64, dtype=np.float64)
+        fn = lib.oracle_prologue_projected
+    else:
+        qkv = _bits_view(inputs["qkv"])
+        fn = lib.oracle_prologue
     N = qkv.shape[0]
     kc = _cache_copy(inputs["k_cache"])
     vc = _cache_copy(inputs["v_cache"])
@@ -203,7 +231,7 @@ def prologue(cfg: dict, inputs: dict, q_rows=None):
         qt = np.ascontiguousarray(rows[:, 0])
         qh = np.ascontiguousarray(rows[:, 1])
         q = np.zeros((nq, D), dtype=np.float64)
-    bad = lib.oracle_prologue(Hq, Hkv, D, float(cfg["rms_eps"]), float(cfg["rope_theta"]),
+    bad = fn(Hq, Hkv, D, float(cfg["rms_eps"]), float(cfg["rope_theta"]),
                               _ptr(qkv), N, _ptr(qw), _ptr(kw), B, _ptr(cu), _ptr(cl), _ptr(sb),
                               _ptr(cap), _ptr(pt), ps, ppr, kc.shape[0], _ptr(kc), _ptr(vc), fp8, ks,
                               vs, nq, _ptr(qt), _ptr(qh), _ptr(q))
@@ -280,6 +308,22 @@ def step(cfg: dict, inputs: dict, rows=None):
     kc, vc, q, bad = prologue(cfg, inputs, q_rows=rows)
     out = attention(cfg, kc, vc, inputs, rows, q)
     return {"k_cache": kc, "v_cache": vc, "rows": rows, "out": out, "q": q, "bad": bad}
+
+
+def projected_step(cfg: dict, inputs: dict, hidden, w_qkv, w_o):
+    """The step with the projections either side of it: qkv = hidden w_qkv^T
+    (fp64, not rounded), the step on every (token, head) row, then
+    o = attention_out w_o^T.  hidden bf16 ``[N, C]``, w_qkv bf16
+    ``[(Hq+2Hkv)*D, C]``, w_o bf16 ``[C, Hq*D]``.  Returns the step's dict
+    plus ``qkv64`` and ``o`` (fp64 ``[N, C]``)."""
+    N = hidden.shape[0]
+    qkv64 = linear(hidden, w_qkv)
+    rows = all_rows(N, cfg["num_q_heads"])
+    kc, vc, q, bad = prologue(cfg, inputs, q_rows=rows, qkv64=qkv64)
+    att = attention(cfg, kc, vc, inputs, rows, q)
+    o = linear(att.reshape(N, -1), w_o)
+    return {"k_cache": kc, "v_cache": vc, "rows": rows, "out": att, "q": q, "bad": bad, "qkv64": qkv64,
+            "o": o}
 
 
 def cfg_of(w) -> dict:

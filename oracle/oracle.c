@@ -172,6 +172,34 @@ static void load_head(const uint16_t* row, int64_t col0, int D, double* out) {
   for (int i = 0; i < D; ++i) out[i] = bf16_bits_to_double(row[col0 + i]);
 }
 
+/* Head vector of token t from the packed qkv: bf16 bits, or (row64 != NULL)
+ * the fp64 output of the projection itself, never rounded. */
+static void load_src(const uint16_t* qkv, const double* qkv64, int64_t t, int64_t W, int64_t col0,
+                     int D, double* out) {
+  if (qkv64) {
+    for (int i = 0; i < D; ++i) out[i] = qkv64[t * W + col0 + i];
+  } else {
+    load_head(qkv + t * W, col0, D, out);
+  }
+}
+
+/*
+ * The merged Q/K/V projection in front of the step and the output projection
+ * behind it (walkthrough section 3.3: qkv_proj, then o_proj on the attention
+ * output): y[n][o] = sum_c x[n][c] * w[o][c], x fp64 [N, C], w bf16 bits
+ * [O, C] (the nn.Linear weight layout), y fp64 [N, O]; plain loops, fp64 sums
+ * in index order.
+ */
+void oracle_linear(int64_t N, int64_t C, int64_t O, const double* x, const uint16_t* w, double* y) {
+#pragma omp parallel for schedule(static)
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t o = 0; o < O; ++o) {
+      double acc = 0.0;
+      for (int64_t c = 0; c < C; ++c) acc += x[n * C + c] * bf16_bits_to_double(w[o * C + c]);
+      y[n * O + o] = acc;
+    }
+}
+
 /*
  * Steps 1-4 for all N tokens.  The cache (k_cache, v_cache: bf16 bits, or
  * E4M3 bytes when kv_fp8, [num_slots, Hkv, D]) is updated in place: token j
@@ -180,8 +208,8 @@ static void load_head(const uint16_t* row, int64_t col0, int D, double* out) {
  * (q_tok[r], q_head[r]) as [nq, D].  Returns the number of requests whose
  * region cannot hold cache_lens + new tokens (those write nothing).
  */
-int oracle_prologue(int Hq, int Hkv, int D, double eps, double theta,
-                    const uint16_t* qkv, int64_t N, const uint16_t* q_norm_w,
+static int prologue_impl(int Hq, int Hkv, int D, double eps, double theta,
+                    const uint16_t* qkv, const double* qkv64, int64_t N, const uint16_t* q_norm_w,
                     const uint16_t* k_norm_w, int B, const int32_t* cu_seqlens,
                     const int32_t* cache_lens, const int64_t* slot_base,
                     const int32_t* slot_capacity, const int32_t* page_table, int page_size,
@@ -215,27 +243,26 @@ int oracle_prologue(int Hq, int Hkv, int D, double eps, double theta,
       int64_t t = cu_seqlens[b] + j;
       double pos = (double)cache_lens[b] + (double)j;
       int64_t slot = slot_of(slot_base, page_table, page_size, pages_per_req, b, cache_lens[b] + j);
-      const uint16_t* row = qkv + t * W;
-      double x[256], y[256];
+      double x[256], y[256], v[256];
       for (int kh = 0; kh < Hkv; ++kh) {
-        load_head(row, (int64_t)(Hq + kh) * D, D, x);
+        load_src(qkv, qkv64, t, W, (int64_t)(Hq + kh) * D, D, x);
         oracle_rmsnorm(x, kw, D, eps, y);
         oracle_rope(y, D, pos, theta);
         const int64_t e0 = (slot * Hkv + kh) * D;
-        const uint16_t* vs = row + (int64_t)(Hq + Hkv + kh) * D;
+        load_src(qkv, qkv64, t, W, (int64_t)(Hq + Hkv + kh) * D, D, v);
         if (kv_fp8) {
           uint8_t* kd = (uint8_t*)k_cache + e0;
           uint8_t* vd = (uint8_t*)v_cache + e0;
           for (int i = 0; i < D; ++i) {
             kd[i] = e4m3_store(y[i], k_scale);
-            vd[i] = e4m3_store(bf16_bits_to_double(vs[i]), v_scale);
+            vd[i] = e4m3_store(v[i], v_scale);
           }
         } else {
           uint16_t* kd = (uint16_t*)k_cache + e0;
           uint16_t* vd = (uint16_t*)v_cache + e0;
           for (int i = 0; i < D; ++i) {
             kd[i] = oracle_bf16_round(y[i]);
-            vd[i] = vs[i];
+            vd[i] = oracle_bf16_round(v[i]);  /* a bf16 input rounds to itself */
           }
         }
       }
@@ -249,13 +276,47 @@ int oracle_prologue(int Hq, int Hkv, int D, double eps, double theta,
     int b = find_request(cu_seqlens, B, t);
     double pos = (double)cache_lens[b] + (double)(t - cu_seqlens[b]);
     double x[256];
-    load_head(qkv + t * W, (int64_t)h * D, D, x);
+    load_src(qkv, qkv64, t, W, (int64_t)h * D, D, x);
     oracle_rmsnorm(x, qw, D, eps, q_out + r * D);
     oracle_rope(q_out + r * D, D, pos, theta);
   }
   free(qw);
   free(kw);
   return bad;
+}
+
+int oracle_prologue(int Hq, int Hkv, int D, double eps, double theta,
+                    const uint16_t* qkv, int64_t N, const uint16_t* q_norm_w,
+                    const uint16_t* k_norm_w, int B, const int32_t* cu_seqlens,
+                    const int32_t* cache_lens, const int64_t* slot_base,
+                    const int32_t* slot_capacity, const int32_t* page_table, int page_size,
+                    int pages_per_req, int64_t num_slots, void* k_cache,
+                    void* v_cache, int kv_fp8, float k_scale, float v_scale, int64_t nq,
+                    const int32_t* q_tok, const int32_t* q_head, double* q_out) {
+  return prologue_impl(Hq, Hkv, D, eps, theta, qkv, NULL, N, q_norm_w, k_norm_w, B, cu_seqlens,
+                       cache_lens, slot_base, slot_capacity, page_table, page_size, pages_per_req,
+                       num_slots, k_cache, v_cache, kv_fp8, k_scale, v_scale, nq, q_tok, q_head,
+                       q_out);
+}
+
+/*
+ * The same steps fed by the projection's own output qkv64 (fp64 [N, W], as
+ * oracle_linear gives it) instead of bf16 qkv: what a projection kernel that
+ * hands its accumulators straight to the norm, the rotation and the cache
+ * computes.  V is then rounded once, like K, when it enters the cache.
+ */
+int oracle_prologue_projected(int Hq, int Hkv, int D, double eps, double theta,
+                              const double* qkv64, int64_t N, const uint16_t* q_norm_w,
+                              const uint16_t* k_norm_w, int B, const int32_t* cu_seqlens,
+                              const int32_t* cache_lens, const int64_t* slot_base,
+                              const int32_t* slot_capacity, const int32_t* page_table,
+                              int page_size, int pages_per_req, int64_t num_slots, void* k_cache,
+                              void* v_cache, int kv_fp8, float k_scale, float v_scale, int64_t nq,
+                              const int32_t* q_tok, const int32_t* q_head, double* q_out) {
+  return prologue_impl(Hq, Hkv, D, eps, theta, NULL, qkv64, N, q_norm_w, k_norm_w, B, cu_seqlens,
+                       cache_lens, slot_base, slot_capacity, page_table, page_size, pages_per_req,
+                       num_slots, k_cache, v_cache, kv_fp8, k_scale, v_scale, nq, q_tok, q_head,
+                       q_out);
 }
 
 /*

@@ -530,3 +530,46 @@ def test_paged_e4m3_cache_gives_the_contiguous_result(page_size):
         sp = pt[b, pos // page_size].long() * page_size + pos % page_size
         sc = hc["slot_base"][b] + pos
         assert torch.equal(rp["k_cache"][sp], rc["k_cache"][sc]) and torch.equal(rp["v_cache"][sp], rc["v_cache"][sc])
+
+
+# ---------------------------------------------------------------- projections around the step
+def test_linear_matches_torch_fp64_matmul():
+    g = torch.Generator().manual_seed(41)
+    for N, C, O in ((3, 7, 5), (17, 64, 40), (64, 2560, 96)):
+        x = torch.randn(N, C, generator=g).to(torch.bfloat16)
+        w = torch.randn(O, C, generator=g).to(torch.bfloat16)
+        ref = (x.double() @ w.double().T).numpy()
+        np.testing.assert_allclose(oracle.linear(x, w), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_projected_prologue_with_identity_weights_is_the_plain_prologue():
+    """hidden = the step's qkv and w_qkv = I: the projection reproduces the bf16
+    qkv exactly, so the projected prologue must give the plain one's caches and
+    queries bit for bit (V included: a bf16 value rounds to itself)."""
+    w = gen.custom("proj_id", 8, 2, 64, [9, 4], [3, 0], seed=43)
+    cfg = oracle.cfg_of(w)
+    h = gen.make_inputs(w)
+    eye = torch.eye(w.qkv_width, dtype=torch.bfloat16)
+    plain = oracle.prologue(cfg, h)
+    proj = oracle.prologue(cfg, h, qkv64=oracle.linear(h["qkv"], eye))
+    assert torch.equal(plain[0].view(torch.int16), proj[0].view(torch.int16))
+    assert torch.equal(plain[1].view(torch.int16), proj[1].view(torch.int16))
+    assert np.array_equal(plain[2], proj[2])
+
+
+def test_projected_step_rounds_v_once_and_applies_the_output_projection():
+    w = gen.custom("proj_step", 8, 2, 64, [6, 3], [2, 5], seed=44)
+    cfg = oracle.cfg_of(w)
+    h = gen.make_inputs(w)
+    pr = gen.make_projection_inputs(w, hidden=96, seed=44)
+    r = oracle.projected_step(cfg, h, pr["hidden"], pr["w_qkv"], pr["w_o"])
+    Hq, Hkv, D = w.num_q_heads, w.num_kv_heads, w.head_dim
+    # V entries: the projection's V columns rounded once by torch's own fp64 -> bf16 conversion
+    for b in range(w.batch):
+        for j in range(w.new_lens[b]):
+            t = int(h["cu_seqlens"][b]) + j
+            slot = int(h["slot_base"][b]) + w.cache_lens[b] + j
+            v64 = torch.from_numpy(r["qkv64"][t, (Hq + Hkv) * D:].reshape(Hkv, D).copy())
+            assert torch.equal(r["v_cache"][slot].view(torch.int16), v64.to(torch.bfloat16).view(torch.int16))
+    ref_o = torch.from_numpy(r["out"]).reshape(w.num_tokens, Hq * D) @ pr["w_o"].double().T
+    np.testing.assert_allclose(r["o"], ref_o.numpy(), rtol=1e-12, atol=1e-12)
