@@ -6,13 +6,17 @@ RoPE + cache append (prologue kernel; for prefill it also writes the prepared
 Q) and causal GQA attention (tcgen05 prefill kernel; split-KV + combine for
 decode, which prepares its few Q rows itself).
 
-Headline (``value``): prefill attention TFLOP/s on the Qwen3-4B-shaped
-prefill (8 packed sequences, lengths U[256, 2048], Hq 32 / Hkv 8 / D 128).
-FLOPs = 4 * D * Hq * (unmasked query-key pairs, diagonal included).
-The decode half of the metric (KV-read GB/s on 64 requests with cached
-lengths U[512, 8192]) is measured in the same run and reported under
-``decode``.  Inputs are seeded synthetic bf16 tensors resident in HBM; L2 is
-flushed (a 256 MiB write) before every timed step, outside the timed events.
+Headline (``value``): prefill TFLOP/s of the whole step on the largest
+single-GPU workload, one 32 768-token sequence with Hq 64 / Hkv 8 / D 128
+(``long_prefill_T32768_hq64_hkv8``).  FLOPs = 4 * D * Hq * (unmasked
+query-key pairs, diagonal included).  Every other workload is measured in the
+same run under its own key: the Qwen3-4B-shaped prefill (8 packed sequences,
+lengths U[256, 2048]), the 64-request decode batch (KV-read GB/s, the decode
+half of the metric), both over bf16 and one-byte E4M3 caches, the mixed
+prefill-chunk + decode step, the tiny 12-token workload (microseconds per
+call) and token sampling.  Inputs are seeded synthetic tensors resident in
+HBM; L2 is flushed (a 256 MiB write) before every timed step, outside the
+timed events.
 
 ``--impl reference`` times the CPU fp64 oracle on the host cores instead
 (a bounded sample of the same workload per step).
@@ -44,7 +48,9 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="qwen3_4b_prefill_8seq_U256_2048")
+    ap.add_argument("--workload", default="long_prefill_T32768_hq64_hkv8")
+    ap.add_argument("--prefill-workload", default="qwen3_4b_prefill_8seq_U256_2048",
+                    help="second prefill workload, reported under its own key")
     ap.add_argument("--decode-workload", default="decode_b64_cache_U512_8192")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode measurement")
     ap.add_argument("--mixed-workload", default="mixed_4x1024chunks_256decode")
@@ -303,19 +309,22 @@ def measure_e2e(w, ds, host, steps, warmup, device, torch):
     return sum(times) / len(times), h2d, d2h
 
 
-def cpu_oracle_rate(w, budget_s: float, seed: int = 0):
+def cpu_oracle_rate(w, budget_s: float, seed: int = 0, host=None):
     """The oracle as it stands on a bounded seeded sample of (token, head)
-    rows of workload w: returns (rate in the metric's unit per second
-    numerator, seconds, sample description, threads)."""
+    rows of workload w, grown until one call takes about budget_s / 2.
+    Returns (FLOPs of the sampled rows, seconds, sample description, threads,
+    host inputs).  The seconds include the oracle's full K/V prologue."""
     import numpy as np
     import oracle
     from causal_gqa_attention_qkv_gb300 import inputs as gen
 
-    host = gen.make_inputs(w)
+    host = gen.make_inputs(w) if host is None else host
     cfg = oracle.cfg_of(w)
     g = np.random.default_rng(seed)
     all_tok = w.num_tokens
-    # grow the sample until it takes about budget_s
+    t0 = time.perf_counter()
+    oracle.step(cfg, host, rows=np.zeros((0, 2), dtype=np.int32))  # the K/V prologue alone
+    t_prologue = time.perf_counter() - t0
     count = 16
     while True:
         toks = g.integers(0, all_tok, size=count).astype(np.int32)
@@ -332,28 +341,58 @@ def cpu_oracle_rate(w, budget_s: float, seed: int = 0):
     b = np.searchsorted(cu, toks, side="right") - 1
     keys = cl[b] + (toks - cu[b]) + 1
     flops = 4.0 * w.head_dim * float(keys.sum())
+    cpu_oracle_rate.t_prologue = t_prologue
     return flops, dt, f"{count} random (token, head) rows of {w.name}, with the full K/V prologue", \
         oracle.num_threads(), host
 
 
-def cpu_oracle_decode_rate(w, budget_s: float):
+def cpu_oracle_decode_rate(w, budget_s: float, host=None):
+    """The oracle on every head of the first nb decode requests of w (nb grown
+    until one call takes about budget_s / 2).  Returns (algorithmic decode
+    bytes of those requests, seconds, description, threads)."""
     import numpy as np
     import oracle
     from causal_gqa_attention_qkv_gb300 import inputs as gen
 
-    host = gen.make_inputs(w)
+    host = gen.make_inputs(w) if host is None else host
     cfg = oracle.cfg_of(w)
+    lo = w.decode_from
     nb = 1
     while True:
-        rows = np.stack([np.repeat(np.arange(nb, dtype=np.int32), w.num_q_heads),
+        reqs = np.arange(lo, lo + nb, dtype=np.int64)
+        toks = host["cu_seqlens"].numpy()[reqs].astype(np.int32)
+        rows = np.stack([np.repeat(toks, w.num_q_heads),
                          np.tile(np.arange(w.num_q_heads, dtype=np.int32), nb)], 1)
         t0 = time.perf_counter()
         oracle.step(cfg, host, rows=rows)
         dt = time.perf_counter() - t0
-        if dt >= budget_s * 0.5 or nb >= w.batch:
+        if dt >= budget_s * 0.5 or nb >= w.batch - lo:
             break
-        nb = int(min(w.batch, max(nb * 2, nb * budget_s / max(dt, 1e-3) * 0.8)))
-    return decode_bytes(w, 0, nb), dt, f"all heads of the first {nb} requests of {w.name}", oracle.num_threads()
+        nb = int(min(w.batch - lo, max(nb * 2, nb * budget_s / max(dt, 1e-3) * 0.8)))
+    return decode_bytes(w, lo, lo + nb), dt, f"all heads of {nb} decode requests of {w.name}, with the full " \
+        "K/V prologue", oracle.num_threads()
+
+
+def cpu_baseline_prefill(w, budget_s, host, flops_total):
+    """cpu_baseline entry for a prefill workload: the oracle's TFLOP/s on a
+    row sample, and the full-workload oracle time extrapolated from it."""
+    f, dt, desc, cores, _ = cpu_oracle_rate(w, budget_s, host=host)
+    rate = f / dt
+    t_pro = min(cpu_oracle_rate.t_prologue, dt)
+    # full time = the prologue once + the attention rows at the sample's rate
+    full = t_pro + (dt - t_pro) * flops_total / f
+    return {"value": round(rate / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": desc, "seconds": round(dt, 2), "prologue_s": round(t_pro, 2),
+            "full_workload_s": round(full, 1), "full_workload_s_kind": "extrapolated"}
+
+
+def cpu_baseline_decode(w, budget_s, host, bytes_total):
+    b, dt, desc, cores = cpu_oracle_decode_rate(w, budget_s, host=host)
+    rate = b / dt
+    return {"value": round(rate / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc,
+            "seconds": round(dt, 2), "full_workload_s": round(bytes_total / rate, 2),
+            "full_workload_s_kind": "measured" if desc.startswith(f"all heads of {w.batch - w.decode_from} ")
+            else "extrapolated"}
 
 
 def measure_decode(wd, args, device, torch, dist_on, peaks, peak_kind, kv_dtype, entry_bytes,
@@ -378,7 +417,98 @@ def measure_decode(wd, args, device, torch, dist_on, peaks, peak_kind, kv_dtype,
                      "frac_of_8tbs_nominal": round(attend_bytes / (dattend * 1e-3) / 8e12, 4),
                      "traffic": recorded_traffic(traffic_kernel, source_sha("decode.cu", "common.cuh"))},
         "gpu_launches": md["launches"],
+        "host": md["host"],
     }
+
+
+def cpu_wanted(args) -> bool:
+    """The oracle baselines run on rank 0 of a single-process run only."""
+    return env_rank()[0] == 0 and env_rank()[2] == 1 and not args.no_cpu
+
+
+def measure_prefill(w, args, device, torch, dist_on, peaks, peak_kind, kv_dtype="bf16", e2e=False) -> dict:
+    """The prefill step (prepare + attention) of workload w: TFLOP/s of the
+    whole step, the attention kernel against the bf16 (f16 for an E4M3 cache)
+    tensor peak, and optionally the same step end to end from host buffers."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    m = measure(w, args.steps, args.warmup, device, torch, dist_on, args.page_size, kv_dtype)
+    step_ms, prep_ms, attend_ms = max_over_ranks([m["ms"]["step"], m["ms"]["prefill_append"],
+                                                  m["ms"]["prefill_attend"]], device)
+    flops = prefill_flops(w)
+    achieved = flops / (attend_ms * 1e-3) / 1e12
+    peak, peak_s = float(peaks["bf16_tflops"]), float(peaks.get("bf16_tflops_sustained", 0) or 0)
+    qkv_bytes = 2.0 * w.num_tokens * w.qkv_width * 2  # prepare: read qkv, write K, V and prepared Q
+    sha = source_sha("prefill_tc.cu", "tcgen05.cuh", "common.cuh")
+    res = {
+        "value": round(whole_job_rate(flops, world, step_ms) / 1e12, 3), "unit": "TFLOP/s",
+        "ms_per_step": round(step_ms, 4), "workload": w.name, "kv_dtype": kv_dtype,
+        "tokens": w.num_tokens, "attended_pairs": w.attended_pairs(), "flops_per_step": flops,
+        "parts_ms": {"prologue": round(prep_ms, 4), "prefill_attention": round(attend_ms, 4)},
+        "roofline": {"bound": "tensor",
+                     "kernel": "prefill attention" + (" (E4M3 cache)" if kv_dtype == "e4m3" else ""),
+                     "achieved": round(achieved, 3), "peak": peak, "peak_kind": f"bf16_tflops ({peak_kind})",
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "frac_of_sustained": round(achieved / peak_s, 4) if peak_s else None,
+                     "traffic": recorded_traffic(f"prefill_attention_{w.name}" + ("_e4m3" if kv_dtype == "e4m3"
+                                                                                  else ""), sha),
+                     "flops_per_launch": flops},
+        "prologue_roofline": {"bound": "hbm", "kernel": "kv_append_kernel (prefill prepare)",
+                              "bytes_per_launch": qkv_bytes,
+                              "achieved": round(qkv_bytes / (prep_ms * 1e-3) / 1e9, 1),
+                              "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                              "frac": round(qkv_bytes / (prep_ms * 1e-3) / 1e9 / float(peaks["hbm_gbs"]), 4)},
+        "gpu_launches": m["launches"],
+    }
+    if e2e:
+        e2e_ms, h2d, d2h = measure_e2e(w, m["ds"], m["host"], max(3, args.steps // 2), 2, device, torch)
+        (e2e_ms,) = max_over_ranks([e2e_ms], device)
+        res["e2e"] = {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                      "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        res["gpu_launches"] += 2 * (max(3, args.steps // 2) + 2)
+    res["host"] = m["host"]
+    del m
+    return res
+
+
+def measure_tiny(args, device, torch, dist_on) -> dict:
+    """The tiny workload (12-token prompt, Hq 4 / Hkv 2 / D 64, then the
+    decode step at position 12): microseconds per call through the public
+    calls, launch-latency bound (5 warm-up calls, then the median of the
+    timed ones, each bracketed by CUDA events)."""
+    from causal_gqa_attention_qkv_gb300 import inputs as gen
+    from causal_gqa_attention_qkv_gb300 import step
+    w = gen.tiny()
+    host = gen.make_inputs(w)
+    pre = step.upload(w, host, device=device)
+    dw = gen.custom("tiny_decode", w.num_q_heads, w.num_kv_heads, w.head_dim, [1], [12], seed=0, decode_from=0)
+    dhost = dict(host, qkv=gen.make_followup_decode_qkv(w), cu_seqlens=torch.tensor([0, 1], dtype=torch.int32),
+                 cache_lens=torch.tensor([12], dtype=torch.int32))
+    dec = step.upload(dw, dhost, device=device)
+    res = {"workload": w.name, "unit": "us per call"}
+    launches = 0
+    for key, ds in (("prefill_us", pre), ("decode_us", dec)):
+        for _ in range(max(5, args.warmup)):
+            ds.run()
+        torch.cuda.synchronize()
+        if dist_on:
+            torch.distributed.barrier()
+        times = []
+        for _ in range(args.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            ds.run()
+            e1.record()
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3)
+        (us,) = max_over_ranks([statistics.median(times)], device)
+        res[key] = round(us, 2)
+        launches += ds.launches() * args.steps
+        if ds.status() != 0:
+            raise RuntimeError("device status set on the tiny workload")
+    res["gpu_launches"] = launches
+    res["host"] = host
+    res["decode_host"] = dhost
+    return res
 
 
 def measure_sampling(args, device, torch, dist_on, peaks, peak_kind, B=64) -> dict:
@@ -443,6 +573,7 @@ def measure_mixed(wm, args, device, torch, dist_on, peaks, peak_kind) -> dict:
         "chunk_attention_tflops": round(fl / (pa * 1e-3) / 1e12, 2),
         "decode_attention_gbs": round(attend_bytes / (dd * 1e-3) / 1e9, 1),
         "gpu_launches": mm["launches"],
+        "host": mm["host"],
     }
 
 
@@ -464,21 +595,17 @@ def run_ours(args):
         torch.distributed.barrier()
     attn.load()
     peaks, peak_kind = load_peaks()
+    cpu = cpu_wanted(args)
+    pop = lambda d, *ks: [d.pop(k, None) for k in ks][0]
     w = gen.ALL[args.workload]
     assert w.decode_from == w.batch, "the headline workload is a prefill workload"
     with ClockSampler(local_rank) as clk:
-        m = measure(w, args.steps, args.warmup, device, torch, dist_on, args.page_size)
+        head = measure_prefill(w, args, device, torch, dist_on, peaks, peak_kind, e2e=True)
     clocks = clk.summary()
-    step_ms, attend_ms = max_over_ranks([m["ms"]["step"], m["ms"]["prefill_attend"]], device)
-    flops = prefill_flops(w)
-    value = whole_job_rate(flops, world, step_ms) / 1e12
-    achieved = flops / (attend_ms * 1e-3) / 1e12
-    peak = float(peaks["bf16_tflops"])
-    sha = source_sha("prefill_tc.cu", "tcgen05.cuh", "common.cuh")
-    e2e_ms, h2d, d2h = measure_e2e(w, m["ds"], m["host"], max(3, args.steps // 2), 2, device, torch)
+    host = pop(head, "host")
     line = {
-        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+        "metric": METRIC, "value": head["value"], "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) qkv, norm weights 1+0.1N(0,1), no trained weights)",
         "config": {"workload": w.name, "global_batch": w.batch * world, "seq_len": max(w.new_lens),
@@ -486,48 +613,63 @@ def run_ours(args):
                    "head_dim": w.head_dim, "attended_pairs": w.attended_pairs(),
                    "parallelism": f"replicas{world}", "l2": "flushed before every timed step",
                    "kv_layout": f"paged{args.page_size}" if args.page_size else "contiguous"},
-        "parts_ms": {"prologue": round(m["ms"]["prefill_append"], 4),
-                     "prefill_attention": round(attend_ms, 4)},
-        "roofline": {"bound": "tensor", "kernel": "prefill attention", "achieved": round(achieved, 3),
-                     "peak": peak, "peak_kind": f"bf16_tflops ({peak_kind})", "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": recorded_traffic("prefill_attention", sha),
-                     "flops_per_launch": flops},
-        "gpu_launches": m["launches"],
-        "e2e": {"value": round(flops * world / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "clocks": clocks,
+        "parts_ms": head["parts_ms"], "roofline": head["roofline"],
+        "prologue_roofline": head["prologue_roofline"],
+        "gpu_launches": head["gpu_launches"], "e2e": head["e2e"], "clocks": clocks,
     }
-    # the same prefill over a one-byte (E4M3) cache: tiles converted to f16 on chip
-    me = measure(w, args.steps, args.warmup, device, torch, dist_on, args.page_size, "e4m3")
-    e_step, e_attend = max_over_ranks([me["ms"]["step"], me["ms"]["prefill_attend"]], device)
-    line["prefill_e4m3"] = {
-        "value": round(whole_job_rate(flops, world, e_step) / 1e12, 3), "unit": "TFLOP/s",
-        "ms_per_step": round(e_step, 4), "kv_dtype": "e4m3",
-        "parts_ms": {"prologue": round(me["ms"]["prefill_append"], 4), "prefill_attention": round(e_attend, 4)},
-        "roofline": {"bound": "tensor", "kernel": "prefill attention (E4M3 cache)",
-                     "achieved": round(flops / (e_attend * 1e-3) / 1e12, 3), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(flops / (e_attend * 1e-3) / 1e12 / peak, 4)},
-        "gpu_launches": me["launches"],
-    }
-    line["gpu_launches"] += me["launches"]
-    del me
+    if cpu:
+        line["cpu_baseline"] = cpu_baseline_prefill(w, args.cpu_seconds, host, head["flops_per_step"])
+    del host
+    # the Qwen3-4B-shaped prefill, over bf16 and over one-byte (E4M3) caches
+    wp = gen.ALL[args.prefill_workload]
+    for key, kvd in (("qwen3_4b_prefill", "bf16"), ("prefill_e4m3", "e4m3")):
+        r = measure_prefill(wp, args, device, torch, dist_on, peaks, peak_kind, kv_dtype=kvd, e2e=kvd == "bf16")
+        h = pop(r, "host")
+        if cpu and kvd == "bf16":
+            r["cpu_baseline"] = cpu_baseline_prefill(wp, args.cpu_seconds / 2, h, r["flops_per_step"])
+        line[key] = r
+        line["gpu_launches"] += r["gpu_launches"]
+        del h
     if not args.no_decode:
         wd = gen.ALL[args.decode_workload]
         for key, kvd, eb, kname in (("decode", "bf16", 2, "decode_split"),
                                     ("decode_e4m3", "e4m3", 1, "decode_split_e4m3")):
-            line[key] = measure_decode(wd, args, device, torch, dist_on, peaks, peak_kind, kvd, eb, kname)
-            line["gpu_launches"] += line[key]["gpu_launches"]
+            r = measure_decode(wd, args, device, torch, dist_on, peaks, peak_kind, kvd, eb, kname)
+            h = pop(r, "host")
+            if cpu and kvd == "bf16":
+                r["cpu_baseline"] = cpu_baseline_decode(wd, args.cpu_seconds / 2, h, r["bytes_per_step"])
+            line[key] = r
+            line["gpu_launches"] += r["gpu_launches"]
     if not args.no_mixed:
-        line["mixed"] = measure_mixed(gen.ALL[args.mixed_workload], args, device, torch, dist_on, peaks,
-                                      peak_kind)
-        line["gpu_launches"] += line["mixed"]["gpu_launches"]
+        wm = gen.ALL[args.mixed_workload]
+        r = measure_mixed(wm, args, device, torch, dist_on, peaks, peak_kind)
+        h = pop(r, "host")
+        if cpu:
+            r["cpu_baseline"] = cpu_baseline_prefill(wm, args.cpu_seconds / 2, h, prefill_flops(wm))
+            r["cpu_baseline"]["sample"] += " (chunk and decode rows alike; FLOPs over all attended pairs)"
+        line["mixed"] = r
+        line["gpu_launches"] += r["gpu_launches"]
+    r = measure_tiny(args, device, torch, dist_on)
+    h, dh = pop(r, "host"), pop(r, "decode_host")
+    if cpu:
+        import oracle
+        wt = gen.tiny()
+        cfg = oracle.cfg_of(wt)
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < 0.5:
+            oracle.step(cfg, h)
+            oracle.step(cfg, dh)
+            reps += 1
+        per = (time.perf_counter() - t0) / reps
+        r["cpu_baseline"] = {"value": round(per * 1e6, 1), "unit": "us per prefill + decode", "cores":
+                             oracle.num_threads(), "kind": "oracle", "sample": f"the whole workload, {reps} times",
+                             "full_workload_s_kind": "measured"}
+    line["tiny"] = r
+    line["gpu_launches"] += r["gpu_launches"]
     if not args.no_sampling:
         line["sampling"] = measure_sampling(args, device, torch, dist_on, peaks, peak_kind)
         line["gpu_launches"] += line["sampling"]["gpu_launches"]
-    if rank == 0 and world == 1 and not args.no_cpu:
-        flops_s, dt, desc, cores, _ = cpu_oracle_rate(w, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": round(flops_s / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
-                                "kind": "oracle", "sample": desc, "seconds": round(dt, 2)}
     if dist_on:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
@@ -542,10 +684,11 @@ def run_reference(args):
     from causal_gqa_attention_qkv_gb300 import inputs as gen
     w = gen.ALL[args.workload]
     per_step = max(1.0, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
+    host = gen.make_inputs(w)
     rates = []
     desc = cores = None
     for k in range(args.warmup + args.steps):
-        flops, dt, desc, cores, _ = cpu_oracle_rate(w, per_step, seed=k)
+        flops, dt, desc, cores, _ = cpu_oracle_rate(w, per_step, seed=k, host=host)
         if k >= args.warmup:
             rates.append((flops, dt))
     tot_f = sum(f for f, _ in rates)
@@ -557,9 +700,15 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)",
         "config": {"workload": w.name, "global_batch": w.batch, "seq_len": max(w.new_lens),
-                   "tokens": w.num_tokens, "parallelism": "host cores (OpenMP)"},
+                   "tokens": w.num_tokens, "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+                   "head_dim": w.head_dim, "attended_pairs": w.attended_pairs(),
+                   "parallelism": "host cores (OpenMP)"},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": desc + " per step"},
+                         "sample": desc + " per step",
+                         "full_workload_s": round(cpu_oracle_rate.t_prologue + (tot_t / len(rates) -
+                                                   cpu_oracle_rate.t_prologue) * prefill_flops(w) /
+                                                  (tot_f / len(rates)), 1),
+                         "full_workload_s_kind": "extrapolated"},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -65,6 +65,7 @@ EXPORTS = {
     "attn_prefill_attend": (ctypes.c_int, [_CFG, _P, _P, _I32, _I32, _I32, _KV, _P, _P, _SZ, _P]),
     "attn_decode_attend": (ctypes.c_int, [_CFG, _P, _P, _I32, _I32, _KV, _P, _P, _SZ, _P]),
     "attn_decode_static_scratch": (ctypes.c_int, [_CFG, _P, _P, _P, _I32, _I32, _KV, _P, _P, _P]),
+    "attn_decode_splits": (_I32, [_CFG, _I32, _I32]),
     "attn_get_status": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "attn_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "attn_sample_tokens": (ctypes.c_int, [_P, _I32, _I32, ctypes.c_int64, _P, _P, _P, _P, _P, _P]),
@@ -139,14 +140,13 @@ class KVCache:
                       ATTN_KV_E4M3 if fp8 else ATTN_KV_BF16, float(self.k_scale), float(self.v_scale))
 
 
-def decode_max_splits(B: int, num_kv_heads: int, max_kv_len: int) -> int:
-    """Number of KV splits attn_decode uses for its longest request (mirrors
-    the library's split policy: about 2048 CTAs when every request is at its
-    longest, splits of at least 256 keys, at most 16 splits, 64-key multiples)."""
-    target = 2048
-    ln = max((max_kv_len * B * num_kv_heads + target - 1) // target, 256, (max_kv_len + 15) // 16)
-    ln = (ln + 63) // 64 * 64
-    return max(1, (max_kv_len + ln - 1) // ln)
+def decode_splits(cfg: AttnConfig, B: int, max_cache_len: int) -> int:
+    """Number of KV splits attn_decode uses for its longest request (the
+    library's own policy, attn_decode_splits)."""
+    n = load().attn_decode_splits(ctypes.byref(cfg), int(B), int(max_cache_len))
+    if n < 0:
+        raise AttnError(int(n), load().attn_strerror(int(n)).decode())
+    return int(n)
 
 
 def workspace_size(cfg: AttnConfig, max_tokens: int, max_batch: int, max_kv_len: int) -> int:

@@ -94,7 +94,10 @@ int check_device() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// Split-KV partials of a decode call.  With one split per request the split
+// kernel writes the output directly and the partials are never touched.
 size_t partial_bytes(const attn_config_t& c, int64_t B, int max_splits) {
+  if (max_splits <= 1) return 0;
   size_t rows = (size_t)B * c.num_q_heads * max_splits;
   return align_up(rows * c.head_dim * 4, 256) + align_up(rows * 2 * 4, 256);
 }
@@ -245,6 +248,13 @@ size_t attn_workspace_size(const attn_config_t* cfg, int32_t max_tokens, int32_t
   return std::max(prefill, decode);
 }
 
+int32_t attn_decode_splits(const attn_config_t* cfg, int32_t B, int32_t max_cache_len) {
+  if (check_config(cfg) != ATTN_OK || B < 0 || max_cache_len < 0) return ATTN_EINVAL;
+  int max_splits = 1;
+  decode_split_len(std::max(B, 1), cfg->num_kv_heads, max_cache_len + 1, &max_splits);
+  return max_splits;
+}
+
 int attn_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
   if (!ws_ok(workspace, ws_bytes, kWsHeader)) return ATTN_EWORKSPACE;
   return cudaMemsetAsync(workspace, 0, kWsHeader, static_cast<cudaStream_t>(stream)) == cudaSuccess
@@ -347,11 +357,14 @@ int attn_decode(const attn_config_t* cfg, const void* qkv, const void* q_norm_w,
 int attn_get_status(void* workspace, void* stream, int32_t* status) {
   if (!workspace || !status) return ATTN_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ELAUNCH;
-  if (cudaMemcpy(status, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+  // ordered on the caller's stream only (a plain cudaMemcpy would also wait
+  // for every blocking stream through the legacy default stream)
+  int32_t word = 0;
+  if (cudaMemcpyAsync(&word, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return ATTN_ELAUNCH;
   if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), s) != cudaSuccess) return ATTN_ELAUNCH;
   if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ELAUNCH;
+  *status = word;
   return ATTN_OK;
 }
 

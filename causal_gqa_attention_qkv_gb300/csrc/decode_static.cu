@@ -65,9 +65,11 @@ extern "C" int attn_decode_static_scratch(const attn_config_t* cfg, const void* 
   int max_splits = 1;
   const int split_len =
       decode_split_len(std::max(B, 1), cfg->num_kv_heads, max_cache_len + 1, &max_splits);
+  // With one split per request the split kernel writes `out` directly and no
+  // partial result is stored: such calls need no scratch at all.
   const size_t rows = (size_t)B * cfg->num_q_heads * max_splits;
   const size_t o_bytes = align_up(rows * cfg->head_dim * 4, 256);
-  const size_t need = o_bytes + align_up(rows * 2 * 4, 256);
+  const size_t need = max_splits > 1 ? o_bytes + align_up(rows * 2 * 4, 256) : 0;
   if (need > kStaticScratchBytes) return ATTN_ESCRATCH;
   if ((rc = abi_check_device())) return rc;
   if (B == 0) return ATTN_OK;

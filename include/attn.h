@@ -206,6 +206,15 @@ ATTN_API int attn_decode(const attn_config_t* cfg, const void* qkv, const void* 
                 const void* k_norm_w, int32_t B, int32_t max_cache_len, const attn_kv_t* kv,
                 void* out, void* workspace, size_t ws_bytes, void* stream);
 
+/* Number of KV splits attn_decode (and attn_decode_attend,
+ * attn_decode_static_scratch) uses for the longest request of a call with B
+ * requests and host bound max_cache_len: the split length is chosen so that
+ * about 2048 CTAs run when every request is at its longest, with at least 256
+ * keys and at most 16 splits per request.  1 means every output row is
+ * written by the split kernel directly (no partials, no merge launch).
+ * Returns ATTN_EINVAL (< 0) for invalid arguments.  Host-only. */
+ATTN_API int32_t attn_decode_splits(const attn_config_t* cfg, int32_t B, int32_t max_cache_len);
+
 /* Attention half of attn_decode (the cache must already hold the new
  * token's K/V at slot slot_base[b] + c_b).  attn_decode == attn_kv_append
  * (cu_seqlens = 0, 1, ..., B) followed by attn_decode_attend. */
@@ -220,14 +229,18 @@ ATTN_API int attn_decode_attend(const attn_config_t* cfg, const void* qkv, const
  * as attn_decode, except that the split-KV partial results live in a
  * library-owned static device array of 16 MiB per GPU (held by every GPU that
  * loads the library until the process exits) instead of a workspace.
- *   - Requests whose partials need more than that (B * Hq * splits * (D + 2)
- *     * 4 bytes, splits as chosen by attn_decode) return ATTN_ESCRATCH and
- *     launch nothing.
+ *   - With splits = attn_decode_splits(cfg, B, max_cache_len) > 1 the
+ *     partials take B * Hq * splits * (D + 2) * 4 bytes (each of the two
+ *     arrays rounded up to 256 bytes); requests needing more than the array
+ *     return ATTN_ESCRATCH and launch nothing.  With splits == 1 every output
+ *     row is written directly and the call needs no scratch at any B.
  *   - device_status: optional caller-owned device int32 (NULL: not recorded)
  *     that receives the ATTN_STATUS_* bits; the caller zeroes it.
  *   - The first call on a device looks up the array's device address on the
- *     current device (cudaGetSymbolAddress); make that first call before any
- *     stream capture.
+ *     current device (cudaGetSymbolAddress) and keeps it for the process;
+ *     make that first call before any stream capture, and after any
+ *     cudaDeviceReset of that device (a reset after it leaves the kept
+ *     address stale: do not reset a device that has used this call).
  *   - All calls share the array: calls that overlap on the GPU race.
  *   - Allocates nothing (no cudaMalloc, no cudaFree, no allocating library
  *     call).
@@ -238,8 +251,9 @@ ATTN_API int attn_decode_static_scratch(const attn_config_t* cfg, const void* qk
                                         int32_t max_cache_len, const attn_kv_t* kv, void* out,
                                         int32_t* device_status, void* stream);
 
-/* Synchronise `stream`, copy the status word to *status (host pointer) and
- * clear it.  Returns ATTN_OK or ATTN_ELAUNCH. */
+/* Read the status word into *status (host pointer) and clear it, both
+ * ordered on `stream`, then synchronise that stream (only that stream).
+ * Returns ATTN_OK or ATTN_ELAUNCH. */
 ATTN_API int attn_get_status(void* workspace, void* stream, int32_t* status);
 
 /* Static string for an ATTN_E* code. */

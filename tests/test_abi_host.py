@@ -106,14 +106,26 @@ def test_null_and_alignment_rejected(lib):
     assert lib.attn_get_status(None, None, None) == -1
 
 
-@pytest.mark.parametrize("B,max_kv", [(1, 13), (5, 3001), (64, 8193), (256, 16385), (8, 300)])
-def test_decode_split_mirror_matches_library(lib, B, max_kv):
+@pytest.mark.parametrize("B,max_cache", [(1, 12), (5, 3000), (64, 8192), (256, 16384), (8, 299),
+                                         (1024, 300), (127, 65535), (4096, 65535)])
+def test_decode_splits_and_workspace_size(lib, B, max_cache):
+    """attn_decode_splits follows its documented policy (at most 16 splits,
+    at least 256 keys per split when a request is split, about 2048 CTAs at
+    the longest length), and the workspace holds the partials only when a
+    request is split."""
     from causal_gqa_attention_qkv_gb300 import attn
     cfg = attn.config(32, 8, 128)
-    ms = attn.decode_max_splits(B, 8, max_kv)
+    ms = attn.decode_splits(cfg, B, max_cache)
+    max_kv = max_cache + 1
+    assert 1 <= ms <= 16
+    assert (ms - 1) * 256 < max_kv  # every split but the last holds at least 256 keys
+    if B * 8 * 2 <= 2048 // 2 and max_kv >= 16 * 256:
+        assert ms > 1  # few CTAs and long requests: the keys are split
     al = lambda x: (x + 255) // 256 * 256
-    expect = 256 + al(B * 32 * ms * 128 * 4) + al(B * 32 * ms * 2 * 4)
-    assert attn.workspace_size(cfg, 1, B, max_kv) == max(expect, 256 + al(32 * 128 * 2))
+    partials = al(B * 32 * ms * 128 * 4) + al(B * 32 * ms * 2 * 4) if ms > 1 else 0
+    assert attn.workspace_size(cfg, 1, B, max_kv) == 256 + max(partials, al(32 * 128 * 2))
+    assert lib.attn_decode_splits(ctypes.byref(cfg), -1, 5) < 0
+    assert lib.attn_decode_splits(None, 1, 5) < 0
 
 
 @pytest.mark.parametrize("page_size,ppr", [(48, 4), (32, 4), (96, 4), (128, 0), (0, 4)])

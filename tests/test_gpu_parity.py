@@ -1,7 +1,10 @@
 """GPU parity: the CUDA path through the C ABI against the CPU oracle on the
 same seeded inputs.  Outputs: max-abs <= 2e-2 and relative Frobenius <= 1e-2
-(bf16 outputs, fp32 accumulation); caches: V bit-exact, K within one bf16
-step, every slot outside the appended ones unchanged."""
+(bf16 outputs, fp32 accumulation); caches: V bit-exact, K within half a bf16
+step of each side plus the derived fp32 error of the norm and rotation, every
+slot outside the appended ones unchanged.  Full-size prefill workloads are
+checked on every head of the last 256 positions of each sequence plus 2048
+seeded random (token, head) rows."""
 import numpy as np
 import pytest
 import torch
@@ -341,13 +344,13 @@ def test_full_decode_batch_all_rows():
 
 def test_full_long_prefill_sampled():
     w = gen.long_prefill()
-    run_and_compare(w, gen.make_inputs(w), rows=_sampled(w, tail=24, count=1024, seed=3))
+    run_and_compare(w, gen.make_inputs(w), rows=_sampled(w, tail=256, count=2048, seed=3))
 
 
 def test_full_mixed_step_sampled():
     w = gen.mixed_step()
     host = gen.make_inputs(w)
-    rows = _sampled(w, tail=16, count=1024, seed=4)
+    rows = _sampled(w, tail=256, count=2048, seed=4)
     run_and_compare(w, host, rows=rows)
 
 
