@@ -66,6 +66,8 @@ EXPORTS = {
     "attn_decode_attend": (ctypes.c_int, [_CFG, _P, _P, _I32, _I32, _KV, _P, _P, _SZ, _P]),
     "attn_decode_static_scratch": (ctypes.c_int, [_CFG, _P, _P, _P, _I32, _I32, _KV, _P, _P, _P]),
     "attn_decode_splits": (_I32, [_CFG, _I32, _I32]),
+    "attn_qkv_proj_prepare": (ctypes.c_int, [_CFG, _P, _I32, _P, _P, _P, _P, _I32, _I32, _KV, _P, _P, _SZ, _P]),
+    "attn_o_proj": (ctypes.c_int, [_CFG, _P, _I32, _P, _I32, _P, _P, _SZ, _P]),
     "attn_get_status": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "attn_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "attn_sample_tokens": (ctypes.c_int, [_P, _I32, _I32, ctypes.c_int64, _P, _P, _P, _P, _P, _P]),
@@ -239,6 +241,29 @@ def decode_static_scratch(cfg: AttnConfig, qkv, q_norm_w, k_norm_w, max_cache_le
         ctypes.byref(cfg), _bf16(qkv, "qkv"), _bf16(q_norm_w, "q_norm_w"), _bf16(k_norm_w, "k_norm_w"),
         qkv.shape[0], int(max_cache_len), ctypes.byref(s), _bf16(out, "out"), _ptr(device_status),
         _stream(stream)))
+
+
+def qkv_proj_prepare(cfg: AttnConfig, hidden, w_qkv, q_norm_w, k_norm_w, cu_seqlens, kv: KVCache, q_out,
+                     workspace, stream=None):
+    """The merged Q/K/V projection fused with ``prefill_prepare``: qkv =
+    hidden [N, C] . w_qkv^T in fp32, then Q/K norm + RoPE, K/V appended,
+    prepared Q written to ``q_out`` [N, Hq, D]."""
+    assert hidden.dim() == 2 and w_qkv.dim() == 2 and w_qkv.shape[1] == hidden.shape[1]
+    B = cu_seqlens.numel() - 1
+    s = kv.struct()
+    _check(load().attn_qkv_proj_prepare(ctypes.byref(cfg), _bf16(hidden, "hidden"), hidden.shape[1],
+                                        _bf16(w_qkv, "w_qkv"), _bf16(q_norm_w, "q_norm_w"),
+                                        _bf16(k_norm_w, "k_norm_w"), _ptr(cu_seqlens), B, hidden.shape[0],
+                                        ctypes.byref(s), _ptr(q_out), _ptr(workspace), workspace.numel(),
+                                        _stream(stream)))
+
+
+def o_proj(cfg: AttnConfig, attn_out, w_o, out, workspace, stream=None):
+    """out [N, C] = attn_out [N, Hq*D] . w_o^T (w_o [C, Hq*D])."""
+    assert w_o.dim() == 2 and out.shape == (attn_out.shape[0], w_o.shape[0])
+    _check(load().attn_o_proj(ctypes.byref(cfg), _bf16(attn_out, "attn_out"), attn_out.shape[0],
+                              _bf16(w_o, "w_o"), w_o.shape[0], _bf16(out, "out"), _ptr(workspace),
+                              workspace.numel(), _stream(stream)))
 
 
 def get_status(workspace, stream=None) -> int:

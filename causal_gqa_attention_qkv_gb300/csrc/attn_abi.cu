@@ -139,6 +139,19 @@ int make_qkv_map(const void* qkv, int N, int Htot, int D, int G, int BT, CUtenso
   return r == CUDA_SUCCESS ? 0 : -1;
 }
 
+int make_matrix_map(const void* base, int64_t rows, int64_t cols, int box_rows, CUtensorMap* m) {
+  auto enc = encoder();
+  if (!enc) return -1;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -1;
+}
+
 int make_cache_maps(const attn_kv_t& kv, int Hkv, int D, int box_rows, CacheMaps* maps) {
   const bool f8 = kv.kv_dtype == ATTN_KV_E4M3;
   if (encode_cache_map(kv.k_cache, kv.num_slots, Hkv, D, box_rows, f8, &maps->k) != 0) return -1;
@@ -352,6 +365,47 @@ int attn_decode(const attn_config_t* cfg, const void* qkv, const void* q_norm_w,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((rc = append(cfg, qkv, nullptr, k_norm_w, nullptr, B, B, kv, nullptr, workspace, s))) return rc;
   return decode_attend(cfg, qkv, q_norm_w, B, max_cache_len, kv, out, workspace, s);
+}
+
+int attn_qkv_proj_prepare(const attn_config_t* cfg, const void* hidden, int32_t hidden_size, const void* w_qkv,
+                          const void* q_norm_w, const void* k_norm_w, const int32_t* cu_seqlens, int32_t B,
+                          int32_t N, const attn_kv_t* kv, void* q_out, void* workspace, size_t ws_bytes,
+                          void* stream) {
+  int rc = check_common(cfg, kv, hidden, q_norm_w, q_out);
+  if (rc) return rc;
+  if (!w_qkv || !aligned16(w_qkv) || !k_norm_w || !aligned16(k_norm_w)) return ATTN_EINVAL;
+  if (!cu_seqlens || B < 0 || N < 0 || hidden_size <= 0 || hidden_size % 8 != 0) return ATTN_EINVAL;
+  if (!ws_ok(workspace, ws_bytes, kWsHeader)) return ATTN_EWORKSPACE;
+  if ((rc = check_device())) return rc;
+  if (N == 0 || B == 0) return ATTN_OK;
+  QkvProjArgs a;
+  a.cfg = *cfg;
+  a.hidden = hidden;
+  a.C = hidden_size;
+  a.w_qkv = w_qkv;
+  a.q_norm_w = q_norm_w;
+  a.k_norm_w = k_norm_w;
+  a.cu_seqlens = cu_seqlens;
+  a.B = B;
+  a.N = N;
+  a.kv = *kv;
+  a.q_out = q_out;
+  a.status = status_of(workspace);
+  make_rope_freqs(cfg->rope_theta, cfg->head_dim, &a.freqs);
+  return launch_qkv_proj(a, static_cast<cudaStream_t>(stream));
+}
+
+int attn_o_proj(const attn_config_t* cfg, const void* attn_out, int32_t N, const void* w_o, int32_t hidden_size,
+                void* out, void* workspace, size_t ws_bytes, void* stream) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  if (!attn_out || !w_o || !out || !aligned16(attn_out) || !aligned16(w_o) || !aligned16(out)) return ATTN_EINVAL;
+  if (N < 0 || hidden_size <= 0 || hidden_size % 8 != 0) return ATTN_EINVAL;
+  if (!ws_ok(workspace, ws_bytes, kWsHeader)) return ATTN_EWORKSPACE;
+  if ((rc = check_device())) return rc;
+  if (N == 0) return ATTN_OK;
+  return launch_linear(attn_out, w_o, out, N, hidden_size, cfg->num_q_heads * cfg->head_dim, status_of(workspace),
+                       static_cast<cudaStream_t>(stream));
 }
 
 int attn_get_status(void* workspace, void* stream, int32_t* status) {

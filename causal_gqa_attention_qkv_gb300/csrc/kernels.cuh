@@ -88,6 +88,33 @@ struct PrefillArgs {
 };
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 
+// Row-major bf16 matrix [rows, cols] as a 2-D tensor map with 128-byte
+// swizzled boxes of 64 columns x box_rows rows (cols % 8 == 0).
+int make_matrix_map(const void* base, int64_t rows, int64_t cols, int box_rows, CUtensorMap* map);
+
+// y [M, N] = x [M, K] . w[N, K]^T, bf16 in and out, fp32 accumulation on the
+// tensor cores (N % 8 == 0, K % 8 == 0, 16-byte aligned pointers).
+int launch_linear(const void* x, const void* w, void* y, int32_t M, int32_t N, int32_t K, int32_t* status,
+                  cudaStream_t stream);
+
+// qkv = hidden [N, C] . w_qkv[(Hq+2Hkv)D, C]^T kept in fp32 and handed to the
+// prologue: Q/K RMSNorm + RoPE, K/V append, prepared Q into q_out [N, Hq, D].
+struct QkvProjArgs {
+  attn_config_t cfg;
+  const void* hidden;
+  int32_t C;
+  const void* w_qkv;
+  const void* q_norm_w;
+  const void* k_norm_w;
+  const int32_t* cu_seqlens;
+  int32_t B, N;
+  attn_kv_t kv;
+  void* q_out;
+  int32_t* status;
+  RopeFreqs freqs;
+};
+int launch_qkv_proj(const QkvProjArgs& a, cudaStream_t stream);
+
 // One token per row of logits (include/sample.h); arguments checked by the caller.
 int launch_sample(const float* logits, int32_t B, int32_t V, int64_t ld, const float* temperature,
                   const int32_t* top_k, const float* top_p, const float* uniform, int32_t* tokens,

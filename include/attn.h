@@ -206,6 +206,37 @@ ATTN_API int attn_decode(const attn_config_t* cfg, const void* qkv, const void* 
                 const void* k_norm_w, int32_t B, int32_t max_cache_len, const attn_kv_t* kv,
                 void* out, void* workspace, size_t ws_bytes, void* stream);
 
+/* The merged Q/K/V projection fused with the first half of attn_prefill.
+ * Code walkthrough section 3.3 (AttentionLayer.forward: qkv_proj of the
+ * hidden states, then the split, the Q/K norms and RoPE) and transformer
+ * basics "Attention calculation: part 1" (the q/k/v projections of the hidden
+ * states, a linear layer y = x W^T).
+ *   qkv = hidden [N, C] . w_qkv^T, w_qkv [(Hq + 2 Hkv) * D, C] (the linear
+ *   layer's weight, row = output feature), bf16 in, fp32 accumulation on the
+ *   tensor cores.  The fp32 qkv is never stored or rounded: each Q and K head
+ *   is RMS-normalised and rotated from the accumulators, V rounded once, and
+ *   then exactly as attn_prefill_prepare: K and V appended to the cache (bf16
+ *   or E4M3 codes), the prepared Q written to q_out [N, Hq, D] (bf16, f16 next
+ *   to an E4M3 cache; 16-byte aligned), ready for attn_prefill_attend.
+ * hidden, w_qkv: bf16, row-major, 16-byte aligned; C = hidden_size, a
+ * multiple of 8.  cu_seqlens, B, N and kv as for attn_prefill; decode rows
+ * are requests with n_b = 1.  The workspace needs only its 256-byte header
+ * (status word). */
+ATTN_API int attn_qkv_proj_prepare(const attn_config_t* cfg, const void* hidden, int32_t hidden_size,
+                                   const void* w_qkv, const void* q_norm_w, const void* k_norm_w,
+                                   const int32_t* cu_seqlens, int32_t B, int32_t N, const attn_kv_t* kv,
+                                   void* q_out, void* workspace, size_t ws_bytes, void* stream);
+
+/* The output projection after the attention (code walkthrough section 3.3:
+ * o_proj; transformer basics "Attention calculation: part 1"):
+ *   out [N, C] = attn_out [N, Hq * D] . w_o^T, w_o [C, Hq * D] (row = output
+ *   feature), bf16 in and out, fp32 accumulation on the tensor cores.
+ * attn_out is the output of attn_prefill / attn_decode; C = hidden_size, a
+ * multiple of 8; all pointers 16-byte aligned.  The workspace needs only its
+ * 256-byte header (status word). */
+ATTN_API int attn_o_proj(const attn_config_t* cfg, const void* attn_out, int32_t N, const void* w_o,
+                         int32_t hidden_size, void* out, void* workspace, size_t ws_bytes, void* stream);
+
 /* Number of KV splits attn_decode (and attn_decode_attend,
  * attn_decode_static_scratch) uses for the longest request of a call with B
  * requests and host bound max_cache_len: the split length is chosen so that
