@@ -13,8 +13,9 @@ query-key pairs, diagonal included).  Every other workload is measured in the
 same run under its own key: the Qwen3-4B-shaped prefill (8 packed sequences,
 lengths U[256, 2048]), the 64-request decode batch (KV-read GB/s, the decode
 half of the metric), both over bf16 and one-byte E4M3 caches, the mixed
-prefill-chunk + decode step, the tiny 12-token workload (microseconds per
-call) and token sampling.  Inputs are seeded synthetic tensors resident in
+prefill-chunk + decode step, the attention layer with its Q/K/V and output
+projections (Qwen3-4B hidden size 2560), the tiny 12-token workload
+(microseconds per call) and token sampling.  Inputs are seeded synthetic tensors resident in
 HBM; L2 is flushed (a 256 MiB write) before every timed step, outside the
 timed events.
 
@@ -56,6 +57,7 @@ def parse_args():
     ap.add_argument("--mixed-workload", default="mixed_4x1024chunks_256decode")
     ap.add_argument("--no-mixed", action="store_true", help="skip the mixed-step measurement")
     ap.add_argument("--no-sampling", action="store_true", help="skip the sampling measurement")
+    ap.add_argument("--no-projection", action="store_true", help="skip the projected-layer measurement")
     ap.add_argument("--page-size", type=int, default=0,
                     help="lay the KV caches out in pages of this many slots (0: contiguous regions)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
@@ -511,6 +513,74 @@ def measure_tiny(args, device, torch, dist_on) -> dict:
     return res
 
 
+def measure_projection(w, args, device, torch, dist_on, peaks, peak_kind, hidden=2560) -> dict:
+    """The attention layer with its projections (code walkthrough section
+    3.3): the merged Q/K/V projection fused with the prologue, the prefill
+    attention and the output projection, back to back on one stream, on
+    workload w with a Qwen3-4B hidden size.  FLOPs: 2 N C (Hq + 2 Hkv) D for
+    qkv_proj, 4 D Hq P for the attention, 2 N (Hq D) C for o_proj."""
+    from causal_gqa_attention_qkv_gb300 import attn
+    from causal_gqa_attention_qkv_gb300 import inputs as gen
+    from causal_gqa_attention_qkv_gb300 import step
+    host = gen.make_inputs(w, page_size=args.page_size)
+    pr = gen.make_projection_inputs(w, hidden=hidden, seed=1)
+    ds = step.upload(w, host, device=device)
+    N = w.num_tokens
+    hid, wq, wo = (pr[k].to(device) for k in ("hidden", "w_qkv", "w_o"))
+    q = torch.empty((N, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=device)
+    att = torch.empty((N, w.num_q_heads * w.head_dim), dtype=torch.bfloat16, device=device)
+    o = torch.empty((N, hidden), dtype=torch.bfloat16, device=device)
+    kv, ws = ds.kv_prefill, ds.workspace
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    def run(ev):
+        ev[0].record()
+        attn.qkv_proj_prepare(ds.cfg, hid, wq, ds.q_norm_w, ds.k_norm_w, ds.cu_seqlens, kv, q, ws)
+        ev[1].record()
+        attn.prefill_attend(ds.cfg, q, ds.cu_seqlens, ds.max_seqlen, kv, att, ws)
+        ev[2].record()
+        attn.o_proj(ds.cfg, att, wo, o, ws)
+        ev[3].record()
+
+    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        run(mk())
+    torch.cuda.synchronize()
+    if dist_on:
+        torch.distributed.barrier()
+    evs = [mk() for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        run(evs[k])
+    torch.cuda.synchronize()
+    if ds.status() != 0:
+        raise RuntimeError("device status set in the projected step")
+    mean = lambda i, j: sum(e[i].elapsed_time(e[j]) for e in evs) / len(evs)
+    t_qkv, t_att, t_o, t_step = max_over_ranks([mean(0, 1), mean(1, 2), mean(2, 3), mean(0, 3)], device)
+    f_qkv = 2.0 * N * hidden * w.qkv_width
+    f_att = prefill_flops(w)
+    f_o = 2.0 * N * w.num_q_heads * w.head_dim * hidden
+    peak = float(peaks["bf16_tflops"])
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    tf = lambda f, ms: f / (ms * 1e-3) / 1e12
+    return {
+        "workload": f"{w.name}_hidden{hidden}", "value": round(whole_job_rate(f_qkv + f_att + f_o, world, t_step) / 1e12, 3),
+        "unit": "TFLOP/s", "ms_per_step": round(t_step, 4),
+        "flops": {"qkv_proj": f_qkv, "attention": f_att, "o_proj": f_o},
+        "parts_ms": {"qkv_proj_prepare": round(t_qkv, 4), "prefill_attention": round(t_att, 4),
+                     "o_proj": round(t_o, 4)},
+        "roofline": {"bound": "tensor", "kernel": "proj_gemm_kernel (qkv projection + prologue epilogue)",
+                     "achieved": round(tf(f_qkv, t_qkv), 3), "peak": peak,
+                     "peak_kind": f"bf16_tflops ({peak_kind})", "unit": "TFLOP/s",
+                     "frac": round(tf(f_qkv, t_qkv) / peak, 4)},
+        "o_proj_roofline": {"bound": "tensor", "kernel": "proj_gemm_kernel (plain epilogue)",
+                            "achieved": round(tf(f_o, t_o), 3), "peak": peak, "unit": "TFLOP/s",
+                            "frac": round(tf(f_o, t_o) / peak, 4)},
+        "gpu_launches": 3 * args.steps,
+    }
+
+
 def measure_sampling(args, device, torch, dist_on, peaks, peak_kind, B=64) -> dict:
     """Token sampling (temperature + top-k + top-p, no greedy rows) from fp32
     logits of B rows over the Qwen3 vocabulary: one kernel launch per step.
@@ -649,6 +719,9 @@ def run_ours(args):
             r["cpu_baseline"]["sample"] += " (chunk and decode rows alike; FLOPs over all attended pairs)"
         line["mixed"] = r
         line["gpu_launches"] += r["gpu_launches"]
+    if not args.no_projection:
+        line["projection"] = measure_projection(wp, args, device, torch, dist_on, peaks, peak_kind)
+        line["gpu_launches"] += line["projection"]["gpu_launches"]
     r = measure_tiny(args, device, torch, dist_on)
     h, dh = pop(r, "host"), pop(r, "decode_host")
     if cpu:

@@ -188,3 +188,46 @@ def test_sample_arguments_checked(lib):
     assert call(V=(1 << 23) + 1, ld=(1 << 23) + 1) == -1
     assert call(ld=99) == -1
     assert call() in (-4, -5)  # past the checks: no GPU here
+
+
+def test_projection_arguments_checked(lib):
+    """attn_qkv_proj_prepare and attn_o_proj check their pointers, alignment,
+    the hidden size (positive, a multiple of 8), the cache and the workspace
+    before touching anything; calls that pass the checks stop at the device
+    query without a GPU (-4 or -5)."""
+    from causal_gqa_attention_qkv_gb300 import attn
+    cfg = attn.config(32, 8, 128)
+    fake = 1 << 20
+    f = ctypes.c_void_p(fake)
+    odd = ctypes.c_void_p(fake + 8)
+    kv = attn.AttnKV(fake, fake, 1024, fake, fake, fake)
+    k = ctypes.byref(kv)
+    past_checks = (-4, -5)
+
+    def qkv(hidden=f, C=2560, w=f, q=f, kvp=k, ws=f, wsb=1 << 20, B=1, N=4):
+        return lib.attn_qkv_proj_prepare(ctypes.byref(cfg), hidden, C, w, f, f, f, B, N, kvp, q, ws, wsb, None)
+
+    assert qkv() in past_checks
+    assert qkv(hidden=None) == -1
+    assert qkv(hidden=odd) == -1
+    assert qkv(w=None) == -1
+    assert qkv(w=odd) == -1
+    assert qkv(q=None) == -1
+    assert qkv(C=0) == -1
+    assert qkv(C=100) == -1          # not a multiple of 8
+    assert qkv(N=-1) == -1
+    assert qkv(kvp=None) == -1
+    assert qkv(ws=None) == -3
+    assert qkv(wsb=100) == -3
+
+    def oproj(x=f, N=4, w=f, C=2560, out=f, ws=f, wsb=1 << 20, c=cfg):
+        return lib.attn_o_proj(ctypes.byref(c), x, N, w, C, out, ws, wsb, None)
+
+    assert oproj() in past_checks
+    assert oproj(x=None) == -1
+    assert oproj(w=odd) == -1
+    assert oproj(out=None) == -1
+    assert oproj(C=12) == -1
+    assert oproj(N=-1) == -1
+    assert oproj(ws=None) == -3
+    assert oproj(c=attn.config(32, 5, 128)) == -2
