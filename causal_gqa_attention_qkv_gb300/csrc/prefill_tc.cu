@@ -463,34 +463,51 @@ __device__ void issue_mma(const TcPar& p, const SeqInfo* seq_tab, const int* rin
   w.start(p, seq_tab, ring, bars, false, ok);
   int g = 0;  // KV tiles of this CTA so far
   int k = 0;  // items so far
+  // S_X of an item's first KV tile: issued as soon as Q_X and the K tile have
+  // landed and (from the second item on) the previous item's last P.V_X is
+  // issued, so the softmax finds it ready after its epilogue.
+  auto first_s = [&](int x, int kk, int gg, int nk_) -> bool {
+    const int st = gg % kKStages;
+    if (!mbar_wait(&bars[kQFullA + x], kk & 1)) return false;
+    if (!mbar_wait(&bars[kKFull0 + st], (gg / kKStages) & 1)) return false;
+    tc::fence_after();
+    qk(x, st);
+    tc::commit(&bars[kSFullA + x]);
+    if (x == 1) tc::commit(&bars[kKEmpty0 + st]);
+    if (nk_ == 1) tc::commit(&bars[kQEmptyA + x]);
+    return true;
+  };
+  if (w.valid && ok && !(first_s(0, 0, 0, w.it.nk) && first_s(1, 0, 0, w.it.nk))) ok = false;
   while (w.valid && ok) {
     const int nk = w.it.nk;
-    if (!mbar_wait(&bars[kQFullA], k & 1) || !mbar_wait(&bars[kQFullB], k & 1)) { ok = false; break; }
-    {
-      const int st = g % kKStages;
-      if (!mbar_wait(&bars[kKFull0 + st], (g / kKStages) & 1)) { ok = false; break; }
-      tc::fence_after();
-      qk(0, st);
-      tc::commit(&bars[kSFullA]);
-      if (nk == 1) tc::commit(&bars[kQEmptyA]);
-      qk(1, st);
-      tc::commit(&bars[kSFullB]);
-      tc::commit(&bars[kKEmpty0 + st]);
-      if (nk == 1) tc::commit(&bars[kQEmptyB]);
-    }
+    bool next_valid = false;
+    int next_nk = 0;
     for (int j = 0; j < nk; ++j) {
       const int gj = g + j;
       const int sv = gj % kVStages;
       const bool last = j == nk - 1;
       const int st1 = (gj + 1) % kKStages;  // K stage of tile j + 1
-      // ---- tile A
+      // ---- tile A: the V tile (and with bf16 the next K tile) is waited
+      // for before P, off the softmax -> P.V -> S chain
+      if (!F8 && !mbar_wait(&bars[kVFull0 + sv], (gj / kVStages) & 1)) { ok = false; break; }
+      if (!F8 && !last && !mbar_wait(&bars[kKFull0 + st1], ((gj + 1) / kKStages) & 1)) { ok = false; break; }
       if (!mbar_wait(&bars[kPFullA], gj & 1)) { ok = false; break; }
-      if (!mbar_wait(&bars[kVFull0 + sv], (gj / kVStages) & 1)) { ok = false; break; }
+      if (F8 && !mbar_wait(&bars[kVFull0 + sv], (gj / kVStages) & 1)) { ok = false; break; }
       tc::fence_after();
       pv(0, sv, j > 0);
-      if (last) tc::commit(&bars[kODoneA]);
-      if (!last) {
-        if (!mbar_wait(&bars[kKFull0 + st1], ((gj + 1) / kKStages) & 1)) { ok = false; break; }
+      if (last) {
+        tc::commit(&bars[kODoneA]);
+        if (!F8) {
+          w.next(p, ok);  // the next item, whose first S_A can go now
+          next_valid = w.valid && ok;
+          if (next_valid) {
+            next_nk = w.it.nk;
+            if (!first_s(0, k + 1, g + nk, next_nk)) { ok = false; break; }
+          }
+        }
+      } else {
+        // with E4M3 the K tile is converted on chip; its wait stays after P.V
+        if (F8 && !mbar_wait(&bars[kKFull0 + st1], ((gj + 1) / kKStages) & 1)) { ok = false; break; }
         tc::fence_after();
         qk(0, st1);
         tc::commit(&bars[kSFullA]);
@@ -501,8 +518,10 @@ __device__ void issue_mma(const TcPar& p, const SeqInfo* seq_tab, const int* rin
       tc::fence_after();
       pv(1, sv, j > 0);
       tc::commit(&bars[kVEmpty0 + sv]);
-      if (last) tc::commit(&bars[kODoneB]);
-      if (!last) {
+      if (last) {
+        tc::commit(&bars[kODoneB]);
+        if (!F8 && next_valid && !first_s(1, k + 1, g + nk, next_nk)) { ok = false; break; }
+      } else {
         qk(1, st1);
         tc::commit(&bars[kSFullB]);
         tc::commit(&bars[kKEmpty0 + st1]);
@@ -512,7 +531,10 @@ __device__ void issue_mma(const TcPar& p, const SeqInfo* seq_tab, const int* rin
     if (!ok) break;
     g += nk;
     ++k;
-    w.next(p, ok);
+    if (F8) {  // converted K tiles land late: the next item's first S after its last P.V_B
+      w.next(p, ok);
+      if (w.valid && ok && !(first_s(0, k, g, w.it.nk) && first_s(1, k, g, w.it.nk))) ok = false;
+    }
   }
   // Nothing may still be running on the tensor cores when TMEM is freed.
   tc::commit(&bars[kMmaDone]);
