@@ -91,3 +91,130 @@ def upload(w, host: dict, device="cuda") -> DeviceStep:
         k_cache=k_cache, v_cache=v_cache, cache_lens=cache_lens, out=out, workspace=ws, n_prefill_tokens=n_pre,
         max_seqlen=max(list(w.new_lens[:df]) + [0]),
         max_cache_len=max(list(w.cache_lens[df:]) + [0]))
+
+
+@dataclasses.dataclass
+class _Chunk:
+    t0: int
+    t1: int
+    b0: int
+    b1: int             # requests [b0, b1) overlap the chunk
+    max_seqlen: int
+    cu: tuple           # offsets of the chunk's cu_seqlens and cached lengths in the metadata
+    cl: tuple
+
+
+@dataclasses.dataclass
+class ChunkPlan:
+    """Token chunks of one packed prefill call and their metadata: per chunk
+    its cu_seqlens and the cached length of each request it touches (int32,
+    in one pinned host buffer copied to the device with the first chunk)."""
+
+    chunks: list
+    meta_host: torch.Tensor
+    meta_dev: torch.Tensor
+
+    @property
+    def h2d_bytes(self) -> int:
+        return self.meta_host.numel() * 4
+
+
+class HostPrefill:
+    """Prefill from pinned host buffers in token chunks, pipelined over three
+    streams: while the kernels of chunk c run, the qkv rows of chunk c + 1
+    are copied in and the output rows of chunk c - 1 are copied out.
+
+    Each chunk is a valid packed prefill call of its own: the part of every
+    request that falls in its token range, with that request's cached length
+    advanced by the request's tokens in earlier chunks (the concept chapter's
+    section 4: a long prompt may be prefilled in chunks over its own cache).
+    The chunks run in order on one stream, so chunk c attends over the keys
+    the earlier chunks appended; every output row is computed by the same
+    kernels over the same key tiles as in one unchunked call.
+
+    Device buffers (qkv, prepared Q, output, the KV cache and its index
+    arrays, the workspace) belong to the caller and are reused across calls.
+    """
+
+    def __init__(self, cfg: attn.AttnConfig, q_norm_w, k_norm_w, kv: attn.KVCache, workspace, qkv_dev,
+                 q_stage, out_dev, chunk_tokens: int = 4096):
+        self.cfg, self.q_norm_w, self.k_norm_w, self.kv = cfg, q_norm_w, k_norm_w, kv
+        self.ws, self.qkv_dev, self.q_stage, self.out_dev = workspace, qkv_dev, q_stage, out_dev
+        self.chunk_tokens = max(1, int(chunk_tokens))
+        dev = qkv_dev.device
+        self.s_in = torch.cuda.Stream(device=dev)
+        self.s_run = torch.cuda.Stream(device=dev)
+        self.s_out = torch.cuda.Stream(device=dev)
+
+    def plan(self, cu_seqlens, cache_lens) -> ChunkPlan:
+        """Chunks of the packed batch given its host cu_seqlens [B + 1] and
+        cached lengths [B]."""
+        cu = [int(x) for x in cu_seqlens]
+        cl = [int(x) for x in cache_lens]
+        N = cu[-1]
+        chunks, meta = [], []
+        t0, b0 = 0, 0
+        while t0 < N:
+            t1 = min(N, t0 + self.chunk_tokens)
+            while cu[b0 + 1] <= t0:  # first request with a token at or after t0
+                b0 += 1
+            b1 = b0
+            while b1 < len(cu) - 1 and cu[b1] < t1:
+                b1 += 1
+            ccu, ccl, mx = [0], [], 0
+            for b in range(b0, b1):
+                lo, hi = max(cu[b], t0), min(cu[b + 1], t1)
+                n = max(0, hi - lo)
+                ccu.append(ccu[-1] + n)
+                ccl.append(cl[b] + max(0, lo - cu[b]))
+                mx = max(mx, n)
+            o = len(meta)
+            meta += ccu + ccl
+            chunks.append(_Chunk(t0, t1, b0, b1, mx, (o, o + len(ccu)), (o + len(ccu), o + len(ccu) + len(ccl))))
+            t0 = t1
+        meta_host = torch.tensor(meta if meta else [0], dtype=torch.int32).pin_memory()
+        meta_dev = torch.empty_like(meta_host, device=self.qkv_dev.device)
+        return ChunkPlan(chunks, meta_host, meta_dev)
+
+    def run(self, plan: ChunkPlan, qkv_host, out_host, start_event=None, end_event=None) -> int:
+        """Issue the pipelined step (asynchronous; returns the kernel launches).
+        qkv_host / out_host: pinned host tensors [N, W] / [N, Hq*D].  Optional
+        events are recorded before the first copy and after the last one."""
+        dev = self.qkv_dev.device
+        cur = torch.cuda.current_stream(dev)
+        kv, meta = self.kv, plan.meta_dev
+        landed, done = [], []
+        self.s_in.wait_stream(cur)
+        with torch.cuda.stream(self.s_in):
+            if start_event is not None:
+                start_event.record(self.s_in)
+            meta.copy_(plan.meta_host, non_blocking=True)
+            for c in plan.chunks:
+                self.qkv_dev[c.t0:c.t1].copy_(qkv_host[c.t0:c.t1], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(self.s_in)
+                landed.append(e)
+        with torch.cuda.stream(self.s_run):
+            for c, e in zip(plan.chunks, landed):
+                self.s_run.wait_event(e)
+                cu_d = meta[c.cu[0]:c.cu[1]]
+                ckv = attn.KVCache(kv.k_cache, kv.v_cache, kv.slot_base[c.b0:c.b1], meta[c.cl[0]:c.cl[1]],
+                                   kv.slot_capacity[c.b0:c.b1],
+                                   None if kv.page_table is None else kv.page_table[c.b0:c.b1],
+                                   kv.page_size, kv.k_scale, kv.v_scale)
+                q = self.q_stage[c.t0:c.t1]
+                attn.prefill_prepare(self.cfg, self.qkv_dev[c.t0:c.t1], self.q_norm_w, self.k_norm_w, cu_d, ckv, q,
+                                     self.ws, self.s_run)
+                attn.prefill_attend(self.cfg, q, cu_d, c.max_seqlen, ckv, self.out_dev[c.t0:c.t1], self.ws,
+                                    self.s_run)
+                e2 = torch.cuda.Event()
+                e2.record(self.s_run)
+                done.append(e2)
+        with torch.cuda.stream(self.s_out):
+            for c, e in zip(plan.chunks, done):
+                self.s_out.wait_event(e)
+                out_host[c.t0:c.t1].copy_(self.out_dev[c.t0:c.t1], non_blocking=True)
+            if end_event is not None:
+                end_event.record(self.s_out)
+        cur.wait_stream(self.s_out)
+        return 2 * len(plan.chunks)
