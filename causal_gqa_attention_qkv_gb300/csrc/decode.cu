@@ -163,16 +163,26 @@ __global__ void __launch_bounds__(kThreads, F8 ? DECODE_F8_MIN_BLOCKS : 0)
     q_row_frags<D>(p.qkv + (int64_t)b * p.W + (int64_t)(h0 + min(qrow, G - 1)) * D, qrow < G,
                    p.q_norm_w, p.eps, (float)r.cached, p.freqs, qa);
   const int qc = lane & 3;  // quad member
-  float o[D / 8][4];
+  // E4M3: transposed products, O^T = V^T P^T and S^T = K Q^T: the warp's 16
+  // keys of a tile are the M dimension and the group's heads the N dimension
+  // (8, heads >= G are zero padding), so one m16n8k16 covers 16 keys.  The
+  // d order inside a product is free as long as both operands agree: for
+  // S^T, quad member q takes d in [q D/4, (q+1) D/4) (the Q fragments use
+  // the same order); for O^T, lane (g, q) holds d in [g D/8, (g+1) D/8) of
+  // heads 2q, 2q+1.  Every lane reads contiguous codes from shared memory.
+  constexpr int MT = D / 16;   // m-tiles of O^T
+  float o[F8 ? MT : D / 8][4];
 #pragma unroll
-  for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  for (int i = 0; i < (F8 ? MT : D / 8); ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   float m = kNegInf, l = 0.f;
+  float mh[2] = {kNegInf, kNegInf}, lh[2] = {0.f, 0.f};  // E4M3: heads 2q, 2q+1
   bool ok = true;
 
   if constexpr (F8) {
-    // Two 64-key tiles per pass: twice the independent work between two
-    // waits, and one softmax reduction and one O rescale per 128 keys.
     constexpr int S = Lay::kStages;
+    constexpr int KW = D / 16;  // 32-bit code words of a key per quad member
+    const int g = qrow;
+    // two 64-key tiles per pass: one softmax reduction and one O rescale per 128 keys
     for (int i = 0; i < ntiles; i += 2) {
       const bool two = i + 1 < ntiles;
       const int st0 = i % S, st1 = (i + 1) % S;
@@ -183,106 +193,110 @@ __global__ void __launch_bounds__(kThreads, F8 ? DECODE_F8_MIN_BLOCKS : 0)
       // Without a second tile, stage st1 holds an older tile or nothing and no
       // copy is in flight into it; all of its keys lie past k1 and are masked.
       const uint32_t kb[2] = {smem_u32(smem + st0 * Lay::kStageBytes), smem_u32(smem + st1 * Lay::kStageBytes)};
-      uint32_t kw[2][2][D / 16];  // [tile][key octet][word]
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int hc = 0; hc < D / 64; ++hc) {
-            const uint4 raw = lds128(kb[t] + f8_off<D>(warp * 16 + nt * 8 + qrow, qc * (D / 64) + hc));
-            kw[t][nt][4 * hc] = raw.x;
-            kw[t][nt][4 * hc + 1] = raw.y;
-            kw[t][nt][4 * hc + 2] = raw.z;
-            kw[t][nt][4 * hc + 3] = raw.w;
-          }
-      float s[2][2][4];
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) s[t][nt][0] = s[t][nt][1] = s[t][nt][2] = s[t][nt][3] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            uint32_t b0, b1;
-            e4m3x4_to_f16(kw[t][nt][ks], b0, b1);
-            mma_f16_16816(s[t][nt], a, b0, b1);
-          }
-      }
-      float sc[2][4];
-      int kA[2];
+      float s[2][4];
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
-        kA[t] = k0 + (i + t) * kKeysPerTile + warp * 16 + 2 * qc;
-        sc[t][0] = kA[t] < k1 ? s[t][0][0] * p.scale_log2 : kNegInf;
-        sc[t][1] = kA[t] + 1 < k1 ? s[t][0][1] * p.scale_log2 : kNegInf;
-        sc[t][2] = kA[t] + 8 < k1 ? s[t][1][0] * p.scale_log2 : kNegInf;
-        sc[t][3] = kA[t] + 9 < k1 ? s[t][1][1] * p.scale_log2 : kNegInf;
+        // codes of keys g and g + 8, columns [q D/4, (q+1) D/4)
+        uint32_t kw[2][KW];
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int hc = 0; hc < D / 64; ++hc) {
+            const uint4 raw = lds128(kb[t] + f8_off<D>(warp * 16 + g + 8 * r, qc * (D / 64) + hc));
+            kw[r][4 * hc] = raw.x;
+            kw[r][4 * hc + 1] = raw.y;
+            kw[r][4 * hc + 2] = raw.z;
+            kw[r][4 * hc + 3] = raw.w;
+          }
+        s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KW; ++ks) {
+          uint32_t a[4];  // rows g, g + 8; columns 2q, 2q + 1 (a0, a1) and 2q + 8, 2q + 9 (a2, a3)
+          e4m3x4_to_f16(kw[0][ks], a[0], a[2]);
+          e4m3x4_to_f16(kw[1][ks], a[1], a[3]);
+          mma_f16_16816(s[t], a, qa[ks][0], qa[ks][1]);
+        }
       }
-      float mx = fmaxf(fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[0][2], sc[0][3])),
-                       fmaxf(fmaxf(sc[1][0], sc[1][1]), fmaxf(sc[1][2], sc[1][3])));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float m_new = fmaxf(m, mx);
-      const float m_use = m_new == kNegInf ? 0.f : m_new;
-      const float alpha = fast_exp2(m - m_use);
-      float pr[2][4], rs = 0.f;
+      // s[t]: key g (c0: head 2q, c1: head 2q + 1) and key g + 8 (c2, c3)
+      float sc[2][4];
+      int kg[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        kg[t] = k0 + (i + t) * kKeysPerTile + warp * 16 + g;
+        sc[t][0] = kg[t] < k1 ? s[t][0] * p.scale_log2 : kNegInf;
+        sc[t][1] = kg[t] < k1 ? s[t][1] * p.scale_log2 : kNegInf;
+        sc[t][2] = kg[t] + 8 < k1 ? s[t][2] * p.scale_log2 : kNegInf;
+        sc[t][3] = kg[t] + 8 < k1 ? s[t][3] * p.scale_log2 : kNegInf;
+      }
+      float alpha[2], m_use[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {  // head 2q + e: maximum over the warp's keys
+        float mx = fmaxf(fmaxf(sc[0][e], sc[0][2 + e]), fmaxf(sc[1][e], sc[1][2 + e]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float m_new = fmaxf(mh[e], mx);
+        m_use[e] = m_new == kNegInf ? 0.f : m_new;
+        alpha[e] = fast_exp2(mh[e] - m_use[e]);
+        mh[e] = m_new;
+      }
+      float pr[2][4], rs[2] = {0.f, 0.f};
 #pragma unroll
       for (int t = 0; t < 2; ++t)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          pr[t][e] = fast_exp2(sc[t][e] - m_use);
-          rs += pr[t][e];
+          pr[t][e] = fast_exp2(sc[t][e] - m_use[e & 1]);
+          rs[e & 1] += pr[t][e];
         }
-      l = l * alpha + rs;
-      m = m_new;
 #pragma unroll
-      for (int dt = 0; dt < D / 8; ++dt) {
-        o[dt][0] *= alpha;
-        o[dt][1] *= alpha;
+      for (int e = 0; e < 2; ++e) lh[e] = lh[e] * alpha[e] + rs[e];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        o[mt][0] *= alpha[0];
+        o[mt][1] *= alpha[1];
+        o[mt][2] *= alpha[0];
+        o[mt][3] *= alpha[1];
       }
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
-        const uint32_t pa[4] = {pack_f16(pr[t][0], pr[t][1]), 0u, pack_f16(pr[t][2], pr[t][3]), 0u};
-        // keys past the end hold arbitrary bits: zero their V entries so 0 * NaN cannot occur
-        const bool partial = kA[t] - 2 * qc + 16 > k1;
-        const uint32_t mA = (kA[t] < k1 ? 0x0000FFFFu : 0u) | (kA[t] + 1 < k1 ? 0xFFFF0000u : 0u);
-        const uint32_t mB = (kA[t] + 8 < k1 ? 0x0000FFFFu : 0u) | (kA[t] + 9 < k1 ? 0xFFFF0000u : 0u);
+        // P^T as the B operand: the 8 x 8 blocks (keys g | g + 8, heads 2q, 2q + 1) transposed
+        uint32_t pb0, pb1;
+        asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(pb0) : "r"(pack_f16(pr[t][0], pr[t][1])));
+        asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(pb1) : "r"(pack_f16(pr[t][2], pr[t][3])));
+        // V codes of keys 2q, 2q + 1, 2q + 8, 2q + 9, columns [g D/8, (g+1) D/8)
         const uint32_t vb = kb[t] + Lay::kTileBytes;
-        // keys 2c, 2c+1 (b0) and 2c+8, 2c+9 (b1) of this warp's 16, columns [g D/8, (g+1) D/8)
-        constexpr int W = D / 32;  // 32-bit words per key and lane
-        uint32_t kv4[4][W];
+        constexpr int VW = D / 32;  // 32-bit words per key
+        uint32_t v4[4][VW];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const int key = warp * 16 + 2 * qc + (q4 & 1) + (q4 >> 1) * 8;
           if constexpr (D == 128) {
-            const uint4 v = lds128(vb + f8_off<D>(key, qrow));
-            kv4[q4][0] = v.x; kv4[q4][1] = v.y; kv4[q4][2] = v.z; kv4[q4][3] = v.w;
+            const uint4 v = lds128(vb + f8_off<D>(key, g));
+            v4[q4][0] = v.x; v4[q4][1] = v.y; v4[q4][2] = v.z; v4[q4][3] = v.w;
           } else {
-            const uint2 v = lds64(vb + key * (uint32_t)D + qrow * 8);
-            kv4[q4][0] = v.x; kv4[q4][1] = v.y;
+            const uint2 v = lds64(vb + key * (uint32_t)D + g * 8);
+            v4[q4][0] = v.x; v4[q4][1] = v.y;
           }
         }
+        // keys past the end hold arbitrary bits: zero their V entries so 0 * NaN cannot occur
+        const int kq = k0 + (i + t) * kKeysPerTile + warp * 16 + 2 * qc;
+        const bool partial = k0 + (i + t) * kKeysPerTile + warp * 16 + 16 > k1;
+        const uint32_t mAB = (kq < k1 ? 0x0000FFFFu : 0u) | (kq + 1 < k1 ? 0xFFFF0000u : 0u);
+        const uint32_t mCD = (kq + 8 < k1 ? 0x0000FFFFu : 0u) | (kq + 9 < k1 ? 0xFFFF0000u : 0u);
 #pragma unroll
-        for (int j = 0; j < W; ++j) {
-          // byte pairs (key a, key b) per column: columns 4j + 0..3 of this lane
-          uint32_t b0[4], b1[4];
-          e4m3x4_to_f16(prmt(kv4[0][j], kv4[1][j], 0x5140u), b0[0], b0[1]);
-          e4m3x4_to_f16(prmt(kv4[0][j], kv4[1][j], 0x7362u), b0[2], b0[3]);
-          e4m3x4_to_f16(prmt(kv4[2][j], kv4[3][j], 0x5140u), b1[0], b1[1]);
-          e4m3x4_to_f16(prmt(kv4[2][j], kv4[3][j], 0x7362u), b1[2], b1[3]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (partial) {
-              b0[e] &= mA;
-              b1[e] &= mB;
-            }
-            mma_f16_16816(o[4 * j + e], pa, b0[e], b1[e]);
+        for (int mt = 0; mt < MT; ++mt) {
+          // rows g / g + 8 of m-tile mt: d = g D/8 + 2 mt and + 1 (bytes 2 mt, 2 mt + 1 of the run)
+          const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+          uint32_t a[4];
+          e4m3x4_to_f16(prmt(v4[0][mt >> 1], v4[1][mt >> 1], sel), a[0], a[1]);
+          e4m3x4_to_f16(prmt(v4[2][mt >> 1], v4[3][mt >> 1], sel), a[2], a[3]);
+          if (partial) {
+            a[0] &= mAB;
+            a[1] &= mAB;
+            a[2] &= mCD;
+            a[3] &= mCD;
           }
+          mma_f16_16816(o[mt], a, pb0, pb1);
         }
       }
       __syncwarp();
@@ -370,6 +384,12 @@ __global__ void __launch_bounds__(kThreads, F8 ? DECODE_F8_MIN_BLOCKS : 0)
   }
   l += __shfl_xor_sync(0xffffffffu, l, 1);
   l += __shfl_xor_sync(0xffffffffu, l, 2);
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {  // E4M3: the head's sum over the warp's keys
+    lh[e] += __shfl_xor_sync(0xffffffffu, lh[e], 4);
+    lh[e] += __shfl_xor_sync(0xffffffffu, lh[e], 8);
+    lh[e] += __shfl_xor_sync(0xffffffffu, lh[e], 16);
+  }
 
   // ---------------- merge the four warps' partial softmax states
   named_sync_consumers();  // every consumer is done with the stage buffers
@@ -377,17 +397,30 @@ __global__ void __launch_bounds__(kThreads, F8 ? DECODE_F8_MIN_BLOCKS : 0)
   float* mo = reinterpret_cast<float*>(smem);                 // [warps][G][D]
   float* mm = mo + kConsumerWarps * G * D;                      // [warps][G]
   float* ml = mm + kConsumerWarps * G;                          // [warps][G]
-  if (qrow < G) {
+  if constexpr (F8) {
+    // lane (g, q): heads 2q, 2q + 1, d in [g D/8, (g+1) D/8)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int head = 2 * qc + e;
+      if (head < G) {
+        float* dst = mo + (warp * G + head) * D + qrow * (D / 8);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          dst[2 * mt] = o[mt][e] * p.v_scale;
+          dst[2 * mt + 1] = o[mt][2 + e] * p.v_scale;
+        }
+        if (qrow == 0) {
+          mm[warp * G + head] = mh[e];
+          ml[warp * G + head] = lh[e];
+        }
+      }
+    }
+  } else if (qrow < G) {
     float* dst = mo + (warp * G + qrow) * D;
 #pragma unroll
     for (int dt = 0; dt < D / 8; ++dt) {
-      if constexpr (F8) {  // n-tile dt, column n: output column n D/8 + dt
-        dst[(2 * qc) * (D / 8) + dt] = o[dt][0] * p.v_scale;
-        dst[(2 * qc + 1) * (D / 8) + dt] = o[dt][1] * p.v_scale;
-      } else {
-        dst[dt * 8 + 2 * qc] = o[dt][0];
-        dst[dt * 8 + 2 * qc + 1] = o[dt][1];
-      }
+      dst[dt * 8 + 2 * qc] = o[dt][0];
+      dst[dt * 8 + 2 * qc + 1] = o[dt][1];
     }
     if ((lane & 3) == 0) {
       mm[warp * G + qrow] = m;
