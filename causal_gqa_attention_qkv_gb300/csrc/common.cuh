@@ -62,6 +62,15 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return r;
 }
 
+// ---------------------------------------------------------------- dependent launches
+// A kernel launched with programmatic stream serialisation may start while
+// the kernel before it in the stream is still running; it waits here before
+// it touches memory that kernel (or any earlier one) writes.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets such a kernel after this one be scheduled once every CTA of this
+// kernel has started (its CTAs then fill SMs as this kernel's CTAs exit).
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- status
 __device__ __forceinline__ void set_status(int32_t* status, int32_t bit) {
   if (status) atomicOr(status, bit);

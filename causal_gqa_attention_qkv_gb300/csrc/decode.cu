@@ -88,7 +88,8 @@ __global__ void __launch_bounds__(kThreads, F8 ? DECODE_F8_MIN_BLOCKS : 0)
   __shared__ int s_cons_abort;  // written by consumers only, read after their barrier
 
   const int split = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
-  const ReqInfo r = load_request(p.kv, b, 1);
+  launch_dependents();  // the merge kernel may be scheduled as CTAs finish
+  const ReqInfo r = load_request(p.kv, b, 1);  // request facts: written by the caller, not by a kernel
   if (!r.valid) return;  // flagged by the prologue
   const int kv_len = r.cached + 1;
   const int n_splits = (kv_len + p.split_len - 1) / p.split_len;
@@ -112,6 +113,7 @@ __global__ void __launch_bounds__(kThreads, F8 ? DECODE_F8_MIN_BLOCKS : 0)
     fence_barrier_init();
   }
   __syncthreads();
+  grid_dependency_wait();  // the append kernel's cache entries, earlier kernels' reads of the outputs
 
   if (warp == kConsumerWarps) {  // producer warp: one thread issues all TMA loads
     if (lane == 0) {
@@ -459,6 +461,7 @@ __global__ void __launch_bounds__(kThreads, F8 ? DECODE_F8_MIN_BLOCKS : 0)
 template <int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const DecodePar p) {
   const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+  grid_dependency_wait();  // the split kernel's partial results
   const ReqInfo r = load_request(p.kv, b, 1);
   if (!r.valid) return;
   const int n = (r.cached + 1 + p.split_len - 1) / p.split_len;
@@ -503,12 +506,12 @@ int launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
                            Lay::kSmemBytes) != cudaSuccess)
     return ATTN_ELAUNCH;
   dim3 grid(a.max_splits, a.cfg.num_kv_heads, a.B);
-  decode_split_kernel<D, F8><<<grid, kThreads, Lay::kSmemBytes, stream>>>(maps.k, maps.v, p);
-  if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
-  if (a.max_splits > 1) {
-    decode_combine_kernel<D><<<dim3(a.cfg.num_q_heads, a.B), D, 0, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
-  }
+  if (launch_dependent(decode_split_kernel<D, F8>, grid, dim3(kThreads), Lay::kSmemBytes, stream, maps.k, maps.v,
+                       p) != cudaSuccess)
+    return ATTN_ELAUNCH;
+  if (a.max_splits > 1 && launch_dependent(decode_combine_kernel<D>, dim3(a.cfg.num_q_heads, a.B), dim3(D), 0,
+                                           stream, p) != cudaSuccess)
+    return ATTN_ELAUNCH;
   return ATTN_OK;
 }
 

@@ -22,6 +22,25 @@ inline KvIndex kv_index(const attn_kv_t& kv) {
   return x;
 }
 
+// Launch with programmatic stream serialisation: the kernel may be scheduled
+// while the one before it in the stream finishes.  It must call
+// grid_dependency_wait() before touching memory an earlier kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Host-side argument checks of the C ABI (ATTN_OK or an ATTN_E* code).
 int abi_check_config(const attn_config_t* cfg);
 int abi_check_kv(const attn_kv_t* kv);

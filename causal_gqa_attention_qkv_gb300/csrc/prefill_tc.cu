@@ -817,6 +817,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const SeqInfo* seq_tab = p.B <= kMaxSeqSmem ? reinterpret_cast<const SeqInfo*>(smem + Lay::kSeq) : nullptr;
   int* ring = reinterpret_cast<int*>(smem + Lay::kRingOff);
   bool ok = true;
+  // Everything above reads only what the caller wrote; the prepared Q and the
+  // cache entries come from the kernel before this one.
+  grid_dependency_wait();
 
   if (warp < 8) {
     softmax_tile<D, F8>(p, seq_tab, ring, sbase, tmem, bars, &omap, warp >> 2, ok);
@@ -896,8 +899,10 @@ int launch_prefill_tc_t(const PrefillArgs& a, cudaStream_t stream) {
                            Lay::kSmemBytes) != cudaSuccess)
     return ATTN_ELAUNCH;
   const int grid = (int)std::min<int64_t>(sms, nv);
-  prefill_tc_kernel<D, F8><<<grid, kThreads, Lay::kSmemBytes, stream>>>(qmap, maps.k, maps.v, omap, p);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
+  return launch_dependent(prefill_tc_kernel<D, F8>, dim3(grid), dim3(kThreads), Lay::kSmemBytes, stream, qmap,
+                          maps.k, maps.v, omap, p) == cudaSuccess
+             ? ATTN_OK
+             : ATTN_ELAUNCH;
 }
 
 }  // namespace

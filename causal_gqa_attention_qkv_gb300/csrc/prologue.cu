@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) kv_append_kernel(const P
   constexpr int HPI = 32 / L;   // head vectors per warp-wide step
   constexpr int PPL = D / 64;   // rotation pairs computed per lane
   const int lane = threadIdx.x & 31;
+  launch_dependents();  // the attention kernel after this one may be scheduled as CTAs finish
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   if (t >= p.N) return;
 
