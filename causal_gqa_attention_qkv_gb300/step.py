@@ -119,6 +119,40 @@ class ChunkPlan:
         return self.meta_host.numel() * 4
 
 
+def plan_chunks(cu_seqlens, cache_lens, chunk_tokens: int):
+    """Split a packed prefill call (host cu_seqlens [B + 1], cached lengths
+    [B]) into calls of at most chunk_tokens tokens, in token order.  Chunk c
+    covers tokens [t0, t1) and the requests [b0, b1) with tokens there; its
+    own cu_seqlens counts each request's tokens inside the chunk, and each
+    request's cached length is advanced by its tokens in earlier chunks.
+    Returns (chunks, metadata): the chunks' cu_seqlens and cached lengths
+    are int32 runs of the metadata list at the offsets the chunks record."""
+    cu = [int(x) for x in cu_seqlens]
+    cl = [int(x) for x in cache_lens]
+    N = cu[-1]
+    chunks, meta = [], []
+    t0, b0 = 0, 0
+    while t0 < N:
+        t1 = min(N, t0 + chunk_tokens)
+        while cu[b0 + 1] <= t0:  # first request with a token at or after t0
+            b0 += 1
+        b1 = b0
+        while b1 < len(cu) - 1 and cu[b1] < t1:
+            b1 += 1
+        ccu, ccl, mx = [0], [], 0
+        for b in range(b0, b1):
+            lo, hi = max(cu[b], t0), min(cu[b + 1], t1)
+            n = max(0, hi - lo)
+            ccu.append(ccu[-1] + n)
+            ccl.append(cl[b] + max(0, lo - cu[b]))
+            mx = max(mx, n)
+        o = len(meta)
+        meta += ccu + ccl
+        chunks.append(_Chunk(t0, t1, b0, b1, mx, (o, o + len(ccu)), (o + len(ccu), o + len(ccu) + len(ccl))))
+        t0 = t1
+    return chunks, meta
+
+
 class HostPrefill:
     """Prefill from pinned host buffers in token chunks, pipelined over three
     streams: while the kernels of chunk c run, the qkv rows of chunk c + 1
@@ -149,29 +183,7 @@ class HostPrefill:
     def plan(self, cu_seqlens, cache_lens) -> ChunkPlan:
         """Chunks of the packed batch given its host cu_seqlens [B + 1] and
         cached lengths [B]."""
-        cu = [int(x) for x in cu_seqlens]
-        cl = [int(x) for x in cache_lens]
-        N = cu[-1]
-        chunks, meta = [], []
-        t0, b0 = 0, 0
-        while t0 < N:
-            t1 = min(N, t0 + self.chunk_tokens)
-            while cu[b0 + 1] <= t0:  # first request with a token at or after t0
-                b0 += 1
-            b1 = b0
-            while b1 < len(cu) - 1 and cu[b1] < t1:
-                b1 += 1
-            ccu, ccl, mx = [0], [], 0
-            for b in range(b0, b1):
-                lo, hi = max(cu[b], t0), min(cu[b + 1], t1)
-                n = max(0, hi - lo)
-                ccu.append(ccu[-1] + n)
-                ccl.append(cl[b] + max(0, lo - cu[b]))
-                mx = max(mx, n)
-            o = len(meta)
-            meta += ccu + ccl
-            chunks.append(_Chunk(t0, t1, b0, b1, mx, (o, o + len(ccu)), (o + len(ccu), o + len(ccu) + len(ccl))))
-            t0 = t1
+        chunks, meta = plan_chunks(cu_seqlens, cache_lens, self.chunk_tokens)
         meta_host = torch.tensor(meta if meta else [0], dtype=torch.int32).pin_memory()
         meta_dev = torch.empty_like(meta_host, device=self.qkv_dev.device)
         return ChunkPlan(chunks, meta_host, meta_dev)
