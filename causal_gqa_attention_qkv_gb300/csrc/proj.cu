@@ -10,9 +10,14 @@
 //
 // One persistent kernel, one CTA per SM, output tiles of 128 rows x 256
 // columns handed out round-robin (row-block major, so that CTAs running at
-// the same time share the rows of x in L2):
-//   warp 0      one thread issues the TMA loads of x (128 x 64) and W
-//               (256 x 64) into a 4-stage ring of 48 KB stages;
+// the same time share the rows of x in L2).  CTAs work in pairs (a cluster
+// of two): the pair computes two vertically adjacent tiles with the same 256
+// columns, and each CTA loads half of that W tile into both CTAs' shared
+// memory by TMA multicast (a third less L2 traffic per CTA); a stage is
+// refilled once both CTAs' MMAs have read it.  Roles per CTA:
+//   warp 0      one thread issues the TMA loads of x (128 x 64) and of its
+//               half of W (128 x 64, multicast) into a 4-stage ring of
+//               48 KB stages;
 //   warp 1      owns the 512 TMEM columns (two 256-column fp32 accumulators)
 //               and one thread issues the MMAs, M128 N256 K16, four per stage;
 //   warps 2-5   the epilogue: thread r of the four warps holds row r of the
@@ -74,6 +79,49 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+#ifndef PROJ_PAIR
+#define PROJ_PAIR 1
+#endif
+// CTA pairs: the two CTAs of a cluster compute vertically adjacent tiles
+// (rows m0 and m0 + 128, the same 256 columns) and each loads half of the
+// shared W tile into both CTAs' shared memory (TMA multicast).
+constexpr int kPair = PROJ_PAIR ? 2 : 1;
+
+__device__ __forceinline__ uint32_t cta_rank_in_cluster() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The box goes to the same shared-memory offset of every CTA in `mask`, and
+// its bytes are counted on the mbarrier at the same offset in each of them.
+__device__ __forceinline__ void tma_load_2d_multicast(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t c0,
+                                                      int32_t c1, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(mask)
+      : "memory");
+}
+// Arrive on the mbarrier at `bar`'s offset in every CTA of `mask` once this
+// thread's earlier MMAs have completed.
+__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+
+// Tile t of this CTA: row block and column block.  With pairs, pair tile t
+// gives both CTAs of the cluster the same column block.
+__device__ __forceinline__ void tile_coords(const ProjPar& p, int t, uint32_t rank, int& m0, int& n0) {
+  m0 = ((t / p.tiles_n) * kPair + (int)rank) * kBM;
+  n0 = (t % p.tiles_n) * kBN;
+}
+
 // ---------------------------------------------------------------- producer
 __device__ void proj_produce(const ProjPar& p, const CUtensorMap* amap, const CUtensorMap* bmap, uint8_t* smem,
                              uint64_t* bars, bool& ok) {
@@ -82,14 +130,20 @@ __device__ void proj_produce(const ProjPar& p, const CUtensorMap* amap, const CU
   uint32_t ph = 0;
   uint32_t filled = 0;  // bit s: stage s was filled at least once
   uint32_t last_par = 0;  // bit s: parity of the last fill of stage s
-  for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
-    const int m0 = (t / p.tiles_n) * kBM, n0 = (t % p.tiles_n) * kBN;
+  const uint32_t rank = kPair > 1 ? cta_rank_in_cluster() : 0u;
+  for (int t = blockIdx.x / kPair; t < p.tiles && ok; t += gridDim.x / kPair) {
+    int m0, n0;
+    tile_coords(p, t, rank, m0, n0);
     for (int kb = 0; kb < kb_count; ++kb) {
       if (!mbar_wait(&bars[kEmpty + st], ph ^ 1)) { ok = false; break; }
       uint8_t* a = smem + st * kStageBytes;
       mbar_arrive_expect_tx(&bars[kFull + st], kStageBytes);
       tma_load_2d(a, amap, &bars[kFull + st], kb * kBK, m0);
-      tma_load_2d(a + kATile, bmap, &bars[kFull + st], kb * kBK, n0);
+      if (kPair > 1)  // this CTA's half of the W tile, into both CTAs
+        tma_load_2d_multicast(a + kATile + rank * (kBTile / 2), bmap, &bars[kFull + st], kb * kBK,
+                              n0 + (int)rank * (kBN / 2), 0x3);
+      else
+        tma_load_2d(a + kATile, bmap, &bars[kFull + st], kb * kBK, n0);
       filled |= 1u << st;
       last_par = (last_par & ~(1u << st)) | (ph << st);
       if (++st == kStages) { st = 0; ph ^= 1; }
@@ -108,7 +162,7 @@ __device__ void proj_mma(const ProjPar& p, uint32_t sbase, uint32_t tmem, uint64
   int st = 0;
   uint32_t ph = 0;
   int it = 0;
-  for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x, ++it) {
+  for (int t = blockIdx.x / kPair; t < p.tiles && ok; t += gridDim.x / kPair, ++it) {
     const int buf = it & 1;
     const uint32_t use = (uint32_t)(it >> 1);
     if (!mbar_wait(&bars[kAccEmpty + buf], (use & 1u) ^ 1u)) { ok = false; break; }
@@ -123,7 +177,10 @@ __device__ void proj_mma(const ProjPar& p, uint32_t sbase, uint32_t tmem, uint64
 #pragma unroll
       for (int k = 0; k < kBK / 16; ++k)  // +32 bytes per K step inside the 128-byte swizzle row
         tc::mma_f16_ss(d, ad + (uint64_t)(k * 2), bd + (uint64_t)(k * 2), idesc, (kb | k) != 0 ? 1u : 0u);
-      tc::commit(&bars[kEmpty + st]);  // the stage is free once these MMAs have read it
+      // the stage is free once these MMAs have read it (with pairs: in both CTAs,
+      // whose producers both write into it)
+      if (kPair > 1) mma_commit_multicast(&bars[kEmpty + st], 0x3);
+      else tc::commit(&bars[kEmpty + st]);
       if (++st == kStages) { st = 0; ph ^= 1; }
     }
     if (!ok) break;
@@ -303,13 +360,15 @@ __device__ void proj_epilogue(const ProjPar& p, uint32_t tmem, uint64_t* bars, c
                               bool& ok) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int lane_grp = warp & 3;  // TMEM lanes [32 lane_grp, 32 lane_grp + 32) of this warp
+  const uint32_t rank = kPair > 1 ? cta_rank_in_cluster() : 0u;
   int it = 0;
-  for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x, ++it) {
+  for (int t = blockIdx.x / kPair; t < p.tiles && ok; t += gridDim.x / kPair, ++it) {
     const int buf = it & 1;
     const uint32_t use = (uint32_t)(it >> 1);
     if (!mbar_wait(&bars[kAccFull + buf], use & 1u)) { ok = false; break; }
     tc::fence_after();
-    const int m0 = (t / p.tiles_n) * kBM, n0 = (t % p.tiles_n) * kBN;
+    int m0, n0;
+    tile_coords(p, t, rank, m0, n0);
     const int row = m0 + 32 * lane_grp + lane;
     const uint32_t taddr = tmem + ((uint32_t)(32 * lane_grp) << 16) + (uint32_t)buf * kBN;
     if (Epi == kEpiPlain) epi_plain(p, row, n0, taddr);
@@ -321,7 +380,7 @@ __device__ void proj_epilogue(const ProjPar& p, uint32_t tmem, uint64_t* bars, c
 }
 
 template <int Epi, int D, bool F8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(kPair, 1, 1) __launch_bounds__(kThreads, 1)
     proj_gemm_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
                      const ProjPar p) {
   extern __shared__ uint8_t smem_raw[];
@@ -335,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars[kFull + s], 1);
-      mbar_init(&bars[kEmpty + s], 1);
+      mbar_init(&bars[kEmpty + s], kPair);  // one MMA completion per CTA of the pair
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[kAccFull + s], 1);
@@ -357,6 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc::fence_before();
   __syncthreads();
+  if (kPair > 1) cluster_barrier();  // both CTAs' barriers exist before either multicasts into the other
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
   bool ok = true;
@@ -370,6 +430,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!ok) set_status(p.status, ATTN_STATUS_TIMEOUT);
   tc::fence_before();
   __syncthreads();
+  // neither CTA leaves while the other may still write into its shared memory
+  // or arrive on its barriers
+  if (kPair > 1) cluster_barrier();
   tc::fence_after();
   if (warp == 1) tc::dealloc(tmem, kTmemCols);
 }
@@ -379,9 +442,10 @@ int launch_proj_t(const ProjPar& p0, const void* a, const void* b, cudaStream_t 
   ProjPar p = p0;
   CUtensorMap amap, bmap;
   if (make_matrix_map(a, p.M, p.K, kBM, &amap) != 0) return ATTN_ELAUNCH;
-  if (make_matrix_map(b, p.N, p.K, kBN, &bmap) != 0) return ATTN_ELAUNCH;
+  if (make_matrix_map(b, p.N, p.K, kBN / kPair, &bmap) != 0) return ATTN_ELAUNCH;
   p.tiles_n = (p.N + kBN - 1) / kBN;
-  const int64_t tiles = (int64_t)((p.M + kBM - 1) / kBM) * p.tiles_n;
+  const int64_t row_blocks = ((int64_t)(p.M + kBM - 1) / kBM + kPair - 1) / kPair;  // pairs of row blocks
+  const int64_t tiles = row_blocks * p.tiles_n;
   if (tiles > (int64_t(1) << 30)) return ATTN_EINVAL;
   p.tiles = (int)tiles;
   int dev = 0, sms = 0;
@@ -391,7 +455,21 @@ int launch_proj_t(const ProjPar& p0, const void* a, const void* b, cudaStream_t 
   if (cudaFuncSetAttribute(proj_gemm_kernel<Epi, D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemBytes) != cudaSuccess)
     return ATTN_ELAUNCH;
-  const int grid = (int)std::min<int64_t>(sms, tiles);
+  // as many clusters as can be resident at once (pairs must share a GPC,
+  // and not every GPC has an even number of SMs): a persistent cluster that
+  // could only start after another one finished would double the run time
+  int clusters = sms / kPair;
+  if (kPair > 1) {
+    cudaLaunchConfig_t qc = {};
+    qc.gridDim = dim3(kPair * clusters);
+    qc.blockDim = dim3(kThreads);
+    qc.dynamicSmemBytes = kSmemBytes;
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, proj_gemm_kernel<Epi, D, F8>, &qc) != cudaSuccess || active <= 0)
+      return ATTN_ELAUNCH;
+    clusters = std::min(clusters, active);
+  }
+  const int grid = (int)std::min<int64_t>(clusters, tiles) * kPair;
   proj_gemm_kernel<Epi, D, F8><<<grid, kThreads, kSmemBytes, stream>>>(amap, bmap, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
 }
