@@ -43,6 +43,10 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+ONLY_PARTS = ("long_prefill", "prefill", "prefill_e4m3", "decode", "decode_e4m3", "mixed", "projection",
+              "sampling")
+
+
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -62,7 +66,14 @@ def parse_args():
                     help="lay the KV caches out in pages of this many slots (0: contiguous regions)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU oracle sample budget")
-    return ap.parse_args()
+    ap.add_argument("--only", default="",
+                    help="comma-separated parts to run alone, without the headline (for profiler captures): "
+                         + ", ".join(ONLY_PARTS))
+    a = ap.parse_args()
+    bad = [x for x in a.only.split(",") if x and x not in ONLY_PARTS]
+    if bad:
+        ap.error(f"--only: unknown part(s) {bad}")
+    return a
 
 
 def load_peaks():
@@ -654,6 +665,39 @@ def measure_mixed(wm, args, device, torch, dist_on, peaks, peak_kind) -> dict:
     }
 
 
+def run_only(args, device, torch, dist_on, peaks, peak_kind, rank):
+    """The named parts alone, each with its own warm-up and timed steps, and
+    no oracle: a short, fixed sequence of launches for profiler captures.
+    Prints one JSON line with the parts' results."""
+    from causal_gqa_attention_qkv_gb300 import inputs as gen
+    parts = [x for x in args.only.split(",") if x]
+    line = {"only": parts}
+    for part in parts:
+        if part in ("long_prefill", "prefill", "prefill_e4m3"):
+            wl = gen.ALL[args.workload if part == "long_prefill" else args.prefill_workload]
+            r = measure_prefill(wl, args, device, torch, dist_on, peaks, peak_kind,
+                                kv_dtype="e4m3" if part == "prefill_e4m3" else "bf16")
+        elif part in ("decode", "decode_e4m3"):
+            f8 = part == "decode_e4m3"
+            r = measure_decode(gen.ALL[args.decode_workload], args, device, torch, dist_on, peaks, peak_kind,
+                               "e4m3" if f8 else "bf16", 1 if f8 else 2,
+                               "decode_split_e4m3" if f8 else "decode_split")
+        elif part == "mixed":
+            r = measure_mixed(gen.ALL[args.mixed_workload], args, device, torch, dist_on, peaks, peak_kind)
+        elif part == "projection":
+            r = measure_projection(gen.ALL[args.prefill_workload], args, device, torch, dist_on, peaks, peak_kind)
+        else:
+            r = measure_sampling(args, device, torch, dist_on, peaks, peak_kind)
+        for k in ("host", "ds", "decode_host"):
+            r.pop(k, None)
+        line[part] = r
+    if dist_on:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_ours(args):
     import torch
 
@@ -674,6 +718,9 @@ def run_ours(args):
     peaks, peak_kind = load_peaks()
     cpu = cpu_wanted(args)
     pop = lambda d, *ks: [d.pop(k, None) for k in ks][0]
+    if args.only:
+        run_only(args, device, torch, dist_on, peaks, peak_kind, rank)
+        return
     w = gen.ALL[args.workload]
     assert w.decode_from == w.batch, "the headline workload is a prefill workload"
     with ClockSampler(local_rank) as clk:

@@ -79,3 +79,34 @@ def test_sampling_edge_cases_and_determinism():
 def test_sampling_single_token_vocabulary():
     h = gen.make_sampling_inputs(5, 1, seed=5)
     assert (gpu_tokens(h) == 0).all()
+
+
+def test_sampling_crossing_in_each_bin_range():
+    """Rows whose truncation ends in each part of the kernel's bins of
+    z = (max - l) log2(e) / T: the fine bins (z < 32), the coarse bins
+    (32 <= z < 159.875, tiny weights), the last bin (weight 0), and crossing
+    bins holding more tokens than the kernel copies (its slower path), plus
+    ties at the crossing."""
+    V = 32000
+    h = gen.make_sampling_inputs(8, V, seed=8, greedy_share=0.0)
+    g = torch.Generator().manual_seed(81)
+    x = torch.randn((8, V), generator=g) * 2.0
+    x[0] = 0.25                                           # one bin holds every token
+    x[1, 5] = 40.0                                        # the rest far below: weight 0
+    x[7] = torch.round(x[7] * 2.0) / 2.0                  # many ties
+    h["logits"] = x
+    rows = [  # (temperature, top_k, top_p)
+        (1.0, 50, 1.0),                                   # count crossing among 32000 equal keys
+        (0.3, 2000, 1.0),                                 # count crossing in the weight-0 bin
+        (0.05, 20, 1.0),                                  # count crossing in the coarse bins
+        (0.3, 0, float(np.nextafter(np.float32(1.0), np.float32(0.0)))),  # mass crossing in the coarse bins
+        (1.5, 0, 0.9),                                    # mass crossing in dense fine bins
+        (1.5, 0, 0.5),
+        (1.0, 2000, 0.95),
+        (1.0, 100, 1.0),                                  # ties at the crossing are kept
+    ]
+    for b, (t, k, p) in enumerate(rows):
+        h["temperature"][b], h["top_k"][b], h["top_p"][b] = t, k, p
+    a = gpu_tokens(h)
+    check(h, a)
+    assert np.array_equal(a, gpu_tokens(h))
