@@ -65,8 +65,8 @@ struct SampleSmem {
       uint32_t cnt_fine[kFine];
       uint32_t mlo_fine[kFine];        // mass = mhi << 32 | mlo (weights up to 2^40): the low words
       uint32_t mhi_fine[kFine];        // wrap into the high ones, counted by the adding thread
-      u64 cm_mid[kMid];                // count << 32 | mass: weights up to 2^8 (z >= 32), sums below
-                                       // 2^29 (V <= 2^23)
+      uint32_t cnt_mid[kMid];
+      uint32_t mass_mid[kMid];         // weights up to 2^8 (z >= 32): sums below 2^29 (V <= 2^23)
       uint32_t cnt_far[kFar];          // bin 0 included
     } h;
     struct {                           // step 3 when the copies overflow: digit histograms
@@ -536,7 +536,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 4)
       sm.u.h.mlo_fine[i] = 0;
       sm.u.h.mhi_fine[i] = 0;
     }
-    for (int i = tid; i < kMid; i += kThreads) sm.u.h.cm_mid[i] = 0;
+    for (int i = tid; i < kMid; i += kThreads) {
+      sm.u.h.cnt_mid[i] = 0;
+      sm.u.h.mass_mid[i] = 0;
+    }
     for (int i = tid; i < kFar; i += kThreads) sm.u.h.cnt_far[i] = 0;
     if (tid == 0) sm.cand_n = 0;
     __syncthreads();
@@ -568,7 +571,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 4)
           }
           if (up) atomicAdd(&sm.u.h.mhi_fine[bi], up);
         } else {
-          atomicAdd(&sm.u.h.cm_mid[kFine + kMid - 1 - m], (1ull << 32) | w);
+          atomicAdd(&sm.u.h.cnt_mid[kFine + kMid - 1 - m], 1u);
+          if (w) atomicAdd(&sm.u.h.mass_mid[kFine + kMid - 1 - m], (uint32_t)w);
         }
       } else if (z < 175.875f) {
         atomicAdd(&sm.u.h.cnt_far[kFar - 1 - (uint32_t)__fmul_rn(__fsub_rn(z, 48.f), 8.f)], 1u);
@@ -618,9 +622,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 4)
         } else if (d >= kFar) {
 #pragma unroll
           for (int r = 0; r < kCluster; ++r) {
-            const u64 cm = peer_u64(&sm.u.h.cm_mid[d - kFar], r);
-            cv[r] = (uint32_t)(cm >> 32);
-            mv[r] = cm & 0xffffffffull;
+            cv[r] = peer_u32(&sm.u.h.cnt_mid[d - kFar], r);
+            mv[r] = peer_u32(&sm.u.h.mass_mid[d - kFar], r);
           }
         } else {
 #pragma unroll
