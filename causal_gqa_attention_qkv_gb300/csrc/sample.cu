@@ -42,8 +42,15 @@ namespace gb300 {
 
 namespace {
 
-constexpr int kCluster = 8;            // CTAs per row
-constexpr int kThreads = 256;
+#ifndef SAMPLE_CLUSTER
+#define SAMPLE_CLUSTER 8
+#endif
+#ifndef SAMPLE_THREADS
+#define SAMPLE_THREADS 256
+#endif
+constexpr int kCluster = SAMPLE_CLUSTER;  // CTAs per row
+constexpr int kThreads = SAMPLE_THREADS;
+constexpr int kMinBlocks = 1024 / kThreads;  // resident CTAs per SM the registers must allow
 constexpr int kWarps = kThreads / 32;
 constexpr int kFine = 2048;            // bins 2048 .. 4095: z in [0, 32), 1/64 wide
 constexpr int kMid = 1024;             // bins 1024 .. 2047: z in [32, 48), 1/64 wide
@@ -446,7 +453,7 @@ __device__ __forceinline__ void for_chunks(const float* row, int lo, int hi, int
   }
 }
 
-__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 4)
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, kMinBlocks)
     sample_kernel(const SamplePar p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SampleSmem& sm = *reinterpret_cast<SampleSmem*>(smem_raw);
