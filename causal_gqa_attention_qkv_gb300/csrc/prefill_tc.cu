@@ -603,15 +603,14 @@ __device__ void softmax_tile(const TcPar& p, const SeqInfo* seq_tab, const int* 
           }
         }
       } else {
+        // the whole row per TMEM wait
+        uint32_t sr[kKeys];
 #pragma unroll
-        for (int c0 = 0; c0 < kKeys; c0 += 32) {
-          uint32_t sr[32];
-          tc::ld_32x32b_x32(s_tmem + c0, sr);
-          tc::wait_ld();
+        for (int c0 = 0; c0 < kKeys; c0 += 32) tc::ld_32x32b_x32(s_tmem + c0, sr + c0);
+        tc::wait_ld();
 #pragma unroll
-          for (int c = 0; c < 32; c += 2)
-            mx[(c >> 1) & 3] = max3f(mx[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-        }
+        for (int c = 0; c < kKeys; c += 2)
+          mx[(c >> 1) & 3] = max3f(mx[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
       }
       const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
       // Reference max: moved only when the row max grows by more than 2^8
