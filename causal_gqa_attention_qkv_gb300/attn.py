@@ -98,9 +98,17 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+# The current stream's handle without building a torch Stream object per call
+# (a few microseconds on every launch); torch.cuda.current_stream() otherwise.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream=None):
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
+    if _raw_stream is not None:
+        return ctypes.c_void_p(_raw_stream(torch.cuda.current_device()))
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
 def config(num_q_heads: int, num_kv_heads: int, head_dim: int, rms_eps: float = 1e-6,
@@ -122,7 +130,21 @@ class KVCache:
     k_scale: float = 1.0        # E4M3 caches: entry = code * scale
     v_scale: float = 1.0
 
+    # The C struct is built (and the tensors checked) once and rebuilt when a
+    # field is assigned; tensors changed in place (resize_, set_) are not seen.
+    def __setattr__(self, name, value):
+        object.__setattr__(self, name, value)
+        if name != "_built":
+            object.__setattr__(self, "_built", None)
+
     def struct(self) -> AttnKV:
+        built = self.__dict__.get("_built")
+        if built is None:
+            built = self._make_struct()
+            object.__setattr__(self, "_built", built)
+        return built
+
+    def _make_struct(self) -> AttnKV:
         fp8 = self.k_cache.dtype == torch.uint8
         for name in ("k_cache", "v_cache"):
             t = getattr(self, name)

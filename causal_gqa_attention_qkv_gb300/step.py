@@ -39,14 +39,17 @@ class DeviceStep:
 
     def run(self, stream=None) -> None:
         """Issue the step: prefill part then decode part (asynchronous)."""
+        v = self.__dict__.get("_views")
+        if v is None:  # the row ranges of the two parts, sliced once
+            n = self.n_prefill_tokens
+            v = (self.qkv[:n], self.out[:n], self.qkv[n:], self.out[n:])
+            self.__dict__["_views"] = v
         if self.kv_prefill is not None:
-            attn.prefill(self.cfg, self.qkv[:self.n_prefill_tokens], self.q_norm_w, self.k_norm_w,
-                         self.cu_seqlens, self.max_seqlen, self.kv_prefill,
-                         self.out[:self.n_prefill_tokens], self.workspace, stream)
+            attn.prefill(self.cfg, v[0], self.q_norm_w, self.k_norm_w, self.cu_seqlens, self.max_seqlen,
+                         self.kv_prefill, v[1], self.workspace, stream)
         if self.kv_decode is not None:
-            attn.decode(self.cfg, self.qkv[self.n_prefill_tokens:], self.q_norm_w, self.k_norm_w,
-                        self.max_cache_len, self.kv_decode, self.out[self.n_prefill_tokens:],
-                        self.workspace, stream)
+            attn.decode(self.cfg, v[2], self.q_norm_w, self.k_norm_w, self.max_cache_len, self.kv_decode,
+                        v[3], self.workspace, stream)
 
     def status(self) -> int:
         return attn.get_status(self.workspace)
