@@ -320,8 +320,8 @@ def measure(w, steps, warmup, device, torch, dist_on, page_size=0, kv_dtype="bf1
 def measure_e2e(w, ds, host, steps, warmup, device, torch):
     """The same prefill through the public API from pinned host buffers:
     step.HostPrefill copies the qkv rows in, runs prepare + attention and
-    copies the output rows out, in token chunks pipelined over three streams
-    (chunk c + 1 copied in and chunk c - 1 copied out while chunk c runs).
+    copies the output rows out, in token chunks pipelined over five streams
+    (copies in, prepare, attention on two streams in turn, copies out).
     Every copy is inside the timed events; the per-chunk metadata (int32
     cu_seqlens and cached lengths) is copied in with the first chunk."""
     from causal_gqa_attention_qkv_gb300 import step
@@ -343,7 +343,7 @@ def measure_e2e(w, ds, host, steps, warmup, device, torch):
         if k >= warmup:
             times.append(e0.elapsed_time(e1))
             launches += n
-    if ds.status() != 0:
+    if ds.status() != 0 or hp.status() != 0:
         raise RuntimeError("device status set in the end-to-end prefill")
     return sum(times) / len(times), h2d, d2h, launches, len(plan.chunks)
 

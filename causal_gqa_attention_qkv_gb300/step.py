@@ -122,21 +122,25 @@ class ChunkPlan:
         return self.meta_host.numel() * 4
 
 
-def plan_chunks(cu_seqlens, cache_lens, chunk_tokens: int):
+def plan_chunks(cu_seqlens, cache_lens, chunk_tokens):
     """Split a packed prefill call (host cu_seqlens [B + 1], cached lengths
-    [B]) into calls of at most chunk_tokens tokens, in token order.  Chunk c
-    covers tokens [t0, t1) and the requests [b0, b1) with tokens there; its
-    own cu_seqlens counts each request's tokens inside the chunk, and each
-    request's cached length is advanced by its tokens in earlier chunks.
-    Returns (chunks, metadata): the chunks' cu_seqlens and cached lengths
-    are int32 runs of the metadata list at the offsets the chunks record."""
+    [B]) into calls of at most chunk_tokens tokens, in token order
+    (chunk_tokens: one size, or the sizes of the first chunks, the last one
+    repeated).  Chunk c covers tokens [t0, t1) and the requests [b0, b1) with
+    tokens there; its own cu_seqlens counts each request's tokens inside the
+    chunk, and each request's cached length is advanced by its tokens in
+    earlier chunks.  Returns (chunks, metadata): the chunks' cu_seqlens and
+    cached lengths are int32 runs of the metadata list at the offsets the
+    chunks record."""
+    sizes = [int(chunk_tokens)] if isinstance(chunk_tokens, int) else [int(x) for x in chunk_tokens]
+    assert sizes and min(sizes) >= 1
     cu = [int(x) for x in cu_seqlens]
     cl = [int(x) for x in cache_lens]
     N = cu[-1]
     chunks, meta = [], []
     t0, b0 = 0, 0
     while t0 < N:
-        t1 = min(N, t0 + chunk_tokens)
+        t1 = min(N, t0 + sizes[min(len(chunks), len(sizes) - 1)])
         while cu[b0 + 1] <= t0:  # first request with a token at or after t0
             b0 += 1
         b1 = b0
@@ -157,9 +161,13 @@ def plan_chunks(cu_seqlens, cache_lens, chunk_tokens: int):
 
 
 class HostPrefill:
-    """Prefill from pinned host buffers in token chunks, pipelined over three
-    streams: while the kernels of chunk c run, the qkv rows of chunk c + 1
-    are copied in and the output rows of chunk c - 1 are copied out.
+    """Prefill from pinned host buffers in token chunks, pipelined over five
+    streams: the qkv rows of each chunk are copied in (one stream), prepared
+    (K/V appended, Q normed and rotated; one stream, in chunk order), their
+    attention runs on one of two streams in turn, each with a workspace of
+    its own, and the output rows are copied out (one stream).  Chunk c + 1's
+    attention needs only the cache entries of chunks 0 .. c + 1, so it can
+    start on the SMs that chunk c's attention has already left.
 
     Each chunk is a valid packed prefill call of its own: the part of every
     request that falls in its token range, with that request's cached length
@@ -174,14 +182,18 @@ class HostPrefill:
     """
 
     def __init__(self, cfg: attn.AttnConfig, q_norm_w, k_norm_w, kv: attn.KVCache, workspace, qkv_dev,
-                 q_stage, out_dev, chunk_tokens: int = 4096):
+                 q_stage, out_dev, chunk_tokens=4096):
         self.cfg, self.q_norm_w, self.k_norm_w, self.kv = cfg, q_norm_w, k_norm_w, kv
         self.ws, self.qkv_dev, self.q_stage, self.out_dev = workspace, qkv_dev, q_stage, out_dev
-        self.chunk_tokens = max(1, int(chunk_tokens))
+        # one chunk size, or the sizes of the first chunks (the last repeated)
+        self.chunk_tokens = (max(1, int(chunk_tokens)) if isinstance(chunk_tokens, int)
+                             else [max(1, int(x)) for x in chunk_tokens])
         dev = qkv_dev.device
         self.s_in = torch.cuda.Stream(device=dev)
-        self.s_run = torch.cuda.Stream(device=dev)
+        self.s_prep = torch.cuda.Stream(device=dev)
+        self.s_att = (torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
         self.s_out = torch.cuda.Stream(device=dev)
+        self.ws_att = (workspace, attn.workspace_like(workspace))  # one item counter per attention stream
 
     def plan(self, cu_seqlens, cache_lens) -> ChunkPlan:
         """Chunks of the packed batch given its host cu_seqlens [B + 1] and
@@ -209,21 +221,30 @@ class HostPrefill:
                 e = torch.cuda.Event()
                 e.record(self.s_in)
                 landed.append(e)
-        with torch.cuda.stream(self.s_run):
+        prepped, ckvs = [], []
+        with torch.cuda.stream(self.s_prep):
             for c, e in zip(plan.chunks, landed):
-                self.s_run.wait_event(e)
+                self.s_prep.wait_event(e)
                 cu_d = meta[c.cu[0]:c.cu[1]]
                 ckv = attn.KVCache(kv.k_cache, kv.v_cache, kv.slot_base[c.b0:c.b1], meta[c.cl[0]:c.cl[1]],
                                    kv.slot_capacity[c.b0:c.b1],
                                    None if kv.page_table is None else kv.page_table[c.b0:c.b1],
                                    kv.page_size, kv.k_scale, kv.v_scale)
-                q = self.q_stage[c.t0:c.t1]
-                attn.prefill_prepare(self.cfg, self.qkv_dev[c.t0:c.t1], self.q_norm_w, self.k_norm_w, cu_d, ckv, q,
-                                     self.ws, self.s_run)
-                attn.prefill_attend(self.cfg, q, cu_d, c.max_seqlen, ckv, self.out_dev[c.t0:c.t1], self.ws,
-                                    self.s_run)
+                attn.prefill_prepare(self.cfg, self.qkv_dev[c.t0:c.t1], self.q_norm_w, self.k_norm_w, cu_d, ckv,
+                                     self.q_stage[c.t0:c.t1], self.ws, self.s_prep)
+                e1 = torch.cuda.Event()
+                e1.record(self.s_prep)  # also: the chunks before it are prepared
+                prepped.append(e1)
+                ckvs.append((cu_d, ckv))
+        for i, (c, e1, (cu_d, ckv)) in enumerate(zip(plan.chunks, prepped, ckvs)):
+            s = self.s_att[i % 2]
+            s.wait_stream(cur)
+            with torch.cuda.stream(s):
+                s.wait_event(e1)
+                attn.prefill_attend(self.cfg, self.q_stage[c.t0:c.t1], cu_d, c.max_seqlen, ckv,
+                                    self.out_dev[c.t0:c.t1], self.ws_att[i % 2], s)
                 e2 = torch.cuda.Event()
-                e2.record(self.s_run)
+                e2.record(s)
                 done.append(e2)
         with torch.cuda.stream(self.s_out):
             for c, e in zip(plan.chunks, done):
@@ -233,3 +254,7 @@ class HostPrefill:
                 end_event.record(self.s_out)
         cur.wait_stream(self.s_out)
         return 2 * len(plan.chunks)
+
+    def status(self) -> int:
+        """The device status words of both workspaces (0: no error)."""
+        return max(attn.get_status(w) for w in self.ws_att)

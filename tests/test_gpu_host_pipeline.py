@@ -34,7 +34,7 @@ def _pipelined(w, host, chunk_tokens):
     out_h = torch.full((N, w.num_q_heads * w.head_dim), float("nan"), dtype=torch.bfloat16).pin_memory()
     hp.run(plan, qkv_h, out_h)
     torch.cuda.synchronize()
-    assert ds.status() == 0
+    assert ds.status() == 0 and hp.status() == 0
     return ds, out_h, plan
 
 
