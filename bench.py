@@ -326,7 +326,7 @@ def measure_e2e(w, ds, host, steps, warmup, device, torch):
     cu_seqlens and cached lengths) is copied in with the first chunk."""
     from causal_gqa_attention_qkv_gb300 import step
     N = w.num_tokens
-    chunk = max(2048, -(-N // 8))
+    chunk = max(4096, -(-N // 8))
     qkv_h = host["qkv"].pin_memory()
     out_h = torch.empty(ds.out.shape, dtype=ds.out.dtype).pin_memory()
     q_stage = torch.empty((N, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=device)

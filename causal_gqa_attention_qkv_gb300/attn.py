@@ -189,14 +189,6 @@ def new_workspace(cfg: AttnConfig, max_tokens: int, max_batch: int, max_kv_len: 
     return ws
 
 
-def workspace_like(ws: torch.Tensor) -> torch.Tensor:
-    """A second workspace of the same size as ``ws`` (allocated with torch,
-    initialised), for calls that run at the same time as calls on ``ws``."""
-    w2 = torch.empty_like(ws)
-    _check(load().attn_workspace_init(_ptr(w2), w2.numel(), _stream()))
-    return w2
-
-
 def _bf16(t, name):
     assert t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous(), name
     return _ptr(t)

@@ -193,7 +193,8 @@ class HostPrefill:
         self.s_prep = torch.cuda.Stream(device=dev)
         self.s_att = (torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
         self.s_out = torch.cuda.Stream(device=dev)
-        self.ws_att = (workspace, attn.workspace_like(workspace))  # one item counter per attention stream
+        # one item counter per attention stream; attention alone needs only the workspace header
+        self.ws_att = (workspace, attn.new_workspace(cfg, 0, 1, 1, device=dev))
 
     def plan(self, cu_seqlens, cache_lens) -> ChunkPlan:
         """Chunks of the packed batch given its host cu_seqlens [B + 1] and
