@@ -17,12 +17,12 @@ namespace {
 constexpr int kWarpsPerBlock = 8;  // one token per warp
 constexpr int kThreads = kWarpsPerBlock * 32;
 #ifndef PROLOGUE_BATCH
-#define PROLOGUE_BATCH 12
+#define PROLOGUE_BATCH 6
 #endif
 #ifndef PROLOGUE_MIN_BLOCKS
 #define PROLOGUE_MIN_BLOCKS 2
 #endif
-constexpr int kBatch = PROLOGUE_BATCH;  // head-vector loads issued per lane before processing
+constexpr int kBatch = PROLOGUE_BATCH;  // steps whose loads are issued before processing
 constexpr int kMinBlocks = PROLOGUE_MIN_BLOCKS;  // resident blocks per SM the registers allow
 
 struct ProloguePar {
@@ -59,17 +59,21 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& raw, float (&y)[8]) {
   }
 }
 
-// One warp per token.  The token's head vectors (D bf16 = D/8 lanes x 16 bytes)
-// are taken HPI = 32 / (D/8) at a time, lane l holding 8 values of head
-// hd0 + j*HPI + l / (D/8): each load instruction reads 512 contiguous bytes of
-// the qkv row and each store writes whole head vectors.  cos/sin of the
-// token's D/2 rotation angles are computed once (D/64 per lane) and handed to
-// the lanes that need them with shuffles.  F8: the cache holds E4M3 codes.
+// One warp per token.  A head vector (D bf16) is held by L = D/16 lanes, lane
+// li taking the 8 values at 8*li and the 8 values at D/2 + 8*li: the two
+// members of each rotation pair (i, i + D/2) sit in the same lane, so RoPE
+// needs no data exchange and the norm's sum of squares needs log2(L) shuffles.
+// HPI = 32 / L head vectors are taken per step; each load instruction reads
+// HPI runs of 128 contiguous bytes and each store writes whole runs.  cos/sin
+// of the token's D/2 rotation angles are computed once (D/64 per lane) and
+// handed to the lanes that need them with shuffles.  F8: the cache holds E4M3
+// codes.
 template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) kv_append_kernel(const ProloguePar p) {
-  constexpr int L = D / 8;      // lanes per head vector
+  constexpr int L = D / 16;     // lanes per head vector
   constexpr int HPI = 32 / L;   // head vectors per warp-wide step
-  constexpr int PPL = D / 64;   // rotation pairs computed per lane
+  constexpr int H2 = D / 2;     // offset of the second member of a rotation pair
+  constexpr int PPL = D / 64;   // rotation angles computed per lane
   const int lane = threadIdx.x & 31;
   launch_dependents();  // the attention kernel after this one may be scheduled as CTAs finish
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
@@ -85,12 +89,14 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) kv_append_kernel(const P
   const uint16_t* row = p.qkv + (int64_t)t * W + (int64_t)hd0 * D + li * 8;
 
   // first batch of loads before anything that depends on the request lookup
-  uint4 raw[kBatch];
+  uint4 raw_a[kBatch], raw_b[kBatch];  // values 8*li.. and D/2 + 8*li.. of a head
 #pragma unroll
   for (int k = 0; k < kBatch; ++k) {
     const int hd = k * HPI + sub;
-    raw[k] = (k < nstep && hd < nhead) ? __ldg(reinterpret_cast<const uint4*>(row + (int64_t)hd * D))
-                                       : make_uint4(0, 0, 0, 0);
+    const bool in = k < nstep && hd < nhead;
+    const uint16_t* src = row + (int64_t)hd * D;
+    raw_a[k] = in ? __ldg(reinterpret_cast<const uint4*>(src)) : make_uint4(0, 0, 0, 0);
+    raw_b[k] = in ? __ldg(reinterpret_cast<const uint4*>(src + H2)) : make_uint4(0, 0, 0, 0);
   }
 
   // request of this token: 0 = none, 1 = Q only (region too small), 2 = Q and cache
@@ -127,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) kv_append_kernel(const P
   }
   if (ok == 0) return;  // warp-uniform
 
-  // cos/sin of the 8 rotation pairs this lane's values belong to
+  // cos/sin of the 8 rotation pairs 8*li .. 8*li + 7 this lane's values belong to
   float cs[8], sn[8];
   {
     float c_own[PPL], s_own[PPL];
@@ -136,30 +142,21 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) kv_append_kernel(const P
       const int pr = lane * PPL + e;
       rope_angle(pos, p.freqs.hi[pr], p.freqs.lo[pr], p.freqs, &c_own[e], &s_own[e]);
     }
-    const int pair0 = (li % (L / 2)) * 8;
-    const bool first_half = li < L / 2;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const int pr = pair0 + e;
-      float c = __shfl_sync(0xffffffffu, c_own[e % PPL], pr / PPL);
-      float s = __shfl_sync(0xffffffffu, s_own[e % PPL], pr / PPL);
-      cs[e] = c;
-      sn[e] = first_half ? -s : s;  // x_i c - x_{i+D/2} s  /  x_{i+D/2} c + x_i s
+      const int pr = li * 8 + e;
+      cs[e] = __shfl_sync(0xffffffffu, c_own[e % PPL], pr / PPL);
+      sn[e] = __shfl_sync(0xffffffffu, s_own[e % PPL], pr / PPL);
     }
   }
-  float qw[8], kw[8];
+  uint4 qw[2], kw[2];  // norm weights of this lane's 16 values, bf16 pairs
   {
-    const uint4 k4 = __ldg(reinterpret_cast<const uint4*>(p.k_norm_w + li * 8));
-    const uint4 q4 = with_q ? __ldg(reinterpret_cast<const uint4*>(p.q_norm_w + li * 8)) : k4;
-    const uint32_t* kr = reinterpret_cast<const uint32_t*>(&k4);
-    const uint32_t* qr = reinterpret_cast<const uint32_t*>(&q4);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      kw[2 * e] = bf16_lo(kr[e]);
-      kw[2 * e + 1] = bf16_hi(kr[e]);
-      qw[2 * e] = bf16_lo(qr[e]);
-      qw[2 * e + 1] = bf16_hi(qr[e]);
-    }
+    const uint16_t* wk = p.k_norm_w + li * 8;
+    const uint16_t* wq = with_q ? p.q_norm_w + li * 8 : wk;
+    kw[0] = __ldg(reinterpret_cast<const uint4*>(wk));
+    kw[1] = __ldg(reinterpret_cast<const uint4*>(wk + H2));
+    qw[0] = __ldg(reinterpret_cast<const uint4*>(wq));
+    qw[1] = __ldg(reinterpret_cast<const uint4*>(wq + H2));
   }
   uint16_t* q_row = with_q ? p.q_out + (int64_t)t * p.Hq * D + li * 8 : nullptr;
   const int64_t cache_row = slot * p.Hkv * D + li * 8;
@@ -169,9 +166,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) kv_append_kernel(const P
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
         const int hd = (base + k) * HPI + sub;
-        raw[k] = (base + k < nstep && hd < nhead)
-                     ? __ldg(reinterpret_cast<const uint4*>(row + (int64_t)hd * D))
-                     : make_uint4(0, 0, 0, 0);
+        const bool in = base + k < nstep && hd < nhead;
+        const uint16_t* src = row + (int64_t)hd * D;
+        raw_a[k] = in ? __ldg(reinterpret_cast<const uint4*>(src)) : make_uint4(0, 0, 0, 0);
+        raw_b[k] = in ? __ldg(reinterpret_cast<const uint4*>(src + H2)) : make_uint4(0, 0, 0, 0);
       }
     }
 #pragma unroll
@@ -188,56 +186,84 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) kv_append_kernel(const P
           const int64_t e0 = cache_row + (int64_t)(hd - p.Hq - p.Hkv) * D;
           if constexpr (F8) {
             float y[8];
-            unpack_bf16x8(raw[k], y);
-            *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.v_cache) + e0) = e4m3x8(y, p.inv_v);
+            uint8_t* dst = static_cast<uint8_t*>(p.v_cache) + e0;
+            unpack_bf16x8(raw_a[k], y);
+            *reinterpret_cast<uint2*>(dst) = e4m3x8(y, p.inv_v);
+            unpack_bf16x8(raw_b[k], y);
+            *reinterpret_cast<uint2*>(dst + H2) = e4m3x8(y, p.inv_v);
           } else {
-            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.v_cache) + e0) = raw[k];
+            uint16_t* dst = static_cast<uint16_t*>(p.v_cache) + e0;
+            *reinterpret_cast<uint4*>(dst) = raw_a[k];
+            *reinterpret_cast<uint4*>(dst + H2) = raw_b[k];
           }
         }
         continue;
       }
-      float x[8];
-      const uint32_t* rw = reinterpret_cast<const uint32_t*>(&raw[k]);
+      float xa[8], xb[8];
+      unpack_bf16x8(raw_a[k], xa);
+      unpack_bf16x8(raw_b[k], xb);
+      float sa = 0.f, sb = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        x[2 * e] = bf16_lo(rw[e]);
-        x[2 * e + 1] = bf16_hi(rw[e]);
+      for (int e = 0; e < 8; ++e) {
+        sa = fmaf(xa[e], xa[e], sa);
+        sb = fmaf(xb[e], xb[e], sb);
       }
-      float ss = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+      float ss = sa + sb;
 #pragma unroll
       for (int off = L / 2; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
       const float inv = rsqrtf(ss * (1.0f / D) + p.eps);
+      {
+        float wa[8], wb[8];
+        unpack_bf16x8(is_q ? qw[0] : kw[0], wa);
+        unpack_bf16x8(is_q ? qw[1] : kw[1], wb);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = (is_q ? qw[e] : kw[e]) * (x[e] * inv);
-      float rot[8];
+        for (int e = 0; e < 8; ++e) {
+          xa[e] = wa[e] * (xa[e] * inv);
+          xb[e] = wb[e] * (xb[e] * inv);
+        }
+      }
+      // rotate-half: (x_i, x_{i+D/2}) -> (x_i c - x_{i+D/2} s, x_{i+D/2} c + x_i s)
+      float ra[8], rb[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float other = __shfl_xor_sync(0xffffffffu, x[e], L / 2);
-        rot[e] = fmaf(other, sn[e], x[e] * cs[e]);
+        ra[e] = fmaf(xb[e], -sn[e], xa[e] * cs[e]);
+        rb[e] = fmaf(xa[e], sn[e], xb[e] * cs[e]);
       }
       if (!live) continue;
       const int64_t e0 = cache_row + (int64_t)(hd - (is_v ? p.Hq + p.Hkv : p.Hq)) * D;
       if (F8 && !is_q) {
         if (ok == 2) {
-          float y[8];
-          if (is_v) unpack_bf16x8(raw[k], y);
           uint8_t* dst = static_cast<uint8_t*>(is_v ? p.v_cache : p.k_cache) + e0;
-          *reinterpret_cast<uint2*>(dst) = e4m3x8(is_v ? y : rot, is_v ? p.inv_v : p.inv_k);
+          const float r = is_v ? p.inv_v : p.inv_k;
+          float ya[8], yb[8];
+          if (is_v) {
+            unpack_bf16x8(raw_a[k], ya);
+            unpack_bf16x8(raw_b[k], yb);
+          }
+          *reinterpret_cast<uint2*>(dst) = e4m3x8(is_v ? ya : ra, r);
+          *reinterpret_cast<uint2*>(dst + H2) = e4m3x8(is_v ? yb : rb, r);
         }
         continue;
       }
       // the prepared Q is f16 next to an E4M3 cache (the prefill kernel's operand type), else bf16
-      const uint4 v4 = is_v ? raw[k]
-                       : F8 ? make_uint4(pack_f16(rot[0], rot[1]), pack_f16(rot[2], rot[3]),
-                                         pack_f16(rot[4], rot[5]), pack_f16(rot[6], rot[7]))
-                            : make_uint4(pack_bf16(rot[0], rot[1]), pack_bf16(rot[2], rot[3]),
-                                         pack_bf16(rot[4], rot[5]), pack_bf16(rot[6], rot[7]));
-      if (is_q) {
-        *reinterpret_cast<uint4*>(q_row + (int64_t)hd * D) = v4;
-      } else if (ok == 2) {
-        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(is_v ? p.v_cache : p.k_cache) + e0) = v4;
+      uint4 va, vb;
+      if (is_v) {
+        va = raw_a[k];
+        vb = raw_b[k];
+      } else if (F8) {
+        va = make_uint4(pack_f16(ra[0], ra[1]), pack_f16(ra[2], ra[3]), pack_f16(ra[4], ra[5]), pack_f16(ra[6], ra[7]));
+        vb = make_uint4(pack_f16(rb[0], rb[1]), pack_f16(rb[2], rb[3]), pack_f16(rb[4], rb[5]), pack_f16(rb[6], rb[7]));
+      } else {
+        va = make_uint4(pack_bf16(ra[0], ra[1]), pack_bf16(ra[2], ra[3]), pack_bf16(ra[4], ra[5]),
+                        pack_bf16(ra[6], ra[7]));
+        vb = make_uint4(pack_bf16(rb[0], rb[1]), pack_bf16(rb[2], rb[3]), pack_bf16(rb[4], rb[5]),
+                        pack_bf16(rb[6], rb[7]));
+      }
+      uint16_t* dst = is_q ? q_row + (int64_t)hd * D
+                           : static_cast<uint16_t*>(is_v ? p.v_cache : p.k_cache) + e0;
+      if (is_q || ok == 2) {
+        *reinterpret_cast<uint4*>(dst) = va;
+        *reinterpret_cast<uint4*>(dst + H2) = vb;
       }
     }
   }

@@ -39,8 +39,9 @@ def written_slots(host: dict, lo: int = 0, hi: int | None = None) -> np.ndarray:
 # (y_i, y_j), j = i +- D/2, is at most K_FP32_REL * |(y_i, y_j)| (the pair's
 # Euclidean norm, which the rotation preserves), from its operations with unit
 # roundoff u = 2^-24:
-#   sum of squares: 8 fused multiply-adds per lane + log2(D/8) shuffle adds,
-#     all terms >= 0: relative error <= 12u;
+#   sum of squares: two chains of 8 fused multiply-adds per lane, their sum,
+#     then log2(D/16) shuffle adds: at most 12 roundings on any term, all
+#     terms >= 0, so relative error <= 12u;
 #   (ss / D + eps) one rounding, rsqrtf <= 2 ulp (4u) as CUDA documents it:
 #     the inverse norm within 12u / 2 + u / 2 + 4u = 10.5u;
 #   x * inv, then * w: two roundings, so y within 12.5u relative;
