@@ -19,10 +19,16 @@ constexpr int kThreads = kWarpsPerBlock * 32;
 #ifndef PROLOGUE_BATCH
 #define PROLOGUE_BATCH 6
 #endif
+#ifndef PROLOGUE_BATCH_F8
+#define PROLOGUE_BATCH_F8 4
+#endif
 #ifndef PROLOGUE_MIN_BLOCKS
 #define PROLOGUE_MIN_BLOCKS 2
 #endif
-constexpr int kBatch = PROLOGUE_BATCH;  // steps whose loads are issued before processing
+// steps whose loads are issued before processing (bf16 cache, E4M3 cache):
+// as many as fit in the registers two blocks per SM allow
+constexpr int kBatchBf16 = PROLOGUE_BATCH;
+constexpr int kBatchF8 = PROLOGUE_BATCH_F8;
 constexpr int kMinBlocks = PROLOGUE_MIN_BLOCKS;  // resident blocks per SM the registers allow
 
 struct ProloguePar {
@@ -37,6 +43,7 @@ struct ProloguePar {
   KvIndex kv;
   int32_t* status;
   int32_t B, N, Hq, Hkv;
+  int64_t steps_per_warp;  // each warp takes this many consecutive (token, step) units
   float eps;
   RopeFreqs freqs;
 };
@@ -74,10 +81,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) kv_append_kernel(const P
   constexpr int HPI = 32 / L;   // head vectors per warp-wide step
   constexpr int H2 = D / 2;     // offset of the second member of a rotation pair
   constexpr int PPL = D / 64;   // rotation angles computed per lane
+  constexpr int kBatch = F8 ? kBatchF8 : kBatchBf16;
   const int lane = threadIdx.x & 31;
   launch_dependents();  // the attention kernel after this one may be scheduled as CTAs finish
-  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-  if (t >= p.N) return;
 
   const bool with_q = p.q_out != nullptr;
   const int hd0 = with_q ? 0 : p.Hq;               // first head handled (Q heads only with q_out)
@@ -86,69 +92,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) kv_append_kernel(const P
   const int64_t W = (int64_t)(p.Hq + 2 * p.Hkv) * D;
   const int li = lane % L;
   const int sub = lane / L;                        // head slot within a step
-  const uint16_t* row = p.qkv + (int64_t)t * W + (int64_t)hd0 * D + li * 8;
 
-  // first batch of loads before anything that depends on the request lookup
-  uint4 raw_a[kBatch], raw_b[kBatch];  // values 8*li.. and D/2 + 8*li.. of a head
-#pragma unroll
-  for (int k = 0; k < kBatch; ++k) {
-    const int hd = k * HPI + sub;
-    const bool in = k < nstep && hd < nhead;
-    const uint16_t* src = row + (int64_t)hd * D;
-    raw_a[k] = in ? __ldg(reinterpret_cast<const uint4*>(src)) : make_uint4(0, 0, 0, 0);
-    raw_b[k] = in ? __ldg(reinterpret_cast<const uint4*>(src + H2)) : make_uint4(0, 0, 0, 0);
-  }
-
-  // request of this token: 0 = none, 1 = Q only (region too small), 2 = Q and cache
-  int ok = 0;
-  int64_t slot = 0;
-  float pos = 0.f;
-  {
-    int b = t, j = 0, n = 1;
-    bool seq_ok = true;
-    if (p.cu_seqlens) {
-      int lo = 0, hi = p.B;  // largest b with cu[b] <= t
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(p.cu_seqlens + mid) <= t) lo = mid; else hi = mid;
-      }
-      b = lo;
-      const int c0 = __ldg(p.cu_seqlens + b);
-      j = t - c0;
-      n = __ldg(p.cu_seqlens + b + 1) - c0;
-      seq_ok = j >= 0 && j < n;
-      if (!seq_ok && lane == 0) set_status(p.status, ATTN_STATUS_SEQLENS);
-      if (t == 0 && lane == 0 && __ldg(p.cu_seqlens + p.B) != p.N) set_status(p.status, ATTN_STATUS_SEQLENS);
-    }
-    if (seq_ok) {
-      const ReqInfo r = load_request(p.kv, b, n);
-      ok = 1;
-      pos = (float)(r.cached + j);
-      slot = r.valid ? cache_slot(p.kv, r, r.cached + j) : -1;
-      if (slot >= 0)
-        ok = 2;
-      else if (lane == 0)
-        set_status(p.status, ATTN_STATUS_CAPACITY);
-    }
-  }
-  if (ok == 0) return;  // warp-uniform
-
-  // cos/sin of the 8 rotation pairs 8*li .. 8*li + 7 this lane's values belong to
-  float cs[8], sn[8];
-  {
-    float c_own[PPL], s_own[PPL];
-#pragma unroll
-    for (int e = 0; e < PPL; ++e) {
-      const int pr = lane * PPL + e;
-      rope_angle(pos, p.freqs.hi[pr], p.freqs.lo[pr], p.freqs, &c_own[e], &s_own[e]);
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int pr = li * 8 + e;
-      cs[e] = __shfl_sync(0xffffffffu, c_own[e % PPL], pr / PPL);
-      sn[e] = __shfl_sync(0xffffffffu, s_own[e % PPL], pr / PPL);
-    }
-  }
   uint4 qw[2], kw[2];  // norm weights of this lane's 16 values, bf16 pairs
   {
     const uint16_t* wk = p.k_norm_w + li * 8;
@@ -158,114 +102,193 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) kv_append_kernel(const P
     qw[0] = __ldg(reinterpret_cast<const uint4*>(wq));
     qw[1] = __ldg(reinterpret_cast<const uint4*>(wq + H2));
   }
-  uint16_t* q_row = with_q ? p.q_out + (int64_t)t * p.Hq * D + li * 8 : nullptr;
-  const int64_t cache_row = slot * p.Hkv * D + li * 8;
 
-  for (int base = 0; base < nstep; base += kBatch) {
-    if (base > 0) {
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        const int hd = (base + k) * HPI + sub;
-        const bool in = base + k < nstep && hd < nhead;
-        const uint16_t* src = row + (int64_t)hd * D;
-        raw_a[k] = in ? __ldg(reinterpret_cast<const uint4*>(src)) : make_uint4(0, 0, 0, 0);
-        raw_b[k] = in ? __ldg(reinterpret_cast<const uint4*>(src + H2)) : make_uint4(0, 0, 0, 0);
-      }
-    }
-#pragma unroll
+  // this warp's units: steps [u0, u_end) of the N x nstep (token, step) grid,
+  // the same count for every warp so that all of them finish together
+  int64_t u0 = ((int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5)) * p.steps_per_warp;
+  const int64_t u_end = min((int64_t)p.N * nstep, u0 + p.steps_per_warp);
+  if (u0 >= u_end) return;
+  int t = (int)(u0 / nstep);
+  int s_begin = (int)(u0 - (int64_t)t * nstep);
+  for (;;) {
+    const int s_end = (int)min((int64_t)nstep, s_begin + (u_end - u0));
+    const uint16_t* row = p.qkv + (int64_t)t * W + (int64_t)hd0 * D + li * 8;
+
+    // first batch of loads before anything that depends on the request lookup
+    uint4 raw_a[kBatch], raw_b[kBatch];  // values 8*li.. and D/2 + 8*li.. of a head
+  #pragma unroll
     for (int k = 0; k < kBatch; ++k) {
-      if (base + k >= nstep) break;  // warp-uniform
-      const int hd = hd0 + (base + k) * HPI + sub;  // head index in the qkv row
-      const bool live = hd < p.Hq + 2 * p.Hkv;
-      const bool is_q = hd < p.Hq;
-      const bool is_v = hd >= p.Hq + p.Hkv;
-      // steps made only of V heads: bit copies into the cache
-      const bool step_all_v = hd0 + (base + k) * HPI >= p.Hq + p.Hkv;
-      if (step_all_v) {
-        if (live && ok == 2) {
-          const int64_t e0 = cache_row + (int64_t)(hd - p.Hq - p.Hkv) * D;
-          if constexpr (F8) {
-            float y[8];
-            uint8_t* dst = static_cast<uint8_t*>(p.v_cache) + e0;
-            unpack_bf16x8(raw_a[k], y);
-            *reinterpret_cast<uint2*>(dst) = e4m3x8(y, p.inv_v);
-            unpack_bf16x8(raw_b[k], y);
-            *reinterpret_cast<uint2*>(dst + H2) = e4m3x8(y, p.inv_v);
-          } else {
-            uint16_t* dst = static_cast<uint16_t*>(p.v_cache) + e0;
-            *reinterpret_cast<uint4*>(dst) = raw_a[k];
-            *reinterpret_cast<uint4*>(dst + H2) = raw_b[k];
-          }
+      const int hd = (s_begin + k) * HPI + sub;
+      const bool in = s_begin + k < s_end && hd < nhead;
+      const uint16_t* src = row + (int64_t)hd * D;
+      raw_a[k] = in ? __ldg(reinterpret_cast<const uint4*>(src)) : make_uint4(0, 0, 0, 0);
+      raw_b[k] = in ? __ldg(reinterpret_cast<const uint4*>(src + H2)) : make_uint4(0, 0, 0, 0);
+    }
+
+    // request of this token: 0 = none, 1 = Q only (region too small), 2 = Q and cache
+    int ok = 0;
+    int64_t slot = 0;
+    float pos = 0.f;
+    {
+      int b = t, j = 0, n = 1;
+      bool seq_ok = true;
+      if (p.cu_seqlens) {
+        int lo = 0, hi = p.B;  // largest b with cu[b] <= t
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (__ldg(p.cu_seqlens + mid) <= t) lo = mid; else hi = mid;
         }
-        continue;
+        b = lo;
+        const int c0 = __ldg(p.cu_seqlens + b);
+        j = t - c0;
+        n = __ldg(p.cu_seqlens + b + 1) - c0;
+        seq_ok = j >= 0 && j < n;
+        if (!seq_ok && lane == 0) set_status(p.status, ATTN_STATUS_SEQLENS);
+        if (t == 0 && lane == 0 && __ldg(p.cu_seqlens + p.B) != p.N) set_status(p.status, ATTN_STATUS_SEQLENS);
       }
-      float xa[8], xb[8];
-      unpack_bf16x8(raw_a[k], xa);
-      unpack_bf16x8(raw_b[k], xb);
-      float sa = 0.f, sb = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        sa = fmaf(xa[e], xa[e], sa);
-        sb = fmaf(xb[e], xb[e], sb);
-      }
-      float ss = sa + sb;
-#pragma unroll
-      for (int off = L / 2; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-      const float inv = rsqrtf(ss * (1.0f / D) + p.eps);
-      {
-        float wa[8], wb[8];
-        unpack_bf16x8(is_q ? qw[0] : kw[0], wa);
-        unpack_bf16x8(is_q ? qw[1] : kw[1], wb);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          xa[e] = wa[e] * (xa[e] * inv);
-          xb[e] = wb[e] * (xb[e] * inv);
-        }
-      }
-      // rotate-half: (x_i, x_{i+D/2}) -> (x_i c - x_{i+D/2} s, x_{i+D/2} c + x_i s)
-      float ra[8], rb[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        ra[e] = fmaf(xb[e], -sn[e], xa[e] * cs[e]);
-        rb[e] = fmaf(xa[e], sn[e], xb[e] * cs[e]);
-      }
-      if (!live) continue;
-      const int64_t e0 = cache_row + (int64_t)(hd - (is_v ? p.Hq + p.Hkv : p.Hq)) * D;
-      if (F8 && !is_q) {
-        if (ok == 2) {
-          uint8_t* dst = static_cast<uint8_t*>(is_v ? p.v_cache : p.k_cache) + e0;
-          const float r = is_v ? p.inv_v : p.inv_k;
-          float ya[8], yb[8];
-          if (is_v) {
-            unpack_bf16x8(raw_a[k], ya);
-            unpack_bf16x8(raw_b[k], yb);
-          }
-          *reinterpret_cast<uint2*>(dst) = e4m3x8(is_v ? ya : ra, r);
-          *reinterpret_cast<uint2*>(dst + H2) = e4m3x8(is_v ? yb : rb, r);
-        }
-        continue;
-      }
-      // the prepared Q is f16 next to an E4M3 cache (the prefill kernel's operand type), else bf16
-      uint4 va, vb;
-      if (is_v) {
-        va = raw_a[k];
-        vb = raw_b[k];
-      } else if (F8) {
-        va = make_uint4(pack_f16(ra[0], ra[1]), pack_f16(ra[2], ra[3]), pack_f16(ra[4], ra[5]), pack_f16(ra[6], ra[7]));
-        vb = make_uint4(pack_f16(rb[0], rb[1]), pack_f16(rb[2], rb[3]), pack_f16(rb[4], rb[5]), pack_f16(rb[6], rb[7]));
-      } else {
-        va = make_uint4(pack_bf16(ra[0], ra[1]), pack_bf16(ra[2], ra[3]), pack_bf16(ra[4], ra[5]),
-                        pack_bf16(ra[6], ra[7]));
-        vb = make_uint4(pack_bf16(rb[0], rb[1]), pack_bf16(rb[2], rb[3]), pack_bf16(rb[4], rb[5]),
-                        pack_bf16(rb[6], rb[7]));
-      }
-      uint16_t* dst = is_q ? q_row + (int64_t)hd * D
-                           : static_cast<uint16_t*>(is_v ? p.v_cache : p.k_cache) + e0;
-      if (is_q || ok == 2) {
-        *reinterpret_cast<uint4*>(dst) = va;
-        *reinterpret_cast<uint4*>(dst + H2) = vb;
+      if (seq_ok) {
+        const ReqInfo r = load_request(p.kv, b, n);
+        ok = 1;
+        pos = (float)(r.cached + j);
+        slot = r.valid ? cache_slot(p.kv, r, r.cached + j) : -1;
+        if (slot >= 0)
+          ok = 2;
+        else if (lane == 0)
+          set_status(p.status, ATTN_STATUS_CAPACITY);
       }
     }
+    if (ok != 0) {  // warp-uniform
+
+      // cos/sin of the 8 rotation pairs 8*li .. 8*li + 7 this lane's values belong to
+      float cs[8], sn[8];
+      {
+        float c_own[PPL], s_own[PPL];
+    #pragma unroll
+        for (int e = 0; e < PPL; ++e) {
+          const int pr = lane * PPL + e;
+          rope_angle(pos, p.freqs.hi[pr], p.freqs.lo[pr], p.freqs, &c_own[e], &s_own[e]);
+        }
+    #pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int pr = li * 8 + e;
+          cs[e] = __shfl_sync(0xffffffffu, c_own[e % PPL], pr / PPL);
+          sn[e] = __shfl_sync(0xffffffffu, s_own[e % PPL], pr / PPL);
+        }
+      }
+      uint16_t* q_row = with_q ? p.q_out + (int64_t)t * p.Hq * D + li * 8 : nullptr;
+      const int64_t cache_row = slot * p.Hkv * D + li * 8;
+
+      for (int base = s_begin; base < s_end; base += kBatch) {
+        if (base > s_begin) {
+    #pragma unroll
+          for (int k = 0; k < kBatch; ++k) {
+            const int hd = (base + k) * HPI + sub;
+            const bool in = base + k < s_end && hd < nhead;
+            const uint16_t* src = row + (int64_t)hd * D;
+            raw_a[k] = in ? __ldg(reinterpret_cast<const uint4*>(src)) : make_uint4(0, 0, 0, 0);
+            raw_b[k] = in ? __ldg(reinterpret_cast<const uint4*>(src + H2)) : make_uint4(0, 0, 0, 0);
+          }
+        }
+    #pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          if (base + k >= s_end) break;  // warp-uniform
+          const int hd = hd0 + (base + k) * HPI + sub;  // head index in the qkv row
+          const bool live = hd < p.Hq + 2 * p.Hkv;
+          const bool is_q = hd < p.Hq;
+          const bool is_v = hd >= p.Hq + p.Hkv;
+          // steps made only of V heads: bit copies into the cache
+          const bool step_all_v = hd0 + (base + k) * HPI >= p.Hq + p.Hkv;
+          if (step_all_v) {
+            if (live && ok == 2) {
+              const int64_t e0 = cache_row + (int64_t)(hd - p.Hq - p.Hkv) * D;
+              if constexpr (F8) {
+                float y[8];
+                uint8_t* dst = static_cast<uint8_t*>(p.v_cache) + e0;
+                unpack_bf16x8(raw_a[k], y);
+                *reinterpret_cast<uint2*>(dst) = e4m3x8(y, p.inv_v);
+                unpack_bf16x8(raw_b[k], y);
+                *reinterpret_cast<uint2*>(dst + H2) = e4m3x8(y, p.inv_v);
+              } else {
+                uint16_t* dst = static_cast<uint16_t*>(p.v_cache) + e0;
+                *reinterpret_cast<uint4*>(dst) = raw_a[k];
+                *reinterpret_cast<uint4*>(dst + H2) = raw_b[k];
+              }
+            }
+            continue;
+          }
+          float xa[8], xb[8];
+          unpack_bf16x8(raw_a[k], xa);
+          unpack_bf16x8(raw_b[k], xb);
+          float sa = 0.f, sb = 0.f;
+    #pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            sa = fmaf(xa[e], xa[e], sa);
+            sb = fmaf(xb[e], xb[e], sb);
+          }
+          float ss = sa + sb;
+    #pragma unroll
+          for (int off = L / 2; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+          const float inv = rsqrtf(ss * (1.0f / D) + p.eps);
+          {
+            float wa[8], wb[8];
+            unpack_bf16x8(is_q ? qw[0] : kw[0], wa);
+            unpack_bf16x8(is_q ? qw[1] : kw[1], wb);
+    #pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              xa[e] = wa[e] * (xa[e] * inv);
+              xb[e] = wb[e] * (xb[e] * inv);
+            }
+          }
+          // rotate-half: (x_i, x_{i+D/2}) -> (x_i c - x_{i+D/2} s, x_{i+D/2} c + x_i s)
+          float ra[8], rb[8];
+    #pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            ra[e] = fmaf(xb[e], -sn[e], xa[e] * cs[e]);
+            rb[e] = fmaf(xa[e], sn[e], xb[e] * cs[e]);
+          }
+          if (!live) continue;
+          const int64_t e0 = cache_row + (int64_t)(hd - (is_v ? p.Hq + p.Hkv : p.Hq)) * D;
+          if (F8 && !is_q) {
+            if (ok == 2) {
+              uint8_t* dst = static_cast<uint8_t*>(is_v ? p.v_cache : p.k_cache) + e0;
+              const float r = is_v ? p.inv_v : p.inv_k;
+              float ya[8], yb[8];
+              if (is_v) {
+                unpack_bf16x8(raw_a[k], ya);
+                unpack_bf16x8(raw_b[k], yb);
+              }
+              *reinterpret_cast<uint2*>(dst) = e4m3x8(is_v ? ya : ra, r);
+              *reinterpret_cast<uint2*>(dst + H2) = e4m3x8(is_v ? yb : rb, r);
+            }
+            continue;
+          }
+          // the prepared Q is f16 next to an E4M3 cache (the prefill kernel's operand type), else bf16
+          uint4 va, vb;
+          if (is_v) {
+            va = raw_a[k];
+            vb = raw_b[k];
+          } else if (F8) {
+            va = make_uint4(pack_f16(ra[0], ra[1]), pack_f16(ra[2], ra[3]), pack_f16(ra[4], ra[5]), pack_f16(ra[6], ra[7]));
+            vb = make_uint4(pack_f16(rb[0], rb[1]), pack_f16(rb[2], rb[3]), pack_f16(rb[4], rb[5]), pack_f16(rb[6], rb[7]));
+          } else {
+            va = make_uint4(pack_bf16(ra[0], ra[1]), pack_bf16(ra[2], ra[3]), pack_bf16(ra[4], ra[5]),
+                            pack_bf16(ra[6], ra[7]));
+            vb = make_uint4(pack_bf16(rb[0], rb[1]), pack_bf16(rb[2], rb[3]), pack_bf16(rb[4], rb[5]),
+                            pack_bf16(rb[6], rb[7]));
+          }
+          uint16_t* dst = is_q ? q_row + (int64_t)hd * D
+                               : static_cast<uint16_t*>(is_v ? p.v_cache : p.k_cache) + e0;
+          if (is_q || ok == 2) {
+            *reinterpret_cast<uint4*>(dst) = va;
+            *reinterpret_cast<uint4*>(dst + H2) = vb;
+          }
+        }
+      }
+    }  // ok != 0
+    u0 += s_end - s_begin;
+    if (u0 >= u_end) break;
+    ++t;
+    s_begin = 0;
   }
 }
 
@@ -292,7 +315,21 @@ cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t stream) {
   p.Hkv = a.cfg.num_kv_heads;
   p.eps = a.cfg.rms_eps;
   p.freqs = a.freqs;
-  const dim3 grid((a.N + kWarpsPerBlock - 1) / kWarpsPerBlock);
+  // (token, step) units: a step covers 32 / (D/16) head vectors of a token.
+  // Warps take equal runs of consecutive units; with more units than the
+  // resident warps (kMinBlocks blocks per SM) the runs are cut across token
+  // boundaries, else every warp takes one token.
+  const int hpi = 512 / a.cfg.head_dim;
+  const int nstep = (a.cfg.num_q_heads * (a.q_out ? 1 : 0) + 2 * a.cfg.num_kv_heads + hpi - 1) / hpi;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorInvalidDevice;
+  const int64_t units = (int64_t)a.N * nstep;
+  const int64_t resident = (int64_t)sms * kMinBlocks * kWarpsPerBlock;
+  p.steps_per_warp = std::max<int64_t>(nstep, (units + resident - 1) / resident);
+  const int64_t warps = (units + p.steps_per_warp - 1) / p.steps_per_warp;
+  const dim3 grid((unsigned)((warps + kWarpsPerBlock - 1) / kWarpsPerBlock));
   if (a.cfg.head_dim == 128) {
     if (f8) kv_append_kernel<128, true><<<grid, kThreads, 0, stream>>>(p);
     else kv_append_kernel<128, false><<<grid, kThreads, 0, stream>>>(p);
