@@ -215,6 +215,19 @@ def test_largest_head_counts(hq, hkv, d, lens, cache):
     run_and_compare(w, gen.make_inputs(w))
 
 
+@pytest.mark.parametrize("hq,hkv,d,lens,cache,kvd", [
+    (8, 1, 64, [3000, 1999, 1], [0, 100, 7], "bf16"),    # 2 steps of 8 heads, the second K + V
+    (6, 3, 128, [2500, 500], [0, 33], "bf16"),           # 3 steps of 4 heads, two of them mixed
+    (6, 3, 128, [2500, 500], [0, 33], "e4m3"),
+])
+def test_prologue_runs_cut_across_tokens(hq, hkv, d, lens, cache, kvd):
+    """Enough (token, step) units that the prologue's per-warp runs are cut
+    across token boundaries (steps per token not dividing the run length),
+    with steps that mix Q, K and V heads: every row and the caches."""
+    w = gen.custom(f"runs_{hq}_{hkv}_{d}_{kvd}", hq, hkv, d, lens, cache, seed=sum(lens) + d)
+    run_and_compare(w, gen.make_inputs(w, kv_dtype=kvd))
+
+
 def test_mixed_prefill_and_decode_small():
     w = gen.custom("mixed_small", 32, 8, 128, [100, 64, 1, 1, 1], [50, 0, 10, 700, 0], seed=77,
                    decode_from=2)
