@@ -316,9 +316,10 @@ cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t stream) {
   p.eps = a.cfg.rms_eps;
   p.freqs = a.freqs;
   // (token, step) units: a step covers 32 / (D/16) head vectors of a token.
-  // Warps take equal runs of consecutive units; with more units than the
-  // resident warps (kMinBlocks blocks per SM) the runs are cut across token
-  // boundaries, else every warp takes one token.
+  // Warps take equal runs of consecutive units, cut across token boundaries:
+  // with more units than the resident warps (kMinBlocks blocks per SM) every
+  // resident warp takes one run, else every unit gets a warp of its own (a
+  // decode append is latency-bound: its steps run side by side).
   const int hpi = 512 / a.cfg.head_dim;
   const int nstep = (a.cfg.num_q_heads * (a.q_out ? 1 : 0) + 2 * a.cfg.num_kv_heads + hpi - 1) / hpi;
   int dev = 0, sms = 0;
@@ -327,7 +328,7 @@ cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t stream) {
     return cudaErrorInvalidDevice;
   const int64_t units = (int64_t)a.N * nstep;
   const int64_t resident = (int64_t)sms * kMinBlocks * kWarpsPerBlock;
-  p.steps_per_warp = std::max<int64_t>(nstep, (units + resident - 1) / resident);
+  p.steps_per_warp = (units + resident - 1) / resident;
   const int64_t warps = (units + p.steps_per_warp - 1) / p.steps_per_warp;
   const dim3 grid((unsigned)((warps + kWarpsPerBlock - 1) / kWarpsPerBlock));
   if (a.cfg.head_dim == 128) {
