@@ -247,7 +247,7 @@ class Timed:
 
     def run(self, ev):
         """ev: list of 5 events: start, after prefill append, after prefill
-        attention, after decode append, after decode attention."""
+        attention, before the decode call, after it."""
         ds, attn = self.ds, self.attn
         n = ds.n_prefill_tokens
         ev[0].record()
@@ -262,11 +262,10 @@ class Timed:
             ev[1].record()
             ev[2].record()
         if ds.kv_decode is not None:
-            B = ds.qkv.shape[0] - n
-            attn.kv_append(ds.cfg, ds.qkv[n:], ds.k_norm_w, ds.decode_cu, ds.kv_decode, ds.workspace)
             ev[3].record()
-            attn.decode_attend(ds.cfg, ds.qkv[n:], ds.q_norm_w, ds.max_cache_len, ds.kv_decode,
-                               ds.out[n:], ds.workspace)
+            # the new tokens' K/V are appended inside the split kernel (one launch, two with a merge)
+            attn.decode(ds.cfg, ds.qkv[n:], ds.q_norm_w, ds.k_norm_w, ds.max_cache_len, ds.kv_decode,
+                        ds.out[n:], ds.workspace)
             ev[4].record()
         else:
             ev[3].record()
@@ -440,20 +439,19 @@ def measure_decode(wd, args, device, torch, dist_on, peaks, peak_kind, kv_dtype,
     over a cache of bf16 or E4M3 entries.  Bytes count the entries as stored."""
     md = measure(wd, args.steps, args.warmup, device, torch, dist_on, args.page_size, kv_dtype)
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    dms, dattend = max_over_ranks([md["ms"]["step"], md["ms"]["decode_attend"]], device)
+    dms, dcall = max_over_ranks([md["ms"]["step"], md["ms"]["decode_attend"]], device)
     nbytes = decode_bytes(wd, entry_bytes=entry_bytes)
-    attend_bytes = nbytes - wd.batch * 2 * wd.num_kv_heads * wd.head_dim * entry_bytes  # no append write
     hbm = float(peaks["hbm_gbs"])
     return {
         "value": round(whole_job_rate(nbytes, world, dms) / 1e9, 1), "unit": "GB/s",
         "ms_per_step": round(dms, 4), "workload": wd.name, "kv_dtype": kv_dtype, "bytes_per_step": nbytes,
-        "parts_ms": {"kv_append": round(md["ms"]["decode_append"], 4),
-                     "decode_attention": round(dattend, 4)},
-        "roofline": {"bound": "hbm", "kernel": "decode split-KV + combine",
-                     "achieved": round(attend_bytes / (dattend * 1e-3) / 1e9, 1), "peak": hbm,
+        "parts_ms": {"decode_split_and_merge": round(dcall, 4)},
+        "roofline": {"bound": "hbm", "kernel": "decode split-KV (K/V append inside) + combine",
+                     "bytes_per_launch": nbytes,
+                     "achieved": round(nbytes / (dcall * 1e-3) / 1e9, 1), "peak": hbm,
                      "peak_kind": f"hbm_gbs ({peak_kind})", "unit": "GB/s",
-                     "frac": round(attend_bytes / (dattend * 1e-3) / 1e9 / hbm, 4),
-                     "frac_of_8tbs_nominal": round(attend_bytes / (dattend * 1e-3) / 8e12, 4),
+                     "frac": round(nbytes / (dcall * 1e-3) / 1e9 / hbm, 4),
+                     "frac_of_8tbs_nominal": round(nbytes / (dcall * 1e-3) / 8e12, 4),
                      "traffic": recorded_traffic(traffic_kernel, source_sha("decode.cu", "common.cuh"))},
         "gpu_launches": md["launches"],
         "host": md["host"],
@@ -660,27 +658,27 @@ def measure_sampling(args, device, torch, dist_on, peaks, peak_kind, B=64) -> di
 def measure_mixed(wm, args, device, torch, dist_on, peaks, peak_kind) -> dict:
     """One serving step that mixes prefill chunks (on top of cached prefixes)
     with decode rows, issued back to back on one stream: the chunks'
-    prepare + attention, then the decode rows' append + attention.  The
+    prepare + attention, then the decode rows (append inside the split
+    kernel) and their merge.  The
     step's roofline fraction adds the tensor-bound and the HBM-bound parts:
     (chunk FLOPs / bf16 peak + decode bytes / HBM peak) / step time."""
     mm = measure(wm, args.steps, args.warmup, device, torch, dist_on, args.page_size)
     ms = mm["ms"]
-    step_ms, pp, pa, da, dd = max_over_ranks([ms["step"], ms["prefill_append"], ms["prefill_attend"],
-                                              ms["decode_append"], ms["decode_attend"]], device)
+    step_ms, pp, pa, dd = max_over_ranks([ms["step"], ms["prefill_append"], ms["prefill_attend"],
+                                          ms["decode_attend"]], device)
     fl = prefill_flops(wm, 0, wm.decode_from)
     nb = decode_bytes(wm, wm.decode_from, wm.batch)
     peak_t, hbm = float(peaks["bf16_tflops"]) * 1e12, float(peaks["hbm_gbs"]) * 1e9
     ideal_s = fl / peak_t + nb / hbm
-    attend_bytes = nb - (wm.batch - wm.decode_from) * 2 * wm.num_kv_heads * wm.head_dim * 2
     return {
         "workload": wm.name, "ms_per_step": round(step_ms, 4),
         "chunk_flops": fl, "decode_bytes": nb,
         "roofline_frac": round(ideal_s / (step_ms * 1e-3), 4),
         "roofline_peaks": f"bf16_tflops and hbm_gbs ({peak_kind})",
         "parts_ms": {"chunk_prepare": round(pp, 4), "chunk_attention": round(pa, 4),
-                     "decode_append": round(da, 4), "decode_attention": round(dd, 4)},
+                     "decode_rows": round(dd, 4)},
         "chunk_attention_tflops": round(fl / (pa * 1e-3) / 1e12, 2),
-        "decode_attention_gbs": round(attend_bytes / (dd * 1e-3) / 1e9, 1),
+        "decode_rows_gbs": round(nb / (dd * 1e-3) / 1e9, 1),
         "gpu_launches": mm["launches"],
         "host": mm["host"],
     }

@@ -222,8 +222,10 @@ size_t decode_ws_need(const attn_config_t* cfg, int32_t B, int32_t max_cache_len
   return kWsHeader + partial_bytes(*cfg, B, *max_splits);
 }
 
-int decode_attend(const attn_config_t* cfg, const void* qkv, const void* q_norm_w, int32_t B,
-                  int32_t max_cache_len, const attn_kv_t* kv, void* out, void* workspace,
+// Split-KV decode (and merge); with k_norm_w, the new tokens' K/V are
+// appended inside the split kernel first.
+int decode_attend(const attn_config_t* cfg, const void* qkv, const void* q_norm_w, const void* k_norm_w,
+                  int32_t B, int32_t max_cache_len, const attn_kv_t* kv, void* out, void* workspace,
                   cudaStream_t s) {
   int split_len = 0, max_splits = 1;
   decode_ws_need(cfg, B, max_cache_len, &split_len, &max_splits);
@@ -235,6 +237,7 @@ int decode_attend(const attn_config_t* cfg, const void* qkv, const void* q_norm_
   d.kv = *kv;
   d.qkv = qkv;
   d.q_norm_w = q_norm_w;
+  d.k_norm_w = k_norm_w;
   make_rope_freqs(cfg->rope_theta, cfg->head_dim, &d.freqs);
   d.out = out;
   d.part_o = reinterpret_cast<float*>(ws + kWsHeader);
@@ -346,7 +349,7 @@ int attn_decode_attend(const attn_config_t* cfg, const void* qkv, const void* q_
     return ATTN_EWORKSPACE;
   if ((rc = check_device())) return rc;
   if (B == 0) return ATTN_OK;
-  return decode_attend(cfg, qkv, q_norm_w, B, max_cache_len, kv, out, workspace,
+  return decode_attend(cfg, qkv, q_norm_w, nullptr, B, max_cache_len, kv, out, workspace,
                        static_cast<cudaStream_t>(stream));
 }
 
@@ -362,9 +365,8 @@ int attn_decode(const attn_config_t* cfg, const void* qkv, const void* q_norm_w,
     return ATTN_EWORKSPACE;
   if ((rc = check_device())) return rc;
   if (B == 0) return ATTN_OK;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if ((rc = append(cfg, qkv, nullptr, k_norm_w, nullptr, B, B, kv, nullptr, workspace, s))) return rc;
-  return decode_attend(cfg, qkv, q_norm_w, B, max_cache_len, kv, out, workspace, s);
+  return decode_attend(cfg, qkv, q_norm_w, k_norm_w, B, max_cache_len, kv, out, workspace,
+                       static_cast<cudaStream_t>(stream));
 }
 
 int attn_qkv_proj_prepare(const attn_config_t* cfg, const void* hidden, int32_t hidden_size, const void* w_qkv,

@@ -279,6 +279,93 @@ __device__ __forceinline__ void rope_angle(float pos, float f_hi, float f_lo, co
   __sincosf(r, s, c);  // |r| <= pi + 1e-6: hardware sin/cos, absolute error ~4e-7
 }
 
+// ---------------------------------------------------------------- head vectors, pair layout
+// A head vector of D bf16 values is held by L = D/16 consecutive lanes: lane
+// li of the group takes the 8 values at 8 li and the 8 values at D/2 + 8 li
+// (two 16-byte loads), so both members of every rotate-half pair (i, i + D/2)
+// sit in one lane.  The prologue kernel and the decode kernel's append both
+// use these, so they write the same cache entries bit for bit.
+
+// Eight bf16 values (16 bytes) as fp32, element i from bytes 2i, 2i + 1.
+__device__ __forceinline__ void unpack_bf16x8(const uint4& raw, float (&y)[8]) {
+  const uint32_t* rw = reinterpret_cast<const uint32_t*>(&raw);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    y[2 * e] = bf16_lo(rw[e]);
+    y[2 * e + 1] = bf16_hi(rw[e]);
+  }
+}
+
+// E4M3 codes of eight fp32 values times an fp32 factor (the product rounded
+// to fp32 first, as the cache format states), element i in byte i.
+__device__ __forceinline__ uint2 e4m3x8(const float (&y)[8], float r) {
+  uint2 v;
+  v.x = e4m3x2(__fmul_rn(y[0], r), __fmul_rn(y[1], r)) | (e4m3x2(__fmul_rn(y[2], r), __fmul_rn(y[3], r)) << 16);
+  v.y = e4m3x2(__fmul_rn(y[4], r), __fmul_rn(y[5], r)) | (e4m3x2(__fmul_rn(y[6], r), __fmul_rn(y[7], r)) << 16);
+  return v;
+}
+
+// cos/sin of the rotation pairs 8 li .. 8 li + 7 (li = lane % (D/16)) at
+// position pos: each lane computes D/64 of the D/2 angles, the lanes that
+// need them read them by shuffle.  All 32 lanes must call this.
+template <int D>
+__device__ __forceinline__ void pair_angles(float pos, const RopeFreqs& fr, int lane, float (&cs)[8],
+                                            float (&sn)[8]) {
+  constexpr int PPL = D / 64;
+  const int li = lane % (D / 16);
+  float c_own[PPL], s_own[PPL];
+#pragma unroll
+  for (int e = 0; e < PPL; ++e) {
+    const int pr = lane * PPL + e;
+    rope_angle(pos, fr.hi[pr], fr.lo[pr], fr, &c_own[e], &s_own[e]);
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int pr = li * 8 + e;
+    cs[e] = __shfl_sync(0xffffffffu, c_own[e % PPL], pr / PPL);
+    sn[e] = __shfl_sync(0xffffffffu, s_own[e % PPL], pr / PPL);
+  }
+}
+
+// RMSNorm and rotate-half of one head vector in the pair layout: raw_a /
+// raw_b are this lane's values at 8 li and D/2 + 8 li, w_a / w_b the norm
+// weights there (bf16).  Sum of squares: two chains of 8 fused multiply-adds,
+// their sum, log2(D/16) shuffle adds over the head's lanes; then
+// y = w * (x * rsqrt(ss / D + eps)) and (y_i, y_j) -> (y_i c - y_j s,
+// y_j c + y_i s) for j = i + D/2.  All 32 lanes must call this.
+template <int D>
+__device__ __forceinline__ void norm_rope_pair(const uint4& raw_a, const uint4& raw_b, const uint4& w_a,
+                                               const uint4& w_b, const float (&cs)[8], const float (&sn)[8],
+                                               float eps, float (&ra)[8], float (&rb)[8]) {
+  constexpr int L = D / 16;
+  float xa[8], xb[8];
+  unpack_bf16x8(raw_a, xa);
+  unpack_bf16x8(raw_b, xb);
+  float sa = 0.f, sb = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    sa = fmaf(xa[e], xa[e], sa);
+    sb = fmaf(xb[e], xb[e], sb);
+  }
+  float ss = sa + sb;
+#pragma unroll
+  for (int off = L / 2; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  const float inv = rsqrtf(ss * (1.0f / D) + eps);
+  float wa[8], wb[8];
+  unpack_bf16x8(w_a, wa);
+  unpack_bf16x8(w_b, wb);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    xa[e] = wa[e] * (xa[e] * inv);
+    xb[e] = wb[e] * (xb[e] * inv);
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    ra[e] = fmaf(xb[e], -sn[e], xa[e] * cs[e]);
+    rb[e] = fmaf(xa[e], sn[e], xb[e] * cs[e]);
+  }
+}
+
 // One query row (D bf16 values at `row`) normalised and rotated, delivered in
 // the m16n8k16 A-fragment distribution: this thread (quad member q = lane & 3)
 // holds columns 16ks + 2q + {0,1} in frag[ks][0] and 16ks + 8 + 2q + {0,1} in

@@ -9,6 +9,10 @@
 // applies it to all Hq/Hkv query heads of the group at the same time, so
 // every cached byte is read from HBM once per step.  Partial results (running max, sum, unscaled
 // output) of the splits are merged by log-sum-exp in a second kernel.
+// With k_norm_w set, the kernel also appends the new token's K and V: the CTA
+// of each (request, KV head) whose split holds position c_b writes them (K
+// normed and rotated, with the prologue kernel's arithmetic) before it loads
+// its first tile, so the whole decode step is one launch (two with a merge).
 #include "kernels.cuh"
 
 namespace gb300 {
@@ -29,6 +33,10 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 struct DecodePar {
   const uint16_t* qkv;       // [B, W]
   const uint16_t* q_norm_w;  // [D]
+  const uint16_t* k_norm_w;  // [D], or NULL: the cache already holds the new K/V
+  void* k_cache;             // written only with k_norm_w
+  void* v_cache;
+  float inv_k, inv_v;        // E4M3: fp32(1 / scale), rounded on the host
   RopeFreqs freqs;
   float eps;
   int32_t W;
@@ -37,7 +45,7 @@ struct DecodePar {
   float* part_ml;
   KvIndex kv;
   int32_t* status;
-  int32_t Hq, G, split_len, max_splits;
+  int32_t Hq, Hkv, G, split_len, max_splits;
   float scale_log2;  // log2(e) / sqrt(D), times k_scale for an E4M3 cache
   float v_scale;     // 1, or v_scale for an E4M3 cache
 };
@@ -68,6 +76,59 @@ __device__ __forceinline__ void named_sync_consumers() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
+// The new token of request b (position c_b): its K and V of KV head kh
+// written to the cache by one warp in the prologue kernel's pair layout and
+// arithmetic (lanes [0, D/16) K, lanes [D/16, D/8) V).  Each writer then
+// orders its stores before later async-proxy (TMA) reads, and the
+// __syncwarp hands that order to the lane that issues the tile loads.
+template <int D, bool F8>
+__device__ __forceinline__ void append_new_kv(const DecodePar& p, const ReqInfo& r, int b, int kh, int lane) {
+  constexpr int L = D / 16, H2 = D / 2;
+  const int li = lane % L, which = lane / L;  // 0: K, 1: V, else idle
+  const int64_t slot = cache_slot(p.kv, r, r.cached);
+  uint4 xa = make_uint4(0, 0, 0, 0), xb = xa;
+  if (which < 2) {
+    const uint16_t* src = p.qkv + (int64_t)b * p.W + (int64_t)(p.Hq + which * p.Hkv + kh) * D + li * 8;
+    xa = __ldg(reinterpret_cast<const uint4*>(src));
+    xb = __ldg(reinterpret_cast<const uint4*>(src + H2));
+  }
+  float cs[8], sn[8];
+  pair_angles<D>((float)r.cached, p.freqs, lane, cs, sn);
+  const uint4 wa = __ldg(reinterpret_cast<const uint4*>(p.k_norm_w + li * 8));
+  const uint4 wb = __ldg(reinterpret_cast<const uint4*>(p.k_norm_w + li * 8 + H2));
+  float ra[8], rb[8];
+  norm_rope_pair<D>(xa, xb, wa, wb, cs, sn, p.eps, ra, rb);
+  if (which < 2 && slot >= 0) {
+    const int64_t e0 = (slot * p.Hkv + kh) * D + li * 8;
+    if constexpr (F8) {
+      uint8_t* dst = static_cast<uint8_t*>(which == 0 ? p.k_cache : p.v_cache) + e0;
+      if (which == 0) {
+        *reinterpret_cast<uint2*>(dst) = e4m3x8(ra, p.inv_k);
+        *reinterpret_cast<uint2*>(dst + H2) = e4m3x8(rb, p.inv_k);
+      } else {
+        float y[8];
+        unpack_bf16x8(xa, y);
+        *reinterpret_cast<uint2*>(dst) = e4m3x8(y, p.inv_v);
+        unpack_bf16x8(xb, y);
+        *reinterpret_cast<uint2*>(dst + H2) = e4m3x8(y, p.inv_v);
+      }
+    } else {
+      uint16_t* dst = static_cast<uint16_t*>(which == 0 ? p.k_cache : p.v_cache) + e0;
+      if (which == 0) {
+        xa = make_uint4(pack_bf16(ra[0], ra[1]), pack_bf16(ra[2], ra[3]), pack_bf16(ra[4], ra[5]),
+                        pack_bf16(ra[6], ra[7]));
+        xb = make_uint4(pack_bf16(rb[0], rb[1]), pack_bf16(rb[2], rb[3]), pack_bf16(rb[4], rb[5]),
+                        pack_bf16(rb[6], rb[7]));
+      }
+      *reinterpret_cast<uint4*>(dst) = xa;
+      *reinterpret_cast<uint4*>(dst + H2) = xb;
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+  }
+  if (lane == 0 && slot < 0) set_status(p.status, ATTN_STATUS_CAPACITY);
+  __syncwarp();
+}
+
 // F8: the cache holds E4M3 codes.  The tiles are converted to f16 in
 // registers (exact) and the products run as f16 mma.sync.  Each lane then
 // reads contiguous bytes: for Q.K^T, quad member c takes the columns
@@ -90,11 +151,19 @@ __global__ void __launch_bounds__(kThreads, F8 ? DECODE_F8_MIN_BLOCKS : 0)
   const int split = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
   launch_dependents();  // the merge kernel may be scheduled as CTAs finish
   const ReqInfo r = load_request(p.kv, b, 1);  // request facts: written by the caller, not by a kernel
-  if (!r.valid) return;  // flagged by the prologue
+  const bool append = p.k_norm_w != nullptr;
+  if (!r.valid) {  // nothing written (with the append kernel before this one: flagged there)
+    if (append && split == 0 && kh == 0 && threadIdx.x == 0) set_status(p.status, ATTN_STATUS_CAPACITY);
+    return;
+  }
   const int kv_len = r.cached + 1;
   const int n_splits = (kv_len + p.split_len - 1) / p.split_len;
   if (n_splits > p.max_splits) {  // max_cache_len below this request's length
     if (split == 0 && kh == 0 && threadIdx.x == 0) set_status(p.status, ATTN_STATUS_BOUNDS);
+    if (append && split == p.max_splits - 1 && threadIdx.x < 32) {  // the new K/V are still appended
+      grid_dependency_wait();
+      append_new_kv<D, F8>(p, r, b, kh, threadIdx.x);
+    }
     return;
   }
   if (split >= n_splits) return;
@@ -116,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, F8 ? DECODE_F8_MIN_BLOCKS : 0)
   grid_dependency_wait();  // the append kernel's cache entries, earlier kernels' reads of the outputs
 
   if (warp == kConsumerWarps) {  // producer warp: one thread issues all TMA loads
+    if (append && split == n_splits - 1) append_new_kv<D, F8>(p, r, b, kh, lane);  // before the last tile's load
     if (lane == 0) {
       prefetch_tmap(&kmap);
       prefetch_tmap(&vmap);
@@ -488,6 +558,11 @@ int launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
   DecodePar p;
   p.qkv = static_cast<const uint16_t*>(a.qkv);
   p.q_norm_w = static_cast<const uint16_t*>(a.q_norm_w);
+  p.k_norm_w = static_cast<const uint16_t*>(a.k_norm_w);
+  p.k_cache = a.kv.k_cache;
+  p.v_cache = a.kv.v_cache;
+  p.inv_k = F8 ? 1.0f / a.kv.k_scale : 1.0f;
+  p.inv_v = F8 ? 1.0f / a.kv.v_scale : 1.0f;
   p.freqs = a.freqs;
   p.eps = a.cfg.rms_eps;
   p.W = (a.cfg.num_q_heads + 2 * a.cfg.num_kv_heads) * D;
@@ -497,6 +572,7 @@ int launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
   p.kv = kv_index(a.kv);
   p.status = a.status;
   p.Hq = a.cfg.num_q_heads;
+  p.Hkv = a.cfg.num_kv_heads;
   p.G = a.cfg.num_q_heads / a.cfg.num_kv_heads;
   p.split_len = a.split_len;
   p.max_splits = a.max_splits;

@@ -77,19 +77,6 @@ extern "C" int attn_decode_static_scratch(const attn_config_t* cfg, const void* 
   if ((rc = static_scratch(&scratch))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  PrologueArgs a;
-  a.cfg = *cfg;
-  a.qkv = qkv;
-  a.q_norm_w = nullptr;
-  a.k_norm_w = k_norm_w;
-  a.q_out = nullptr;       // Q is prepared inside the decode kernel
-  a.cu_seqlens = nullptr;  // token b is request b
-  a.B = B;
-  a.N = B;
-  a.kv = *kv;
-  a.status = device_status;
-  make_rope_freqs(cfg->rope_theta, cfg->head_dim, &a.freqs);
-  if (launch_prologue(a, s) != cudaSuccess) return ATTN_ELAUNCH;
 
   DecodeArgs d;
   d.cfg = *cfg;
@@ -97,7 +84,8 @@ extern "C" int attn_decode_static_scratch(const attn_config_t* cfg, const void* 
   d.kv = *kv;
   d.qkv = qkv;
   d.q_norm_w = q_norm_w;
-  d.freqs = a.freqs;
+  d.k_norm_w = k_norm_w;  // the new K/V are appended inside the split kernel
+  make_rope_freqs(cfg->rope_theta, cfg->head_dim, &d.freqs);
   d.out = out;
   d.part_o = static_cast<float*>(scratch);
   d.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + o_bytes);

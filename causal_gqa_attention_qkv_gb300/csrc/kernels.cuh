@@ -83,6 +83,7 @@ struct DecodeArgs {
   attn_kv_t kv;
   const void* qkv;       // [B, W] bf16
   const void* q_norm_w;  // [D] bf16
+  const void* k_norm_w;  // [D] bf16: append the new K/V inside the kernel; NULL: already in the cache
   RopeFreqs freqs;
   void* out;      // [B, Hq*D] bf16
   float* part_o;  // [B, Hq, max_splits, D] fp32

@@ -48,24 +48,6 @@ struct ProloguePar {
   RopeFreqs freqs;
 };
 
-// E4M3 codes of eight fp32 values times an fp32 factor (the product rounded
-// to fp32 first, as the cache format states), element i in byte i.
-__device__ __forceinline__ uint2 e4m3x8(const float (&y)[8], float r) {
-  uint2 v;
-  v.x = e4m3x2(__fmul_rn(y[0], r), __fmul_rn(y[1], r)) | (e4m3x2(__fmul_rn(y[2], r), __fmul_rn(y[3], r)) << 16);
-  v.y = e4m3x2(__fmul_rn(y[4], r), __fmul_rn(y[5], r)) | (e4m3x2(__fmul_rn(y[6], r), __fmul_rn(y[7], r)) << 16);
-  return v;
-}
-
-__device__ __forceinline__ void unpack_bf16x8(const uint4& raw, float (&y)[8]) {
-  const uint32_t* rw = reinterpret_cast<const uint32_t*>(&raw);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    y[2 * e] = bf16_lo(rw[e]);
-    y[2 * e + 1] = bf16_hi(rw[e]);
-  }
-}
-
 // One warp per token.  A head vector (D bf16) is held by L = D/16 lanes, lane
 // li taking the 8 values at 8*li and the 8 values at D/2 + 8*li: the two
 // members of each rotation pair (i, i + D/2) sit in the same lane, so RoPE
@@ -80,7 +62,6 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) kv_append_kernel(const P
   constexpr int L = D / 16;     // lanes per head vector
   constexpr int HPI = 32 / L;   // head vectors per warp-wide step
   constexpr int H2 = D / 2;     // offset of the second member of a rotation pair
-  constexpr int PPL = D / 64;   // rotation angles computed per lane
   constexpr int kBatch = F8 ? kBatchF8 : kBatchBf16;
   const int lane = threadIdx.x & 31;
   launch_dependents();  // the attention kernel after this one may be scheduled as CTAs finish
@@ -116,7 +97,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) kv_append_kernel(const P
 
     // first batch of loads before anything that depends on the request lookup
     uint4 raw_a[kBatch], raw_b[kBatch];  // values 8*li.. and D/2 + 8*li.. of a head
-  #pragma unroll
+#pragma unroll
     for (int k = 0; k < kBatch; ++k) {
       const int hd = (s_begin + k) * HPI + sub;
       const bool in = s_begin + k < s_end && hd < nhead;
@@ -161,26 +142,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) kv_append_kernel(const P
 
       // cos/sin of the 8 rotation pairs 8*li .. 8*li + 7 this lane's values belong to
       float cs[8], sn[8];
-      {
-        float c_own[PPL], s_own[PPL];
-    #pragma unroll
-        for (int e = 0; e < PPL; ++e) {
-          const int pr = lane * PPL + e;
-          rope_angle(pos, p.freqs.hi[pr], p.freqs.lo[pr], p.freqs, &c_own[e], &s_own[e]);
-        }
-    #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int pr = li * 8 + e;
-          cs[e] = __shfl_sync(0xffffffffu, c_own[e % PPL], pr / PPL);
-          sn[e] = __shfl_sync(0xffffffffu, s_own[e % PPL], pr / PPL);
-        }
-      }
+      pair_angles<D>(pos, p.freqs, lane, cs, sn);
       uint16_t* q_row = with_q ? p.q_out + (int64_t)t * p.Hq * D + li * 8 : nullptr;
       const int64_t cache_row = slot * p.Hkv * D + li * 8;
 
       for (int base = s_begin; base < s_end; base += kBatch) {
         if (base > s_begin) {
-    #pragma unroll
+#pragma unroll
           for (int k = 0; k < kBatch; ++k) {
             const int hd = (base + k) * HPI + sub;
             const bool in = base + k < s_end && hd < nhead;
@@ -189,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) kv_append_kernel(const P
             raw_b[k] = in ? __ldg(reinterpret_cast<const uint4*>(src + H2)) : make_uint4(0, 0, 0, 0);
           }
         }
-    #pragma unroll
+#pragma unroll
         for (int k = 0; k < kBatch; ++k) {
           if (base + k >= s_end) break;  // warp-uniform
           const int hd = hd0 + (base + k) * HPI + sub;  // head index in the qkv row
@@ -216,36 +184,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) kv_append_kernel(const P
             }
             continue;
           }
-          float xa[8], xb[8];
-          unpack_bf16x8(raw_a[k], xa);
-          unpack_bf16x8(raw_b[k], xb);
-          float sa = 0.f, sb = 0.f;
-    #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            sa = fmaf(xa[e], xa[e], sa);
-            sb = fmaf(xb[e], xb[e], sb);
-          }
-          float ss = sa + sb;
-    #pragma unroll
-          for (int off = L / 2; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-          const float inv = rsqrtf(ss * (1.0f / D) + p.eps);
-          {
-            float wa[8], wb[8];
-            unpack_bf16x8(is_q ? qw[0] : kw[0], wa);
-            unpack_bf16x8(is_q ? qw[1] : kw[1], wb);
-    #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              xa[e] = wa[e] * (xa[e] * inv);
-              xb[e] = wb[e] * (xb[e] * inv);
-            }
-          }
-          // rotate-half: (x_i, x_{i+D/2}) -> (x_i c - x_{i+D/2} s, x_{i+D/2} c + x_i s)
           float ra[8], rb[8];
-    #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            ra[e] = fmaf(xb[e], -sn[e], xa[e] * cs[e]);
-            rb[e] = fmaf(xa[e], sn[e], xb[e] * cs[e]);
-          }
+          norm_rope_pair<D>(raw_a[k], raw_b[k], is_q ? qw[0] : kw[0], is_q ? qw[1] : kw[1], cs, sn, p.eps, ra, rb);
           if (!live) continue;
           const int64_t e0 = cache_row + (int64_t)(hd - (is_v ? p.Hq + p.Hkv : p.Hq)) * D;
           if (F8 && !is_q) {

@@ -59,7 +59,7 @@ class DeviceStep:
         n = 2 if self.kv_prefill is not None else 0
         if self.kv_decode is not None:
             B = self.qkv.shape[0] - self.n_prefill_tokens
-            n += 2 + (1 if attn.decode_splits(self.cfg, B, self.max_cache_len) > 1 else 0)
+            n += 1 + (1 if attn.decode_splits(self.cfg, B, self.max_cache_len) > 1 else 0)
         return n
 
 

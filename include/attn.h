@@ -199,7 +199,10 @@ ATTN_API int attn_prefill(const attn_config_t* cfg, const void* qkv, const void*
 
 /* Decode: one new token per request (row b of qkv is request b's token at
  * position c_b), appended and attended over c_b + 1 keys with split-KV and a
- * log-sum-exp merge.  max_cache_len >= every c_b (host value).
+ * log-sum-exp merge.  max_cache_len >= every c_b (host value).  One kernel
+ * launch (two when a request spans several splits): the split that holds
+ * position c_b writes the new K/V before it reads its keys, with the same
+ * arithmetic as attn_kv_append.
  * out: bf16 [B, Hq*D].  Concept chapter section 4.2 "Decode";
  * transformer-basics "Prefill vs Decode" (one more row of the lower triangle). */
 ATTN_API int attn_decode(const attn_config_t* cfg, const void* qkv, const void* q_norm_w,
@@ -247,8 +250,9 @@ ATTN_API int attn_o_proj(const attn_config_t* cfg, const void* attn_out, int32_t
 ATTN_API int32_t attn_decode_splits(const attn_config_t* cfg, int32_t B, int32_t max_cache_len);
 
 /* Attention half of attn_decode (the cache must already hold the new
- * token's K/V at slot slot_base[b] + c_b).  attn_decode == attn_kv_append
- * (cu_seqlens = 0, 1, ..., B) followed by attn_decode_attend. */
+ * token's K/V at slot slot_base[b] + c_b).  attn_decode gives bit for bit the
+ * output and cache of attn_kv_append (cu_seqlens = 0, 1, ..., B) followed by
+ * attn_decode_attend, in fewer launches. */
 ATTN_API int attn_decode_attend(const attn_config_t* cfg, const void* qkv, const void* q_norm_w,
                                 int32_t B, int32_t max_cache_len, const attn_kv_t* kv, void* out,
                                 void* workspace, size_t ws_bytes, void* stream);

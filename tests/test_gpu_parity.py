@@ -166,6 +166,37 @@ def test_e4m3_decode_static_scratch_matches_workspace_decode():
     assert torch.equal(a.k_cache, b.k_cache) and torch.equal(a.v_cache, b.v_cache)
 
 
+@pytest.mark.parametrize("hq,hkv,d,cache,ps,kvd", [
+    (32, 8, 128, [0, 5, 63, 64, 700, 3000, 9000], 0, "bf16"),   # several splits per request
+    (4, 2, 64, [12, 300], 0, "bf16"),                          # one split: no merge
+    (16, 2, 128, [7, 129, 4000], 64, "bf16"),                  # paged
+    (32, 8, 128, [0, 5, 700, 3000, 9000], 0, "e4m3"),
+    (8, 8, 64, [12, 300, 5000], 128, "e4m3"),
+])
+def test_decode_append_inside_equals_append_then_attend(hq, hkv, d, cache, ps, kvd):
+    """attn_decode appends the new tokens' K/V inside the split kernel; the
+    result must equal attn_kv_append followed by attn_decode_attend bit for
+    bit (output and both caches), and match the oracle."""
+    from causal_gqa_attention_qkv_gb300 import attn, step
+    w = gen.custom(f"fused_{hq}_{hkv}_{d}_{ps}_{kvd}", hq, hkv, d, [1] * len(cache), cache,
+                   seed=len(cache) * 7 + d + ps, decode_from=0)
+    host = gen.make_inputs(w, page_size=ps, kv_dtype=kvd)
+    a = step.upload(w, host)
+    attn.decode(a.cfg, a.qkv, a.q_norm_w, a.k_norm_w, a.max_cache_len, a.kv_decode, a.out, a.workspace)
+    b = step.upload(w, host)
+    cu = torch.arange(len(cache) + 1, dtype=torch.int32, device=b.out.device)
+    attn.kv_append(b.cfg, b.qkv, b.k_norm_w, cu, b.kv_decode, b.workspace)
+    attn.decode_attend(b.cfg, b.qkv, b.q_norm_w, b.max_cache_len, b.kv_decode, b.out, b.workspace)
+    torch.cuda.synchronize()
+    assert a.status() == 0 and b.status() == 0
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+    for x, y in ((a.k_cache, b.k_cache), (a.v_cache, b.v_cache)):
+        assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
+    ref = oracle.step(oracle.cfg_of(w), host)
+    check_out(gather_rows(a.out, w, ref["rows"]), ref["out"], w.name)
+    check_caches(host, ref, a.k_cache, a.v_cache)
+
+
 def test_e4m3_full_decode_batch_all_rows():
     w = gen.decode_batch()
     run_and_compare(w, gen.make_inputs(w, kv_dtype="e4m3"))
