@@ -46,7 +46,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 ONLY_PARTS = ("long_prefill", "prefill", "prefill_e4m3", "decode", "decode_e4m3", "mixed", "projection",
-              "sampling")
+              "sampling", "tiny")
 
 
 def parse_args():
@@ -513,7 +513,8 @@ def measure_tiny(args, device, torch, dist_on) -> dict:
     """The tiny workload (12-token prompt, Hq 4 / Hkv 2 / D 64, then the
     decode step at position 12): microseconds per call through the public
     calls, launch-latency bound (5 warm-up calls, then the median of the
-    timed ones, each bracketed by CUDA events)."""
+    timed ones, each bracketed by CUDA events); then both calls recorded
+    into one CUDA graph and replayed, timed the same way."""
     from causal_gqa_attention_qkv_gb300 import inputs as gen
     from causal_gqa_attention_qkv_gb300 import step
     w = gen.tiny()
@@ -544,6 +545,35 @@ def measure_tiny(args, device, torch, dist_on) -> dict:
         launches += ds.launches() * args.steps
         if ds.status() != 0:
             raise RuntimeError("device status set on the tiny workload")
+    # the same two calls recorded once into a CUDA graph and replayed: the
+    # launch floor without the per-call host work
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        pre.run()
+        dec.run()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        pre.run()
+        dec.run()
+    for _ in range(max(5, args.warmup)):
+        g.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e3)
+    (us,) = max_over_ranks([statistics.median(times)], device)
+    res["graph_prefill_and_decode_us"] = round(us, 2)
+    launches += (pre.launches() + dec.launches()) * args.steps
+    if pre.status() != 0 or dec.status() != 0:
+        raise RuntimeError("device status set on the tiny workload (graph replay)")
     res["gpu_launches"] = launches
     res["host"] = host
     res["decode_host"] = dhost
@@ -705,6 +735,8 @@ def run_only(args, device, torch, dist_on, peaks, peak_kind, rank):
             r = measure_mixed(gen.ALL[args.mixed_workload], args, device, torch, dist_on, peaks, peak_kind)
         elif part == "projection":
             r = measure_projection(gen.ALL[args.prefill_workload], args, device, torch, dist_on, peaks, peak_kind)
+        elif part == "tiny":
+            r = measure_tiny(args, device, torch, dist_on)
         else:
             r = measure_sampling(args, device, torch, dist_on, peaks, peak_kind)
         for k in ("host", "ds", "decode_host"):

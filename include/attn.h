@@ -37,6 +37,11 @@
  *   buffers, the stream and the workspace belong to the caller.  Calls are
  *   asynchronous on `stream` (a cudaStream_t; NULL is the legacy default
  *   stream).
+ * Graphs.  Every call except attn_get_status may be recorded by stream
+ *   capture into a CUDA graph (it allocates nothing, waits for nothing and
+ *   reads no device data on the host); replaying the graph repeats the
+ *   calls with the same results.  attn_decode_static_scratch wants its first
+ *   call before any capture (see there).
  * Sizes.  D in {64, 128}; Hq / Hkv in {1, 2, 4, 8}; Hq <= 128; the cache pool
  *   holds fewer than 2^31 slots; cache_lens[b] + n_b <= 2^24.
  * Errors.  A host-side check failure returns a negative ATTN_E* code and
@@ -44,8 +49,10 @@
  *   region cannot hold c_b + n_b entries, cu_seqlens that are not
  *   non-decreasing or do not end at N, a host bound max_seqlen or
  *   max_cache_len below the device data) set bits of the status word in the
- *   workspace (ATTN_STATUS_*); that request writes nothing to the cache and
- *   its output rows are left unwritten.  Nothing traps.
+ *   workspace (ATTN_STATUS_*).  A request whose region is too small writes
+ *   nothing to the cache; a request past max_seqlen / max_cache_len leaves
+ *   its output rows unwritten (its new K/V are still appended).  Nothing
+ *   traps.
  */
 #ifndef GB300_ATTN_H
 #define GB300_ATTN_H
