@@ -687,21 +687,41 @@ def measure_sampling(args, device, torch, dist_on, peaks, peak_kind, B=64) -> di
 
 def measure_mixed(wm, args, device, torch, dist_on, peaks, peak_kind) -> dict:
     """One serving step that mixes prefill chunks (on top of cached prefixes)
-    with decode rows, issued back to back on one stream: the chunks'
-    prepare + attention, then the decode rows (append inside the split
-    kernel) and their merge.  The
-    step's roofline fraction adds the tensor-bound and the HBM-bound parts:
+    with decode rows: the chunks' prepare + attention and the decode rows
+    (append inside the split kernel) with their merge.  parts_ms and
+    serial_ms_per_step time the parts one after the other on one stream;
+    ms_per_step times the step as step.DeviceStep.run issues it, the decode
+    rows on a side stream beside the chunks.  The roofline fraction adds the
+    tensor-bound and the HBM-bound parts:
     (chunk FLOPs / bf16 peak + decode bytes / HBM peak) / step time."""
     mm = measure(wm, args.steps, args.warmup, device, torch, dist_on, args.page_size)
     ms = mm["ms"]
-    step_ms, pp, pa, dd = max_over_ranks([ms["step"], ms["prefill_append"], ms["prefill_attend"],
-                                          ms["decode_attend"]], device)
+    # the step as step.DeviceStep.run issues it: the decode rows on a side
+    # stream beside the prefill chunks (the parts above run one after the other)
+    ds, flush = mm["ds"], L2Flush(device, torch)
+    for _ in range(args.warmup):
+        flush()
+        ds.run()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(args.steps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        ds.run()
+        e1.record()
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    if ds.status() != 0:
+        raise RuntimeError("device status set in the overlapped mixed step")
+    step_ms, serial_ms, pp, pa, dd = max_over_ranks([sum(times) / len(times), ms["step"], ms["prefill_append"],
+                                                     ms["prefill_attend"], ms["decode_attend"]], device)
     fl = prefill_flops(wm, 0, wm.decode_from)
     nb = decode_bytes(wm, wm.decode_from, wm.batch)
     peak_t, hbm = float(peaks["bf16_tflops"]) * 1e12, float(peaks["hbm_gbs"]) * 1e9
     ideal_s = fl / peak_t + nb / hbm
     return {
-        "workload": wm.name, "ms_per_step": round(step_ms, 4),
+        "workload": wm.name, "ms_per_step": round(step_ms, 4), "serial_ms_per_step": round(serial_ms, 4),
         "chunk_flops": fl, "decode_bytes": nb,
         "roofline_frac": round(ideal_s / (step_ms * 1e-3), 4),
         "roofline_peaks": f"bf16_tflops and hbm_gbs ({peak_kind})",
@@ -709,7 +729,7 @@ def measure_mixed(wm, args, device, torch, dist_on, peaks, peak_kind) -> dict:
                      "decode_rows": round(dd, 4)},
         "chunk_attention_tflops": round(fl / (pa * 1e-3) / 1e12, 2),
         "decode_rows_gbs": round(nb / (dd * 1e-3) / 1e9, 1),
-        "gpu_launches": mm["launches"],
+        "gpu_launches": mm["launches"] + ds.launches() * args.steps,
         "host": mm["host"],
     }
 

@@ -5,8 +5,11 @@ A packed batch may mix prefill requests (several new tokens, possibly with a
 cached prefix) and decode requests (one new token).  As the concept chapter's
 section 4 puts it, prefill and decode are two stages of the same loop; here
 the requests ``[0, decode_from)`` of a batch go through ``attn_prefill`` and
-the requests ``[decode_from, B)`` through ``attn_decode``, back to back on
-one stream, writing disjoint row ranges of one packed output.
+the requests ``[decode_from, B)`` through ``attn_decode``, writing disjoint
+row ranges of one packed output and disjoint cache slots.  When a batch has
+both, the decode call runs on a side stream beside the prefill call (with a
+workspace of its own): the prefill part is bound by the tensor cores and the
+decode part by HBM, so each fills the other's idle units.
 """
 from __future__ import annotations
 
@@ -36,23 +39,40 @@ class DeviceStep:
     n_prefill_tokens: int
     max_seqlen: int
     max_cache_len: int            # largest cached length among decode requests
+    decode_workspace: torch.Tensor | None = None  # the decode part's own, when both parts are present
 
     def run(self, stream=None) -> None:
-        """Issue the step: prefill part then decode part (asynchronous)."""
+        """Issue the step (asynchronous): the prefill part, and the decode part
+        beside it on a side stream when both are present (joined back into
+        ``stream`` before this returns), else one after the other."""
         v = self.__dict__.get("_views")
         if v is None:  # the row ranges of the two parts, sliced once
             n = self.n_prefill_tokens
             v = (self.qkv[:n], self.out[:n], self.qkv[n:], self.out[n:])
             self.__dict__["_views"] = v
+        side = None
+        if self.kv_prefill is not None and self.kv_decode is not None and self.decode_workspace is not None:
+            main = stream if stream is not None else torch.cuda.current_stream(self.out.device)
+            side = self.__dict__.get("_side")
+            if side is None:
+                side = torch.cuda.Stream(self.out.device)
+                self.__dict__["_side"] = side
+            side.wait_stream(main)
         if self.kv_prefill is not None:
             attn.prefill(self.cfg, v[0], self.q_norm_w, self.k_norm_w, self.cu_seqlens, self.max_seqlen,
                          self.kv_prefill, v[1], self.workspace, stream)
         if self.kv_decode is not None:
+            ws = self.workspace if side is None else self.decode_workspace
             attn.decode(self.cfg, v[2], self.q_norm_w, self.k_norm_w, self.max_cache_len, self.kv_decode,
-                        v[3], self.workspace, stream)
+                        v[3], ws, stream if side is None else side)
+        if side is not None:
+            main.wait_stream(side)
 
     def status(self) -> int:
-        return attn.get_status(self.workspace)
+        st = attn.get_status(self.workspace)
+        if self.decode_workspace is not None:
+            st |= attn.get_status(self.decode_workspace)
+        return st
 
     def launches(self) -> int:
         """Kernels one run() launches."""
@@ -88,12 +108,13 @@ def upload(w, host: dict, device="cuda") -> DeviceStep:
     out = torch.zeros((N, w.num_q_heads * w.head_dim), dtype=torch.bfloat16, device=device)
     max_kv = max([c + n for c, n in zip(w.cache_lens, w.new_lens)] + [1])
     ws = attn.new_workspace(cfg, max(N, 1), max(w.batch, 1), max_kv, device)
+    ws_dec = attn.new_workspace(cfg, 1, w.batch - df, max_kv, device) if 0 < df < w.batch else None
     return DeviceStep(
         cfg=cfg, qkv=dev(host["qkv"]), q_norm_w=dev(host["q_norm_w"]), k_norm_w=dev(host["k_norm_w"]),
         cu_seqlens=dev(host["cu_seqlens"][:df + 1]), kv_prefill=kv_p, kv_decode=kv_d,
         k_cache=k_cache, v_cache=v_cache, cache_lens=cache_lens, out=out, workspace=ws, n_prefill_tokens=n_pre,
         max_seqlen=max(list(w.new_lens[:df]) + [0]),
-        max_cache_len=max(list(w.cache_lens[df:]) + [0]))
+        max_cache_len=max(list(w.cache_lens[df:]) + [0]), decode_workspace=ws_dec)
 
 
 @dataclasses.dataclass
