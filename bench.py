@@ -247,7 +247,9 @@ class Timed:
 
     def run(self, ev):
         """ev: list of 5 events: start, after prefill append, after prefill
-        attention, before the decode call, after it."""
+        attention, before the decode call, after it.  An absent part records
+        no events of its own (each record takes about 2 us of device time):
+        its slots are set to the event before it, so that part times 0."""
         ds, attn = self.ds, self.attn
         n = ds.n_prefill_tokens
         ev[0].record()
@@ -259,17 +261,15 @@ class Timed:
                                 ds.out[:n], ds.workspace)
             ev[2].record()
         else:
-            ev[1].record()
-            ev[2].record()
+            ev[1] = ev[2] = ev[0]
         if ds.kv_decode is not None:
-            ev[3].record()
+            ev[3] = ev[2]
             # the new tokens' K/V are appended inside the split kernel (one launch, two with a merge)
             attn.decode(ds.cfg, ds.qkv[n:], ds.q_norm_w, ds.k_norm_w, ds.max_cache_len, ds.kv_decode,
                         ds.out[n:], ds.workspace)
             ev[4].record()
         else:
-            ev[3].record()
-            ev[4].record()
+            ev[3] = ev[4] = ev[2]
 
 
 def measure(w, steps, warmup, device, torch, dist_on, page_size=0, kv_dtype="bf16"):
