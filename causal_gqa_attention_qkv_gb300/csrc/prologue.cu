@@ -6,7 +6,7 @@
 // head's last dimension and RoPE at each token's position (V is not rotated);
 // transformer-basics "Prefill vs Decode": the new K/V are appended to the
 // per-layer cache (past_key_values.update).  One pass: every (token, head)
-// vector of D bf16 values is read once with 16-byte loads by a group of D/8
+// vector of D bf16 values is read once with 16-byte loads by a group of D/16
 // lanes, reduced with warp shuffles, and written once.
 #include "kernels.cuh"
 
@@ -14,7 +14,7 @@ namespace gb300 {
 
 namespace {
 
-constexpr int kWarpsPerBlock = 8;  // one token per warp
+constexpr int kWarpsPerBlock = 8;  // each warp takes one run of (token, step) units
 constexpr int kThreads = kWarpsPerBlock * 32;
 #ifndef PROLOGUE_BATCH
 #define PROLOGUE_BATCH 6
