@@ -693,7 +693,10 @@ def measure_mixed(wm, args, device, torch, dist_on, peaks, peak_kind) -> dict:
     ms_per_step times the step as step.DeviceStep.run issues it, the decode
     rows on a side stream beside the chunks.  The roofline fraction adds the
     tensor-bound and the HBM-bound parts:
-    (chunk FLOPs / bf16 peak + decode bytes / HBM peak) / step time."""
+    (chunk FLOPs / bf16 peak + decode bytes / HBM peak) / step time, the
+    bound of the parts run one after the other; the overlapped fraction
+    takes the larger of the two instead, the bound of the parts side by
+    side."""
     mm = measure(wm, args.steps, args.warmup, device, torch, dist_on, args.page_size)
     ms = mm["ms"]
     # the step as step.DeviceStep.run issues it: the decode rows on a side
@@ -724,6 +727,8 @@ def measure_mixed(wm, args, device, torch, dist_on, peaks, peak_kind) -> dict:
         "workload": wm.name, "ms_per_step": round(step_ms, 4), "serial_ms_per_step": round(serial_ms, 4),
         "chunk_flops": fl, "decode_bytes": nb,
         "roofline_frac": round(ideal_s / (step_ms * 1e-3), 4),
+        # with the parts overlapped the bound is the larger of the two, not their sum
+        "roofline_frac_overlapped": round(max(fl / peak_t, nb / hbm) / (step_ms * 1e-3), 4),
         "roofline_peaks": f"bf16_tflops and hbm_gbs ({peak_kind})",
         "parts_ms": {"chunk_prepare": round(pp, 4), "chunk_attention": round(pa, 4),
                      "decode_rows": round(dd, 4)},

@@ -40,6 +40,7 @@ class DeviceStep:
     max_seqlen: int
     max_cache_len: int            # largest cached length among decode requests
     decode_workspace: torch.Tensor | None = None  # the decode part's own, when both parts are present
+    side_stream: torch.cuda.Stream | None = None  # where the decode part runs then
 
     def run(self, stream=None) -> None:
         """Issue the step (asynchronous): the prefill part, and the decode part
@@ -51,12 +52,9 @@ class DeviceStep:
             v = (self.qkv[:n], self.out[:n], self.qkv[n:], self.out[n:])
             self.__dict__["_views"] = v
         side = None
-        if self.kv_prefill is not None and self.kv_decode is not None and self.decode_workspace is not None:
+        if self.kv_prefill is not None and self.kv_decode is not None and self.side_stream is not None:
             main = stream if stream is not None else torch.cuda.current_stream(self.out.device)
-            side = self.__dict__.get("_side")
-            if side is None:
-                side = torch.cuda.Stream(self.out.device)
-                self.__dict__["_side"] = side
+            side = self.side_stream
             side.wait_stream(main)
         if self.kv_prefill is not None:
             attn.prefill(self.cfg, v[0], self.q_norm_w, self.k_norm_w, self.cu_seqlens, self.max_seqlen,
@@ -108,13 +106,15 @@ def upload(w, host: dict, device="cuda") -> DeviceStep:
     out = torch.zeros((N, w.num_q_heads * w.head_dim), dtype=torch.bfloat16, device=device)
     max_kv = max([c + n for c, n in zip(w.cache_lens, w.new_lens)] + [1])
     ws = attn.new_workspace(cfg, max(N, 1), max(w.batch, 1), max_kv, device)
-    ws_dec = attn.new_workspace(cfg, 1, w.batch - df, max_kv, device) if 0 < df < w.batch else None
+    both = 0 < df < w.batch
+    ws_dec = attn.new_workspace(cfg, 1, w.batch - df, max_kv, device) if both else None
+    side = torch.cuda.Stream(out.device) if both else None
     return DeviceStep(
         cfg=cfg, qkv=dev(host["qkv"]), q_norm_w=dev(host["q_norm_w"]), k_norm_w=dev(host["k_norm_w"]),
         cu_seqlens=dev(host["cu_seqlens"][:df + 1]), kv_prefill=kv_p, kv_decode=kv_d,
         k_cache=k_cache, v_cache=v_cache, cache_lens=cache_lens, out=out, workspace=ws, n_prefill_tokens=n_pre,
         max_seqlen=max(list(w.new_lens[:df]) + [0]),
-        max_cache_len=max(list(w.cache_lens[df:]) + [0]), decode_workspace=ws_dec)
+        max_cache_len=max(list(w.cache_lens[df:]) + [0]), decode_workspace=ws_dec, side_stream=side)
 
 
 @dataclasses.dataclass
